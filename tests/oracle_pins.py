@@ -1,0 +1,291 @@
+"""Pins of the CPU oracle against things other than itself.
+
+Each ``check_*`` takes the oracle module and raises AssertionError when it
+disagrees with a closed form, a library routine, a printed format point, an
+invariant or a brute-force search. ``tests/test_oracle_pins.py`` runs them
+on the oracle; ``tests/test_oracle_mutations.py`` runs them on copies of the
+oracle with one planted mistake each and requires some check to fail.
+"""
+
+from __future__ import annotations
+
+import math
+import pathlib
+
+import numpy as np
+
+GOLDEN = pathlib.Path(__file__).parent / "golden"
+E_STAR = 4096.0
+
+
+def _bf16_bits(v) -> np.ndarray:
+    """Exact bf16 bit patterns of values that are bf16 already."""
+    v32 = np.asarray(v, dtype=np.float32)
+    u = v32.view(np.uint32)
+    assert np.all((u & 0xFFFF) == 0), "value is not a bf16 number"
+    return (u >> 16).astype(np.uint16)
+
+
+def _random_bf16(rng, shape, scale=1.0):
+    """Random bf16 bit patterns (truncation of fp32 normals; input only)."""
+    v = (rng.standard_normal(shape) * scale).astype(np.float32)
+    return (v.view(np.uint32) >> 16).astype(np.uint16)
+
+
+# --------------------------------------------------------------------------
+# Hadamard
+# --------------------------------------------------------------------------
+def check_hadamard_orthogonal(O):
+    for k in range(0, 9):
+        n = 1 << k
+        H = O.sylvester_hadamard(n)
+        assert np.array_equal(H @ H.T, n * np.eye(n, dtype=H.dtype)), n
+
+
+def check_hadamard_scipy(O):
+    scipy_linalg = __import__("scipy.linalg", fromlist=["hadamard"])
+    for n in (1, 2, 4, 64, 128, 256):
+        assert np.array_equal(O.sylvester_hadamard(n), scipy_linalg.hadamard(n)), n
+
+
+def check_hadamard_closed_form(O):
+    n = 256
+    i = np.arange(n)[:, None]
+    j = np.arange(n)[None, :]
+    pop = np.vectorize(lambda v: bin(int(v)).count("1"))(i & j)
+    assert np.array_equal(O.sylvester_hadamard(n), np.where(pop % 2 == 0, 1, -1))
+
+
+# --------------------------------------------------------------------------
+# E4M3 codec
+# --------------------------------------------------------------------------
+def check_e4m3_decode_torch(O):
+    import torch
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = O.e4m3_decode_table()
+    assert np.array_equal(np.isnan(ref), np.isnan(got))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(ref[ok], got[ok])
+
+
+def _torch_e4m3_codes(v32: np.ndarray) -> np.ndarray:
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(v32, dtype=np.float32))
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def check_e4m3_encode_torch_all_bf16(O):
+    """Every bf16 pattern with |v| <= 448 against torch's float8_e4m3fn cast."""
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    v = (bits.astype(np.uint32) << 16).view(np.float32)
+    keep = np.isfinite(v) & (np.abs(v) <= 448.0)
+    v = v[keep]
+    assert np.array_equal(O.e4m3_encode(v), _torch_e4m3_codes(v))
+
+
+def check_e4m3_encode_torch_ties(O):
+    """Exact midpoints between neighbouring E4M3 values, and random fp32."""
+    table = O.e4m3_decode_table()[:127]
+    mids = ((table[:-1] + table[1:]) / 2).astype(np.float32)
+    assert np.array_equal(mids.astype(np.float64), (table[:-1] + table[1:]) / 2)
+    rng = np.random.default_rng(7)
+    rnd = (np.exp2(rng.uniform(-12, np.log2(448.0), 200_000))).astype(np.float32)
+    v = np.concatenate([mids, -mids, rnd, -rnd])
+    v = v[np.abs(v) <= 448.0]
+    assert np.array_equal(O.e4m3_encode(v), _torch_e4m3_codes(v))
+
+
+def check_e4m3_points(O):
+    for line in (GOLDEN / "e4m3_points.txt").read_text().splitlines():
+        line = line.split("#")[0].strip()
+        if not line:
+            continue
+        expr, code = line.split()
+        val = eval(expr, {"__builtins__": {}}, {"float": float})
+        got = int(O.e4m3_encode(np.array([val], dtype=np.float32))[0])
+        assert got == int(code, 16), (expr, hex(got), code)
+
+
+def check_e4m3_roundtrip(O):
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    vals = O.e4m3_decode(codes).astype(np.float32)
+    assert np.array_equal(O.e4m3_encode(vals), codes)
+
+
+# --------------------------------------------------------------------------
+# bf16 rounding of the reduced output
+# --------------------------------------------------------------------------
+def check_bf16_round_torch(O):
+    import torch
+    rng = np.random.default_rng(11)
+    u = rng.integers(0, 1 << 32, size=400_000, dtype=np.uint64).astype(np.uint32)
+    # include exact ties (low half 0x8000) and values near the top of the range
+    u[:50_000] = (u[:50_000] & 0xFFFF0000) | 0x8000
+    u[50_000:51_000] = 0x7F7F0000 + rng.integers(0, 0x10000, 1000).astype(np.uint32)
+    v = u.view(np.float32)
+    v = v[np.isfinite(v)]
+    ref = torch.from_numpy(v.copy()).to(torch.bfloat16).to(torch.float64).numpy()
+    got = O.round_to_bf16(v.astype(np.float64))
+    assert np.array_equal(ref, got)
+
+
+def check_bf16_round_bruteforce_f64(O):
+    """fp64 inputs that fp32 cannot hold: nearest of the two bf16 neighbours."""
+    rng = np.random.default_rng(12)
+    v = rng.standard_normal(20_000) * np.exp2(rng.uniform(-30, 30, 20_000))
+    got = O.round_to_bf16(v)
+    for x, g in zip(v[:4000], got[:4000]):
+        t = np.float32(x)
+        b = int(np.array([t]).view(np.uint32)[0]) >> 16           # a nearby bf16 pattern
+        cands = []
+        for d in (-2, -1, 0, 1, 2):
+            bb = (b + d) & 0xFFFF
+            cv = float(np.array([bb << 16], dtype=np.uint32).view(np.float32)[0])
+            if math.isfinite(cv):
+                cands.append((abs(cv - x), bb & 1, cv))
+        cands.sort()
+        best = cands[0]
+        if len(cands) > 1 and cands[1][0] == best[0]:                # tie: even pattern
+            best = min(cands[:2], key=lambda c: c[1])
+        assert g == best[2], (x, g, best)
+
+
+# --------------------------------------------------------------------------
+# Energy, rotation and the dual scale
+# --------------------------------------------------------------------------
+def check_energy_invariant(O):
+    rng = np.random.default_rng(3)
+    for n in (64, 128, 256):
+        for scale in (1e-4, 1e-2, 3.0):
+            x = _random_bf16(rng, (16, 4 * n), scale)
+            st = O.compress_stages(x, n, E_STAR)
+            xb = O.bf16_bits_to_f64(x).reshape(16, 4, n)
+            a = st["alpha"].astype(np.float64)[..., None]
+            e_after = np.mean((a * xb) ** 2, axis=-1)
+            assert np.allclose(e_after, E_STAR, rtol=3e-7, atol=0), (n, scale)
+            # the rotated block keeps that energy: sum y^2 = n E*
+            y = st["y"].astype(np.float64)
+            assert np.allclose(np.sum(y * y, axis=-1), n * E_STAR, rtol=2e-6), (n, scale)
+
+
+def check_dual_scale_guard(O):
+    rng = np.random.default_rng(4)
+    for n in (64, 128, 256):
+        x = _random_bf16(rng, (64, 2 * n), 0.01)
+        # make some blocks concentrated (a Hadamard row times a constant)
+        x[:8, :n] = _bf16_bits(np.full(n, 0.5, dtype=np.float32))
+        st = O.compress_stages(x, n, E_STAR)
+        s = st["s"].astype(np.float64)
+        assert np.all(s >= 1.0)
+        clamped = st["amax"] > 448.0
+        assert np.array_equal(s > 1.0, clamped)
+        assert np.allclose(s[clamped], st["amax"][clamped] / 448.0, rtol=1e-7)
+        assert np.all(np.abs(O.e4m3_decode(st["codes"])) <= 448.0)
+        assert st["header"]["n_clamped"] == int(clamped.sum()) >= 8
+        assert st["header"]["s_max"] == float(s.max())
+
+
+def _closed_form_rows():
+    for line in (GOLDEN / "closed_form_blocks.txt").read_text().splitlines():
+        line = line.split("#")[0].strip()
+        if line:
+            n, case, alpha_c, s, code = line.split()
+            yield int(n), case, float(alpha_c), float(s), int(code, 16)
+
+
+def check_spike_and_constant_blocks(O):
+    rng = np.random.default_rng(5)
+    for n, case, alpha_c, s_ref, code in _closed_form_rows():
+        H = O.sylvester_hadamard(n)
+        for c in (0.0078125, -3.5, 0.001220703125):
+            cb = float(np.float32(c))
+            xv = np.zeros(n, dtype=np.float32)
+            if case == "spike":
+                j = int(rng.integers(n))
+                xv[j] = cb
+                sign = np.sign(cb) * H[:, j]
+                want = np.where(sign > 0, code, code | 0x80)
+            else:
+                xv[:] = cb
+                want = np.zeros(n, dtype=np.int64)
+                want[0] = code if cb > 0 else code | 0x80
+            x = _bf16_bits(xv)[None, :]
+            codes, alpha, s, hdr = O.compress(x, n, E_STAR)
+            assert math.isclose(float(alpha[0, 0]) * abs(cb), alpha_c, rel_tol=2e-7), (n, case)
+            assert math.isclose(float(s[0, 0]), s_ref, rel_tol=2e-7), (n, case)
+            got = codes[0].astype(np.int64)
+            nonzero = want & 0x7F != 0
+            assert np.array_equal(got[nonzero], want[nonzero]), (n, case)
+            assert np.all(got[~nonzero] & 0x7F == 0), (n, case)
+            assert hdr["n_clamped"] == (1 if case == "constant" else 0)
+            # reconstruction is the input itself
+            rec = O.decompress_reduce(codes[None], alpha[None], s[None], n)
+            assert np.array_equal(rec, x), (n, case)
+
+
+def check_zero_block(O):
+    for n in (64, 128, 256):
+        x = np.zeros((2, 2 * n), dtype=np.uint16)
+        x[1, n:] = _bf16_bits(np.full(n, 2.0, np.float32))    # a non-zero neighbour
+        codes, alpha, s, _ = O.compress(x, n, E_STAR)
+        assert alpha[0, 0] == 1.0 and alpha[0, 1] == 1.0 and alpha[1, 0] == 1.0
+        assert s[0, 0] == 1.0 and s[1, 0] == 1.0
+        assert np.all(codes[0] & 0x7F == 0) and np.all(codes[1, :n] & 0x7F == 0)
+        rec = O.decompress_reduce(codes[None], alpha[None], s[None], n)
+        assert np.all(O.bf16_bits_to_f64(rec[0]) == 0.0)
+        assert np.all(O.bf16_bits_to_f64(rec[1, :n]) == 0.0)
+
+
+def check_absmax_variant(O):
+    rng = np.random.default_rng(6)
+    n = 128
+    x = _random_bf16(rng, (32, 4 * n), 0.02)
+    c1, _, s1, _ = O.compress(x, n, E_STAR, O.VARIANT_ABSMAX)
+    c2, _, _, _ = O.compress(x, n, 3.0, O.VARIANT_ABSMAX)
+    mag = np.abs(O.e4m3_decode(c1)).reshape(32, 4, n)
+    assert np.all(mag.max(axis=-1) == 448.0)          # the block maximum maps to Q_max
+    assert np.mean(c1 == c2) > 0.9999                 # alpha cancels from the codes
+
+
+# --------------------------------------------------------------------------
+# Decompress-reduce: sum in the rotated domain, invert once (linearity)
+# --------------------------------------------------------------------------
+def check_reduce_linearity(O):
+    scipy_linalg = __import__("scipy.linalg", fromlist=["hadamard"])
+    rng = np.random.default_rng(8)
+    for n, P in ((64, 3), (128, 2), (256, 4)):
+        N, h = 8, 2 * n
+        K = h // n
+        codes = rng.integers(0, 256, size=(P, N, h)).astype(np.uint8)
+        codes[(codes & 0x7F) == 0x7F] = 0x11                      # no NaN codes
+        alpha = np.exp(rng.uniform(-3, 9, size=(P, N, K))).astype(np.float32)
+        s = np.maximum(1.0, np.exp(rng.normal(0, 0.5, size=(P, N, K)))).astype(np.float32)
+        table = O.e4m3_decode_table()
+        vals = table[codes].reshape(P, N, K, n)
+        z = np.sum((s.astype(np.float64) / alpha.astype(np.float64))[..., None] * vals, axis=0)
+        ref = (z @ scipy_linalg.hadamard(n).astype(np.float64)) / math.sqrt(n)
+        got = O.decompress_reduce_f64(codes, alpha, s, n).reshape(N, K, n)
+        assert np.allclose(got, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max()), (n, P)
+
+
+def check_roundtrip_error(O):
+    """One shard round trip: the error of a 3-bit-mantissa code, not more."""
+    rng = np.random.default_rng(9)
+    for n in (64, 128, 256):
+        x = _random_bf16(rng, (64, 4 * n), 0.01)
+        codes, alpha, s, _ = O.compress(x, n, E_STAR)
+        rec = O.bf16_bits_to_f64(O.decompress_reduce(codes[None], alpha[None], s[None], n))
+        ref = O.bf16_bits_to_f64(x)
+        rel = np.linalg.norm(rec - ref) / np.linalg.norm(ref)
+        assert 0.005 < rel < 0.04, (n, rel)
+
+
+def check_wire_ratio(O):
+    """FP8 codes plus two fp32 scales per block: near the pages' ~45% cut."""
+    for n in (64, 128, 256):
+        saving = 1.0 - O.wire_bytes_per_element(n) / 2.0
+        assert 0.40 < saving < 0.50, (n, saving)
+
+
+ALL_CHECKS = [v for k, v in sorted(globals().items()) if k.startswith("check_")]

@@ -1,0 +1,60 @@
+"""Plant one plausible mistake in a copy of the oracle; some pin must catch it.
+
+Each mutation edits one expression of the oracle's source (a dropped term, a
+wrong sign, an inverted ratio, a wrong tie rule ...), loads the edited copy
+as a separate module on the CPU and runs every pin against it.
+"""
+
+import importlib.util
+import pathlib
+
+import pytest
+
+import oracle_pins
+
+SRC = (pathlib.Path(__file__).resolve().parent.parent / "oracle" / "taco_oracle.py").read_text()
+
+MUTATIONS = {
+    "rotation_not_normalised": ("y = ((scaled @ H.T) / math.sqrt(n))", "y = ((scaled @ H.T) / 1.0)"),
+    "alpha_inverted": ("np.sqrt(target_energy / energy[nz])", "np.sqrt(energy[nz] / target_energy)"),
+    "energy_sum_not_mean": ("energy = np.sum(x * x, axis=-1) / n", "energy = np.sum(x * x, axis=-1)"),
+    "energy_centred": ("energy = np.sum(x * x, axis=-1) / n",
+                       "energy = np.var(x, axis=-1)"),
+    "no_overflow_floor": ("np.maximum(1.0, amax / Q_MAX)", "(amax / Q_MAX)"),
+    "qmax_wrong": ("Q_MAX = 448.0", "Q_MAX = 240.0"),
+    "hadamard_sign_moved": ("h = np.block([[h, h], [h, -h]])", "h = np.block([[h, -h], [h, h]])"),
+    "e4m3_ties_odd": ("(hi % 2 == 0)", "(hi % 2 == 1)"),
+    "e4m3_ties_away": ("((d_hi == d_lo) & (hi % 2 == 0))", "(d_hi == d_lo)"),
+    "e4m3_bias_8": ("2.0 ** (exp_field - 7)", "2.0 ** (exp_field - 8)"),
+    "e4m3_no_subnormal_scale": ("man_field * 2.0 ** -9", "man_field * 2.0 ** -10"),
+    "decode_forgets_s": ("w = np.asarray(s, dtype=np.float32).astype(np.float64)[..., None] * q",
+                         "w = q"),
+    "decode_forgets_alpha": ("xr = u / np.asarray(alpha, dtype=np.float32).astype(np.float64)[..., None]",
+                             "xr = u"),
+    "decode_not_normalised": ("u = (w @ H) / math.sqrt(n)", "u = (w @ H) / n"),
+    "bf16_truncates": ("np.rint(np.ldexp(v[finite], -q))", "np.trunc(np.ldexp(v[finite], -q))"),
+    "reduce_drops_last_shard": ("for p in range(P):", "for p in range(P - 1):"),
+}
+
+
+def _load_mutant(name, tmp_path):
+    old, new = MUTATIONS[name]
+    assert SRC.count(old) == 1, f"mutation anchor not unique/found: {old!r}"
+    path = tmp_path / f"oracle_mutant_{name}.py"
+    path.write_text(SRC.replace(old, new))
+    spec = importlib.util.spec_from_file_location(path.stem, path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistake_is_caught(name, tmp_path):
+    mod = _load_mutant(name, tmp_path)
+    failed = []
+    for check in oracle_pins.ALL_CHECKS:
+        try:
+            check(mod)
+        except (AssertionError, ValueError, IndexError, FloatingPointError):
+            failed.append(check.__name__)
+    assert failed, f"no pin caught the planted mistake {name}"
