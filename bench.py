@@ -1,0 +1,402 @@
+#!/usr/bin/env python
+"""Benchmark of the TACO fused compress + decompress-reduce hot path on GB300.
+
+One step = compress P bf16 shards [N, h] (one launch) + decompress-reduce
+P shards into bf16 [N, h] (one launch), the two kernels of the operator.
+The decompress-reduce input is the bundle compressed one buffer set later
+(the "received" bundle); buffer sets rotate so that every step reads data
+that left L2 long ago. Inputs are synthetic and already resident in HBM.
+
+value = bf16 bytes of the step's P input shards / step time (GB/s),
+summed over ranks for N > 1 (each rank its own data: weak scaling).
+
+--impl reference times the CPU oracle (numpy, fp64) on a bounded sample of
+the same workload on the host cores, rank 0 only.
+"""
+
+from __future__ import annotations
+
+import argparse
+import dataclasses
+import hashlib
+import json
+import math
+import os
+import pathlib
+import re
+import resource
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = pathlib.Path(__file__).resolve().parent
+METRIC = "compress / decompress-reduce GB/s (bf16 in) and % of GB300 HBM roofline"
+FALLBACK_HBM_GBS = 6800.0
+DEFAULT_TARGET_ENERGY = 4096.0
+
+
+# ------------------------------------------------------------- helpers ----
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["taco", "reference"], default="taco")
+    ap.add_argument("--workload", default=None, help="workload name (default: the GPT-2-1.5B activation)")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--cpu-baseline-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def job_throughput(bytes_per_rank_step: float, world: int, steps: int, max_ms: float) -> float:
+    """Whole-job GB/s: the bytes every rank processed over the slowest rank's time."""
+    return bytes_per_rank_step * world * steps / (max_ms * 1e-3) / 1e9
+
+
+def reduce_max_over_ranks(value: float, device=None) -> float:
+    """Max of a float over the ranks of the default process group (identity alone)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measured_peaks() -> dict:
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        try:
+            return json.loads(p.read_text())
+        except json.JSONDecodeError:
+            pass
+    return {}
+
+
+def source_hash() -> str:
+    """Hash of the CUDA sources: ties an ncu traffic figure to the kernel it measured."""
+    h = hashlib.sha256()
+    csrc = ROOT / "grads_taco_compress_gb300" / "csrc"
+    for f in sorted(csrc.glob("*")):
+        if f.suffix in (".cu", ".cuh", ".h"):
+            h.update(f.name.encode())
+            h.update(f.read_bytes())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """dram bytes per launch from the committed ncu summary, if it matches these sources."""
+    f = ROOT / "profiles" / f"{kernel}_{workload}.md"
+    if not f.exists():
+        return None
+    text = f.read_text()
+    mh = re.search(r"source_hash:\s*([0-9a-f]+)", text)
+    mt = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not mh or not mt or mh.group(1) != source_hash():
+        return None
+    return float(mt.group(1))
+
+
+# --------------------------------------------------------- clock sampler ----
+CLOCK_FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+                "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+                "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+
+def start_clock_sampler(uuid: str | None):
+    cmd = ["nvidia-smi", "--query-gpu=" + ",".join(CLOCK_FIELDS), "--format=csv,noheader,nounits",
+           "-lms", "20"]
+    if uuid:
+        cmd.insert(1, f"--id={uuid}")
+    try:
+        return subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+    except OSError:
+        return None
+
+
+def stop_clock_sampler(proc) -> dict:
+    if proc is None:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "note": "nvidia-smi unavailable"}
+    proc.terminate()
+    try:
+        out, _ = proc.communicate(timeout=5)
+    except subprocess.TimeoutExpired:
+        proc.kill()
+        out, _ = proc.communicate()
+    return parse_clock_samples(out)
+
+
+def parse_clock_samples(text: str) -> dict:
+    sm, smax, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in text.strip().splitlines():
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) != len(CLOCK_FIELDS):
+            continue
+        try:
+            sm.append(float(parts[0]))
+            smax.append(float(parts[1]))
+        except ValueError:
+            continue
+        for name, val in zip(names, parts[4:]):
+            if val.lower().startswith("active"):
+                reasons.add(name)
+    return {"sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(smax) if smax else None,
+            "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ CPU oracle ----
+def oracle_step(w, x_rows: np.ndarray) -> None:
+    """Oracle compress of P shards' rows and decompress-reduce of the result."""
+    from oracle import taco_oracle as O
+    parts = [O.compress(x_rows[p], w.block, DEFAULT_TARGET_ENERGY) for p in range(x_rows.shape[0])]
+    codes = np.stack([c for c, _, _, _ in parts])
+    alpha = np.stack([a for _, a, _, _ in parts])
+    s = np.stack([s_ for _, _, s_, _ in parts])
+    O.decompress_reduce(codes, alpha, s, w.block)
+
+
+def time_oracle(w, x: np.ndarray, rows: int, reps: int):
+    """Wall and CPU seconds of `reps` oracle steps over the first `rows` rows."""
+    xs = np.ascontiguousarray(x[:, :rows])
+    ru0 = resource.getrusage(resource.RUSAGE_SELF)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle_step(w, xs)
+    wall = time.perf_counter() - t0
+    ru1 = resource.getrusage(resource.RUSAGE_SELF)
+    cpu = (ru1.ru_utime - ru0.ru_utime) + (ru1.ru_stime - ru0.ru_stime)
+    return wall, cpu
+
+
+def cpu_baseline(w, x: np.ndarray, seconds: float) -> dict:
+    """The oracle, as it stands, on a bounded sample sized to about `seconds`."""
+    probe_rows = min(w.N, 16)
+    wall, _ = time_oracle(w, x, probe_rows, 1)
+    rows = int(min(w.N, max(probe_rows, probe_rows * seconds / max(wall, 1e-3))))
+    wall, cpu = time_oracle(w, x, rows, 1)
+    gbs = x.shape[0] * rows * w.h * 2 / wall / 1e9
+    return {"value": round(gbs, 6), "unit": "GB/s", "cores": max(1, math.ceil(cpu / wall - 0.05)),
+            "kind": "oracle",
+            "sample": f"{rows} of {w.N} rows of each of the {x.shape[0]} shards [{w.N},{w.h}] "
+                      f"(compress + decompress-reduce, numpy fp64), {wall:.1f} s wall, "
+                      f"{os.cpu_count()} host cores visible"}
+
+
+def run_reference(args, w) -> None:
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from grads_taco_compress_gb300 import workloads as W
+    x = W.make_shards(w)
+    # size each step so that warm-up + timed steps take about two minutes
+    probe_rows = min(w.N, 8)
+    wall, _ = time_oracle(w, x, probe_rows, 1)
+    per_row = wall / probe_rows
+    rows = int(max(1, min(w.N, 120.0 / max(args.steps + args.warmup, 1) / per_row)))
+    for _ in range(args.warmup):
+        time_oracle(w, x, rows, 1)
+    wall, cpu = time_oracle(w, x, rows, args.steps)
+    step_ms = wall / args.steps * 1e3
+    value = x.shape[0] * rows * w.h * 2 * args.steps / wall / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "shape": [w.N, w.h], "block": w.block, "P": w.P,
+                   "target_energy": DEFAULT_TARGET_ENERGY, "variant": "dual",
+                   "sample_rows_per_step": rows},
+        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s",
+                         "cores": max(1, math.ceil(cpu / wall - 0.05)), "kind": "oracle",
+                         "sample": f"{rows} of {w.N} rows of each of {x.shape[0]} shards per step"},
+        "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------- GPU arm ----
+def run_taco(args, w) -> None:
+    import torch
+    import torch.distributed as dist
+
+    import grads_taco_compress_gb300 as taco
+    from grads_taco_compress_gb300 import workloads as W
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    w = dataclasses.replace(w, seed=w.seed + rank)              # each rank its own batch
+    lib = taco.library()
+    stream = torch.cuda.current_stream()
+    sptr = stream.cuda_stream
+
+    P, N, h, n = w.P, w.N, w.h, w.block
+    K = h // n
+    x_host = W.make_shards(w)                                     # bf16 bits [P, N, h]
+    sb = taco.shard_bytes(N, h, n)
+    in_bytes = P * N * h * 2
+    set_bytes = in_bytes + P * sb + N * h * 2
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 129 * 2**20) or 129 * 2**20
+    R = max(3, math.ceil(3 * l2 / set_bytes))
+
+    x0 = torch.from_numpy(x_host.view(np.int16)).view(torch.bfloat16).to(dev)
+    xs = [x0] + [x0.clone() for _ in range(R - 1)]
+    bundles = [torch.empty((P, sb), dtype=torch.uint8, device=dev) for _ in range(R)]
+    headers = [torch.empty((P, taco.HEADER_BYTES), dtype=torch.uint8, device=dev) for _ in range(R)]
+    outs = [torch.empty((N, h), dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    ws = taco.new_workspace(P, dev)
+    wsb = ws.numel()
+    E = float(DEFAULT_TARGET_ENERGY)
+    xp = [t.data_ptr() for t in xs]
+    bp = [t.data_ptr() for t in bundles]
+    hp = [t.data_ptr() for t in headers]
+    op = [t.data_ptr() for t in outs]
+
+    def compress(k):
+        st = lib.taco_compress_shards(xp[k], P, N, h, n, E, 0, bp[k], hp[k], ws.data_ptr(), wsb, sptr)
+        if st:
+            raise taco.TacoError(st, "taco_compress_shards")
+
+    def decompress(k, src):
+        st = lib.taco_decompress_reduce(bp[src], P, N, h, n, op[k], sptr)
+        if st:
+            raise taco.TacoError(st, "taco_decompress_reduce")
+
+    for k in range(R):                                            # every bundle holds codes
+        compress(k)
+    for i in range(args.warmup):
+        compress(i % R)
+        decompress(i % R, (i + 1) % R)
+    torch.cuda.synchronize()
+
+    steps = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    uuid = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+    sampler = start_clock_sampler(f"GPU-{uuid}" if uuid else None)
+    time.sleep(0.3)                                               # let the sampler start
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(steps):
+        k = i % R
+        e = ev[i]
+        e[0].record(stream)
+        compress(k)
+        e[1].record(stream)
+        decompress(k, (k + 1) % R)
+        e[2].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = stop_clock_sampler(sampler)
+    local_ms = start.elapsed_time(end)
+    max_ms = reduce_max_over_ranks(local_ms, dev)
+    t_c = statistics.fmean(e[0].elapsed_time(e[1]) for e in ev) * 1e-3
+    t_d = statistics.fmean(e[1].elapsed_time(e[2]) for e in ev) * 1e-3
+
+    # ---- end to end through the public API, host buffers in and out ----
+    x_pin = torch.from_numpy(x_host.view(np.int16)).view(torch.bfloat16).pin_memory()
+    out_pin = torch.empty((N, h), dtype=torch.bfloat16).pin_memory()
+    e2e_steps = max(1, args.e2e_steps)
+
+    def e2e_step(k):
+        xs[k].copy_(x_pin, non_blocking=True)
+        taco.taco_compress_shards(xs[k], n, E, bundle=bundles[k], headers=headers[k], workspace=ws,
+                                  stream=stream)
+        taco.taco_decompress_reduce(bundles[k], P, N, h, n, out=outs[k], stream=stream)
+        out_pin.copy_(outs[k], non_blocking=True)
+
+    for i in range(3):
+        e2e_step(i % R)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(e2e_steps):
+        e2e_step(i % R)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max_over_ranks(e0.elapsed_time(e1), dev)
+
+    if rank == 0:
+        peaks = measured_peaks()
+        hbm = float(peaks.get("hbm_gbs") or FALLBACK_HBM_GBS)
+        peak_src = "measured" if peaks.get("hbm_gbs") else "fallback"
+        c_bytes = P * N * h * 3 + P * N * K * 8
+        d_bytes = P * N * h + P * N * K * 8 + N * h * 2
+        kern = {
+            "compress": {"us": round(t_c * 1e6, 3), "alg_bytes": c_bytes,
+                         "hbm_gbs": round(c_bytes / t_c / 1e9, 1),
+                         "bf16_in_gbs": round(in_bytes / t_c / 1e9, 1),
+                         "frac": round(c_bytes / t_c / 1e9 / hbm, 4)},
+            "decompress_reduce": {"us": round(t_d * 1e6, 3), "alg_bytes": d_bytes,
+                                  "hbm_gbs": round(d_bytes / t_d / 1e9, 1),
+                                  "bf16_in_gbs": round(in_bytes / t_d / 1e9, 1),
+                                  "frac": round(d_bytes / t_d / 1e9 / hbm, 4)},
+        }
+        dom = "compress" if t_c >= t_d else "decompress_reduce"
+        achieved = kern[dom]["hbm_gbs"]
+        line = {
+            "metric": METRIC,
+            "value": round(job_throughput(in_bytes, world, steps, max_ms), 3),
+            "unit": "GB/s",
+            "n_gpus": world, "steps": steps, "warmup": args.warmup,
+            "ms_per_step": round(max_ms / steps, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "shape": [N, h], "block": n, "P": P,
+                       "target_energy": E, "variant": "dual",
+                       "l2": f"inputs larger than L2: {R} rotating buffer sets of "
+                             f"{set_bytes / 1e6:.1f} MB ({R * set_bytes / 1e6:.0f} MB vs "
+                             f"{l2 / 1e6:.0f} MB L2)",
+                       "parallelism": f"{world} independent rank(s), no data-path collective"},
+            "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm,
+                         "peak_source": peak_src, "unit": "GB/s",
+                         "frac": round(achieved / hbm, 4),
+                         "traffic": profiled_traffic(dom, w.name)},
+            "kernels": kern,
+            "e2e": {"value": round(job_throughput(in_bytes, world, e2e_steps, e2e_ms), 3),
+                    "unit": "GB/s", "h2d_bytes_per_step": in_bytes,
+                    "d2h_bytes_per_step": N * h * 2, "steps": e2e_steps},
+            "gpu_launches": 2 * steps,
+            "clocks": clocks,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(w, x_host, args.cpu_baseline_seconds)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    sys.path.insert(0, str(ROOT))
+    from grads_taco_compress_gb300 import workloads as W
+    w = W.WORKLOADS[args.workload or W.BENCH_WORKLOAD]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_taco(args, w)
+
+
+if __name__ == "__main__":
+    main()

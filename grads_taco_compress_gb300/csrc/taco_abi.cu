@@ -1,0 +1,275 @@
+// C ABI of the TACO operator: argument checks, shard layout, grid sizing and
+// dispatch to the sm_103a kernels. Declarations and contracts are in taco.h.
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "taco_launch.h"
+
+namespace taco {
+
+cudaError_t launch_e4m3_encode(const float* in, uint8_t* out, int64_t n, cudaStream_t st);
+cudaError_t launch_e4m3_decode(const uint8_t* in, float* out, int64_t n, cudaStream_t st);
+
+namespace {
+
+constexpr int64_t kMaxElements = int64_t{1} << 40;   // per shard
+constexpr int kMaxDevices = 64;
+
+inline size_t pad256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+inline bool valid_block(int block) { return block == 64 || block == 128 || block == 256; }
+
+inline int block_index(int block) { return block == 64 ? 0 : (block == 128 ? 1 : 2); }
+
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+inline bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return na && nb && x < y + nb && y < x + na;
+}
+
+taco_status check_shape(int64_t N, int64_t h, int block) {
+  if (!valid_block(block)) return TACO_ERR_BLOCK;
+  if (N < 0 || h <= 0 || h % block != 0) return TACO_ERR_SHAPE;
+  if (N > 0 && N > kMaxElements / h) return TACO_ERR_SHAPE;
+  return TACO_OK;
+}
+
+// Per-device launch facts, filled once per device.
+struct DeviceInfo {
+  int sms = 0;
+  int occ_compress[3][2] = {};
+  int occ_decompress[3] = {};
+};
+
+std::once_flag g_once[kMaxDevices];
+DeviceInfo g_info[kMaxDevices];
+cudaError_t g_info_err[kMaxDevices];
+
+cudaError_t device_info(const DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::call_once(g_once[dev], [dev]() {
+    DeviceInfo& d = g_info[dev];
+    cudaError_t err = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    const int blocks[3] = {64, 128, 256};
+    for (int b = 0; b < 3 && err == cudaSuccess; ++b) {
+      for (int v = 0; v < 2 && err == cudaSuccess; ++v)
+        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &d.occ_compress[b][v], compress_kernel_ptr(blocks[b], v), kCompressThreads, 0);
+      if (err == cudaSuccess)
+        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &d.occ_decompress[b], decompress_kernel_ptr(blocks[b]), kDecompressThreads, 0);
+    }
+    g_info_err[dev] = err;
+  });
+  if (g_info_err[dev] != cudaSuccess) return g_info_err[dev];
+  *out = &g_info[dev];
+  return cudaSuccess;
+}
+
+struct Layout {
+  size_t alpha_off, s_off, bytes;
+};
+
+Layout shard_layout(int64_t N, int64_t h, int block) {
+  const size_t elems = static_cast<size_t>(N) * static_cast<size_t>(h);
+  const size_t nblk = elems / static_cast<size_t>(block);
+  Layout l;
+  l.alpha_off = pad256(elems);
+  l.s_off = l.alpha_off + pad256(4 * nblk);
+  l.bytes = l.s_off + pad256(4 * nblk);
+  return l;
+}
+
+taco_status decompress_common(const uint8_t* const* shards, int P, int64_t N, int64_t h,
+                              int block, void* out, void* stream) {
+  taco_status st = check_shape(N, h, block);
+  if (st != TACO_OK) return st;
+  if (P < 1 || P > TACO_MAX_SHARDS) return TACO_ERR_ARG;
+  if (N == 0) return TACO_OK;
+  if (!out) return TACO_ERR_NULL;
+  if (!aligned(out, 16)) return TACO_ERR_ALIGN;
+  const Layout l = shard_layout(N, h, block);
+  const size_t out_bytes = static_cast<size_t>(N) * static_cast<size_t>(h) * 2;
+  DecompressArgs a{};
+  for (int p = 0; p < P; ++p) {
+    if (!shards[p]) return TACO_ERR_NULL;
+    if (!aligned(shards[p], 16)) return TACO_ERR_ALIGN;
+    if (overlap(shards[p], l.bytes, out, out_bytes)) return TACO_ERR_ARG;
+    a.shard[p] = shards[p];
+  }
+  a.alpha_off = l.alpha_off;
+  a.s_off = l.s_off;
+  a.P = P;
+  a.nblocks = N * h / block;
+  a.out = static_cast<uint16_t*>(out);
+  a.inv_sqrt_n = static_cast<float>(1.0 / std::sqrt(static_cast<double>(block)));
+
+  const DeviceInfo* info = nullptr;
+  if (device_info(&info) != cudaSuccess) return TACO_ERR_CUDA;
+  const int64_t tiles = (a.nblocks + decompress_tile_blocks(block) - 1) / decompress_tile_blocks(block);
+  const int64_t needed = (tiles + kDecompressThreads / 32 - 1) / (kDecompressThreads / 32);
+  int64_t grid = static_cast<int64_t>(info->sms) * info->occ_decompress[block_index(block)];
+  if (grid > needed) grid = needed;
+  if (grid < 1) grid = 1;
+  if (launch_decompress(a, block, static_cast<int>(grid), static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return TACO_ERR_CUDA;
+  return TACO_OK;
+}
+
+}  // namespace
+}  // namespace taco
+
+using namespace taco;
+
+extern "C" {
+
+size_t taco_shard_bytes(int64_t N, int64_t h, int block) {
+  if (check_shape(N, h, block) != TACO_OK) return 0;
+  return shard_layout(N, h, block).bytes;
+}
+
+size_t taco_shard_alpha_offset(int64_t N, int64_t h, int block) {
+  if (check_shape(N, h, block) != TACO_OK) return 0;
+  return shard_layout(N, h, block).alpha_off;
+}
+
+size_t taco_shard_s_offset(int64_t N, int64_t h, int block) {
+  if (check_shape(N, h, block) != TACO_OK) return 0;
+  return shard_layout(N, h, block).s_off;
+}
+
+size_t taco_workspace_bytes(int P) {
+  if (P < 1 || P > TACO_MAX_SHARDS) return 0;
+  return static_cast<size_t>(P) * kWorkspaceShardStride;
+}
+
+taco_status taco_compress_shards(const void* x_bf16, int P, int64_t N, int64_t h, int block,
+                                 float target_energy, int variant, void* bundle_out,
+                                 taco_header* headers_out, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  taco_status st = check_shape(N, h, block);
+  if (st != TACO_OK) return st;
+  if (P < 1 || P > TACO_MAX_SHARDS) return TACO_ERR_ARG;
+  if (variant != TACO_VARIANT_DUAL && variant != TACO_VARIANT_ABSMAX) return TACO_ERR_ARG;
+  if (!(target_energy > 0.0f) || !std::isfinite(target_energy)) return TACO_ERR_ARG;
+  const double sqrt_nE = std::sqrt(static_cast<double>(block) * target_energy);
+  if (!(sqrt_nE < 3.0e38)) return TACO_ERR_ARG;
+  if (!headers_out) return TACO_ERR_NULL;
+  if (!workspace || workspace_bytes < taco_workspace_bytes(P)) return TACO_ERR_WORKSPACE;
+  if (!aligned(headers_out, 8) || !aligned(workspace, 16)) return TACO_ERR_ALIGN;
+  const Layout l = shard_layout(N, h, block);
+  const size_t in_bytes = static_cast<size_t>(P) * N * h * 2;
+  if (N > 0) {
+    if (!x_bf16 || !bundle_out) return TACO_ERR_NULL;
+    if (!aligned(x_bf16, 16) || !aligned(bundle_out, 16)) return TACO_ERR_ALIGN;
+    if (overlap(x_bf16, in_bytes, bundle_out, P * l.bytes)) return TACO_ERR_ARG;
+  }
+
+  CompressArgs a{};
+  a.x = static_cast<const uint16_t*>(x_bf16);
+  a.shard_elems = N * h;
+  a.nblocks = N * h / block;
+  a.bundle = static_cast<uint8_t*>(bundle_out);
+  a.shard_bytes = l.bytes;
+  a.alpha_off = l.alpha_off;
+  a.s_off = l.s_off;
+  a.headers = headers_out;
+  a.workspace = static_cast<uint8_t*>(workspace);
+  a.N = N;
+  a.h = h;
+  a.target_energy = target_energy;
+  a.sqrt_nE = static_cast<float>(sqrt_nE);
+  a.inv_sqrt_n = static_cast<float>(1.0 / std::sqrt(static_cast<double>(block)));
+
+  const DeviceInfo* info = nullptr;
+  if (device_info(&info) != cudaSuccess) return TACO_ERR_CUDA;
+  const int tb = compress_tile_blocks(block);
+  const int64_t tiles = (a.nblocks + tb - 1) / tb;
+  const int64_t needed = (tiles + kCompressThreads / 32 - 1) / (kCompressThreads / 32);
+  const int64_t total = static_cast<int64_t>(info->sms) * info->occ_compress[block_index(block)][variant];
+  int64_t gx = (total + P - 1) / P;
+  if (gx > needed) gx = needed;
+  if (gx > kMaxCtasPerShard) gx = kMaxCtasPerShard;
+  if (gx < 1) gx = 1;
+  if (launch_compress(a, block, variant, static_cast<int>(gx), P, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return TACO_ERR_CUDA;
+  return TACO_OK;
+}
+
+taco_status taco_compress(const void* x_bf16, int64_t N, int64_t h, int block, float target_energy,
+                          int variant, void* shard_out, taco_header* header_out, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  return taco_compress_shards(x_bf16, 1, N, h, block, target_energy, variant, shard_out,
+                              header_out, workspace, workspace_bytes, stream);
+}
+
+taco_status taco_decompress_reduce(const void* bundle, int P, int64_t N, int64_t h, int block,
+                                   void* out_bf16, void* stream) {
+  taco_status st = check_shape(N, h, block);
+  if (st != TACO_OK) return st;
+  if (P < 1 || P > TACO_MAX_SHARDS) return TACO_ERR_ARG;
+  if (N == 0) return TACO_OK;
+  if (!bundle) return TACO_ERR_NULL;
+  const size_t sb = shard_layout(N, h, block).bytes;
+  const uint8_t* ptrs[TACO_MAX_SHARDS];
+  for (int p = 0; p < P; ++p) ptrs[p] = static_cast<const uint8_t*>(bundle) + p * sb;
+  return decompress_common(ptrs, P, N, h, block, out_bf16, stream);
+}
+
+taco_status taco_decompress_reduce_ptrs(const void* const* shards, int P, int64_t N, int64_t h,
+                                        int block, void* out_bf16, void* stream) {
+  taco_status st = check_shape(N, h, block);
+  if (st != TACO_OK) return st;
+  if (P < 1 || P > TACO_MAX_SHARDS) return TACO_ERR_ARG;
+  if (N == 0) return TACO_OK;
+  if (!shards) return TACO_ERR_NULL;
+  const uint8_t* ptrs[TACO_MAX_SHARDS];
+  for (int p = 0; p < P; ++p) ptrs[p] = static_cast<const uint8_t*>(shards[p]);
+  return decompress_common(ptrs, P, N, h, block, out_bf16, stream);
+}
+
+taco_status taco_e4m3_encode_f32(const float* in, uint8_t* out, int64_t n, void* stream) {
+  if (n < 0) return TACO_ERR_SHAPE;
+  if (n == 0) return TACO_OK;
+  if (!in || !out) return TACO_ERR_NULL;
+  if (!aligned(in, 4)) return TACO_ERR_ALIGN;
+  return launch_e4m3_encode(in, out, n, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? TACO_OK
+             : TACO_ERR_CUDA;
+}
+
+taco_status taco_e4m3_decode_f32(const uint8_t* in, float* out, int64_t n, void* stream) {
+  if (n < 0) return TACO_ERR_SHAPE;
+  if (n == 0) return TACO_OK;
+  if (!in || !out) return TACO_ERR_NULL;
+  if (!aligned(out, 4)) return TACO_ERR_ALIGN;
+  return launch_e4m3_decode(in, out, n, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? TACO_OK
+             : TACO_ERR_CUDA;
+}
+
+const char* taco_status_string(taco_status s) {
+  switch (s) {
+    case TACO_OK: return "ok";
+    case TACO_ERR_NULL: return "null pointer";
+    case TACO_ERR_SHAPE: return "bad shape (N < 0, h <= 0, h % block != 0 or too large)";
+    case TACO_ERR_BLOCK: return "block size must be 64, 128 or 256";
+    case TACO_ERR_ALIGN: return "pointer not aligned (tensors and bundles need 16 bytes)";
+    case TACO_ERR_ARG: return "bad argument (target energy, P, variant or overlapping buffers)";
+    case TACO_ERR_CUDA: return "CUDA error";
+    case TACO_ERR_WORKSPACE: return "workspace missing or smaller than taco_workspace_bytes";
+  }
+  return "unknown status";
+}
+
+int taco_abi_version(void) { return TACO_ABI_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,165 @@
+/*
+ * taco.h - C ABI of the GB300 (sm_103a) TACO fused compression operator.
+ *
+ * The operator is the one described for tensor-parallel intermediate tensors
+ * in "TACO: Efficient Communication Compression of Intermediate Tensors for
+ * Scalable Tensor-Parallel LLM Training" (gist.science Portuguese summary,
+ * §2.B.1 "Adaptive Scale-Hadamard transform", §2.B.2 "Dual-Scale
+ * quantization", §2.B.3 "fused operator" and "two-shot AllReduce"):
+ *
+ *   compress, per block of n contiguous elements of a row (n = 64, 128, 256):
+ *     E      = mean of x^2 over the block            (raw second moment)
+ *     alpha  = sqrt(E* / E)      (1 when E == 0)      (pre-rotation scale)
+ *     y      = (H_n / sqrt(n)) (alpha x)              (Sylvester Hadamard)
+ *     s      = max(1, max|y| / 448)                   (post-rotation scale)
+ *     q      = E4M3(y / s)   round-to-nearest-even, saturating at +-448
+ *   decompress-reduce, over P shards compressed with the same n:
+ *     x_hat  = bf16( sum_p (1/alpha_p) (H_n / sqrt(n)) (s_p dec(q_p)) )
+ *
+ * Conventions of every entry point:
+ *   - All buffers are device memory owned by the caller. The library never
+ *     allocates, frees or synchronises; work is enqueued on `stream`
+ *     (a cudaStream_t; NULL is the legacy default stream) of the device that
+ *     is current on the calling thread.
+ *   - Arguments are checked on the host before anything is enqueued. On any
+ *     error nothing is launched and nothing is written.
+ *   - A launch failure is reported as TACO_ERR_CUDA (from cudaGetLastError).
+ *   - bf16 tensors are row-major [N, h] with h % n == 0; a block is n
+ *     contiguous elements of one row, block b = row * (h/n) + column / n.
+ */
+#ifndef TACO_H_
+#define TACO_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum taco_status {
+  TACO_OK = 0,
+  TACO_ERR_NULL = 1,       /* a required pointer is NULL                       */
+  TACO_ERR_SHAPE = 2,      /* N < 0, h <= 0, h % block != 0, or N*h too large  */
+  TACO_ERR_BLOCK = 3,      /* block is not 64, 128 or 256                      */
+  TACO_ERR_ALIGN = 4,      /* a tensor or bundle pointer is not 16-byte aligned */
+  TACO_ERR_ARG = 5,        /* target energy not finite and > 0, P out of
+                              [1, TACO_MAX_SHARDS], unknown variant            */
+  TACO_ERR_CUDA = 6,       /* a CUDA call or launch failed                     */
+  TACO_ERR_WORKSPACE = 7   /* workspace NULL or smaller than taco_workspace_bytes */
+} taco_status;
+
+/* Dual-scale variants. DUAL is the operator above. ABSMAX replaces the
+ * overflow guard by s = max|y| / 448 (1 for an all-zero block); alpha then
+ * cancels from the codes. It is kept for error studies. */
+enum { TACO_VARIANT_DUAL = 0, TACO_VARIANT_ABSMAX = 1 };
+
+#define TACO_MAX_SHARDS 16
+#define TACO_Q_MAX 448.0f
+#define TACO_ABI_VERSION 1
+
+/* Per-tensor header written by the compress kernel (one per shard).
+ * s_max = max over blocks of s (0 for an empty tensor); n_clamped = number of
+ * blocks with s > 1. This is the per-tensor part of the dual scale: the
+ * "per-tensor scale adapted to the dynamic range" of the euno.news rewrite
+ * ("Adaptive Scale-Hadamard Transform" in its Methodology), kept as a
+ * summary, not applied to the codes. */
+typedef struct taco_header {
+  int64_t N;
+  int64_t h;
+  int32_t block;
+  int32_t variant;
+  float target_energy;
+  float q_max;
+  float s_max;
+  uint32_t n_clamped;
+} taco_header; /* 40 bytes */
+
+/* ---- Shard layout -------------------------------------------------------
+ * One compressed tensor ("shard") is one contiguous byte range:
+ *   [codes: N*h bytes, E4M3, row-major][pad to 256]
+ *   [alpha: N*(h/n) fp32, block order][pad to 256]
+ *   [s:     N*(h/n) fp32, block order][pad to 256]
+ * A bundle is P shards back to back, shard p at p * taco_shard_bytes(...);
+ * it is the receive buffer of the ReduceScatter half of the two-shot
+ * AllReduce (TACO pt summary, §2.B.3). Every part starts 256-byte aligned
+ * relative to the shard start. Returns 0 for invalid arguments. */
+size_t taco_shard_bytes(int64_t N, int64_t h, int block);
+size_t taco_shard_alpha_offset(int64_t N, int64_t h, int block);
+size_t taco_shard_s_offset(int64_t N, int64_t h, int block);
+
+/* Bytes of device workspace that compress needs for P shards. The
+ * workspace holds per-CTA partial maxima and arrival counters used to write
+ * the per-tensor header in the same launch. It must be zero-filled before
+ * its first use; each call leaves it zero-filled again. Calls that share a
+ * workspace must not overlap on the GPU (use one workspace per stream). */
+size_t taco_workspace_bytes(int P);
+
+/* ---- taco_compress ------------------------------------------------------
+ * Compress one bf16 tensor x [N, h] (device, 16-byte aligned) into one
+ * shard at `shard_out` (device, 16-byte aligned, taco_shard_bytes(N,h,block)
+ * bytes) and its header at `header_out` (device, 8-byte aligned).
+ *   block          n, one of 64, 128, 256
+ *   target_energy  E* > 0, the per-element energy of every rescaled block
+ *                  (TACO pt summary §2.B.1: "normalise the energy to a
+ *                  target level"); 4096 puts the rotated RMS at 64 code units
+ *   variant        TACO_VARIANT_DUAL or TACO_VARIANT_ABSMAX
+ * N == 0 is valid: no code is written and the header reports s_max = 0. */
+taco_status taco_compress(const void* x_bf16, int64_t N, int64_t h, int block,
+                          float target_energy, int variant, void* shard_out,
+                          taco_header* header_out, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
+/* ---- taco_compress_shards -----------------------------------------------
+ * The same for P tensors x [P, N, h] (contiguous) in one launch: shard p of
+ * the bundle at `bundle_out` (P * taco_shard_bytes bytes) and header p of
+ * `headers_out` [P]. 1 <= P <= TACO_MAX_SHARDS. These are the P chunks one
+ * rank compresses before the ReduceScatter (TACO pt summary §2.B.3). */
+taco_status taco_compress_shards(const void* x_bf16, int P, int64_t N, int64_t h,
+                                 int block, float target_energy, int variant,
+                                 void* bundle_out, taco_header* headers_out,
+                                 void* workspace, size_t workspace_bytes,
+                                 void* stream);
+
+/* ---- taco_decompress_reduce ---------------------------------------------
+ * Reconstruct and sum P shards of one bundle (device, 16-byte aligned, the
+ * layout above, all compressed from [N, h] tensors with the same block)
+ * into bf16 out [N, h] (device, 16-byte aligned). The P reconstructions are
+ * summed in fp32 in the rotated domain and rotated back once (the rotation is
+ * linear and shared by all shards), then rounded to bf16 once. This is the
+ * reconstruction of TACO pt summary §2.B.2 fused with the reduce of the
+ * ReduceScatter step of §2.B.3. 1 <= P <= TACO_MAX_SHARDS. N == 0 is valid
+ * and launches nothing. `out` must not overlap the bundle. */
+taco_status taco_decompress_reduce(const void* bundle, int P, int64_t N, int64_t h,
+                                   int block, void* out_bf16, void* stream);
+
+/* ---- taco_decompress_reduce_ptrs ----------------------------------------
+ * As taco_decompress_reduce, with the P shards in P separate buffers
+ * (`shards[p]` a device pointer to one shard, 16-byte aligned; `shards` itself
+ * is a host array of P pointers, read before the call returns). This is the
+ * form a receive step that lands each peer's chunk in its own buffer uses. */
+taco_status taco_decompress_reduce_ptrs(const void* const* shards, int P, int64_t N,
+                                        int64_t h, int block, void* out_bf16,
+                                        void* stream);
+
+/* ---- E4M3 codec ----------------------------------------------------------
+ * Elementwise conversions with the instructions the operator's kernels use
+ * (TACO pt summary §2.A: FP8 E4M3 instead of INT8). `in` and `out` are device
+ * arrays of n elements; n == 0 launches nothing.
+ *   taco_e4m3_encode_f32: fp32 -> E4M3 code, round to nearest even, |v| > 448
+ *                         and +-inf saturate to +-448, NaN -> 0x7F.
+ *   taco_e4m3_decode_f32: E4M3 code -> its exact fp32 value (0x7F/0xFF: NaN). */
+taco_status taco_e4m3_encode_f32(const float* in, uint8_t* out, int64_t n, void* stream);
+taco_status taco_e4m3_decode_f32(const uint8_t* in, float* out, int64_t n, void* stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* taco_status_string(taco_status status);
+
+/* TACO_ABI_VERSION of the loaded library. */
+int taco_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TACO_H_ */

@@ -1,0 +1,150 @@
+"""The C ABI without a GPU: exports, layout, and host-side argument checks.
+
+Every call below is rejected by the host checks before any CUDA call, so the
+fake addresses are never dereferenced; no case here reaches a launch.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import pathlib
+import re
+
+import pytest
+import torch
+
+from grads_taco_compress_gb300 import binding as tb
+
+# Fake addresses are only safe where no kernel could ever be launched.
+no_gpu_only = pytest.mark.skipif(torch.cuda.is_available(),
+                                 reason="fake-address host checks run on machines without a GPU")
+
+ROOT = pathlib.Path(__file__).resolve().parent.parent
+OK, NULL, SHAPE, BLOCK, ALIGN, ARG, CUDA, WS = range(8)
+A = 0x10000          # a 256-byte aligned fake device address
+WSB = 16 * 16400     # larger than any workspace the library asks for
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not tb.LIB_PATH.exists():
+        from grads_taco_compress_gb300 import build_lib
+        build_lib.build()
+    return tb.library()
+
+
+def _declared_functions():
+    text = (ROOT / "include" / "taco.h").read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(taco_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _declared_functions()
+    assert declared, "no declarations found"
+    assert sorted(tb.EXPORTED_SYMBOLS) == declared
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert lib.taco_abi_version() == 1
+
+
+def test_shard_layout(lib):
+    def pad(v):
+        return (v + 255) // 256 * 256
+    for N, h, n in [(512, 1024, 128), (8192, 1600, 64), (16384, 3584, 128), (1, 64, 64), (3, 768, 256),
+                    (0, 256, 128)]:
+        K = h // n
+        a = pad(N * h)
+        s = a + pad(4 * N * K)
+        assert lib.taco_shard_alpha_offset(N, h, n) == a
+        assert lib.taco_shard_s_offset(N, h, n) == s
+        assert lib.taco_shard_bytes(N, h, n) == s + pad(4 * N * K)
+    for N, h, n in [(4, 100, 64), (4, 128, 100), (-1, 128, 64), (4, 0, 64)]:
+        assert lib.taco_shard_bytes(N, h, n) == 0
+    assert lib.taco_workspace_bytes(0) == 0 and lib.taco_workspace_bytes(17) == 0
+    assert 0 < lib.taco_workspace_bytes(1) < lib.taco_workspace_bytes(16) <= WSB
+
+
+def _compress(lib, x=A, P=1, N=4, h=256, block=128, E=4096.0, variant=0, bundle=A * 64,
+              headers=A * 128, ws=A * 256, wsb=WSB):
+    return lib.taco_compress_shards(x, P, N, h, block, E, variant, bundle, headers, ws, wsb, None)
+
+
+@no_gpu_only
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(block=100), BLOCK), (dict(block=32), BLOCK), (dict(block=512), BLOCK),
+    (dict(h=130, block=64), SHAPE), (dict(N=-1), SHAPE), (dict(h=0), SHAPE),
+    (dict(N=1 << 34, h=1 << 10), SHAPE),
+    (dict(P=0), ARG), (dict(P=17), ARG), (dict(variant=2), ARG), (dict(variant=-1), ARG),
+    (dict(E=0.0), ARG), (dict(E=-1.0), ARG), (dict(E=float("nan")), ARG),
+    (dict(E=float("inf")), ARG),
+    (dict(headers=None), NULL), (dict(ws=None), WS), (dict(wsb=100), WS),
+    (dict(x=None), NULL), (dict(bundle=None), NULL),
+    (dict(x=A + 8), ALIGN), (dict(bundle=A * 64 + 4), ALIGN), (dict(headers=A * 128 + 4), ALIGN),
+    (dict(ws=A * 256 + 8), ALIGN),
+    (dict(x=A, bundle=A + 64), ARG),                  # input and output overlap
+])
+def test_compress_rejects(lib, kwargs, status):
+    assert status not in (OK, CUDA)
+    assert _compress(lib, **kwargs) == status
+
+
+@no_gpu_only
+def test_single_compress_rejects(lib):
+    assert lib.taco_compress(A, 4, 256, 100, 4096.0, 0, A * 64, A * 128, A * 256, WSB, None) == BLOCK
+    assert lib.taco_compress(A + 2, 4, 256, 128, 4096.0, 0, A * 64, A * 128, A * 256, WSB, None) == ALIGN
+
+
+def _decompress(lib, bundle=A, P=2, N=4, h=256, block=128, out=A * 1024):
+    return lib.taco_decompress_reduce(bundle, P, N, h, block, out, None)
+
+
+@no_gpu_only
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(block=96), BLOCK), (dict(h=200, block=64), SHAPE), (dict(N=-3), SHAPE),
+    (dict(P=0), ARG), (dict(P=17), ARG), (dict(bundle=None), NULL), (dict(out=None), NULL),
+    (dict(out=A * 1024 + 2), ALIGN), (dict(bundle=A + 8), ALIGN),
+    (dict(bundle=A, out=A + 512), ARG),               # output inside the bundle
+])
+def test_decompress_rejects(lib, kwargs, status):
+    assert _decompress(lib, **kwargs) == status
+
+
+@no_gpu_only
+def test_decompress_empty_is_ok_without_launch(lib):
+    # N == 0 returns before any device work, even with no buffers at all
+    assert _decompress(lib, bundle=None, N=0, out=None) == OK
+
+
+@no_gpu_only
+def test_decompress_ptrs_rejects(lib):
+    arr = (ctypes.c_void_p * 3)(A, A * 64, None)
+    assert lib.taco_decompress_reduce_ptrs(arr, 3, 4, 256, 128, A * 1024, None) == NULL
+    arr = (ctypes.c_void_p * 2)(A, A * 64 + 8)
+    assert lib.taco_decompress_reduce_ptrs(arr, 2, 4, 256, 128, A * 1024, None) == ALIGN
+    assert lib.taco_decompress_reduce_ptrs(None, 2, 4, 256, 128, A * 1024, None) == NULL
+    arr = (ctypes.c_void_p * 2)(A, A * 64)
+    assert lib.taco_decompress_reduce_ptrs(arr, 0, 4, 256, 128, A * 1024, None) == ARG
+
+
+@no_gpu_only
+def test_codec_rejects(lib):
+    assert lib.taco_e4m3_encode_f32(A, A * 8, -1, None) == SHAPE
+    assert lib.taco_e4m3_encode_f32(None, A * 8, 10, None) == NULL
+    assert lib.taco_e4m3_encode_f32(A + 2, A * 8, 10, None) == ALIGN
+    assert lib.taco_e4m3_decode_f32(A, None, 10, None) == NULL
+    assert lib.taco_e4m3_decode_f32(A, A * 8 + 1, 10, None) == ALIGN
+    assert lib.taco_e4m3_encode_f32(None, None, 0, None) == OK
+
+
+def test_status_strings(lib):
+    for s in range(8):
+        assert lib.taco_status_string(s)
+    assert b"unknown" in lib.taco_status_string(99)
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(tb, "LIB_PATH", tmp_path / "missing.so")
+    monkeypatch.setattr(tb, "_LIB", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        tb.shard_bytes(4, 256, 128)
