@@ -36,6 +36,7 @@ assert HEADER_DTYPE.itemsize == HEADER_BYTES
 EXPORTED_SYMBOLS = (
     "taco_shard_bytes", "taco_shard_alpha_offset", "taco_shard_s_offset",
     "taco_workspace_bytes", "taco_compress", "taco_compress_shards",
+    "taco_compress_shards_noalloc",
     "taco_decompress_reduce", "taco_decompress_reduce_ptrs",
     "taco_e4m3_encode_f32", "taco_e4m3_decode_f32",
     "taco_status_string", "taco_abi_version",
@@ -69,6 +70,7 @@ def _lib() -> ctypes.CDLL:
             "taco_workspace_bytes": (sz, [i32]),
             "taco_compress": (i32, [vp, i64, i64, i32, f32, i32, vp, vp, vp, sz, vp]),
             "taco_compress_shards": (i32, [vp, i32, i64, i64, i32, f32, i32, vp, vp, vp, sz, vp]),
+            "taco_compress_shards_noalloc": (i32, [vp, i32, i64, i64, i32, f32, i32, vp, vp, vp]),
             "taco_decompress_reduce": (i32, [vp, i32, i64, i64, i32, vp, vp]),
             "taco_decompress_reduce_ptrs": (i32, [ctypes.POINTER(vp), i32, i64, i64, i32, vp, vp]),
             "taco_e4m3_encode_f32": (i32, [vp, vp, i64, vp]),
@@ -163,6 +165,29 @@ def taco_compress_shards(x: torch.Tensor, block: int, target_energy: float = DEF
                                      _ptr(bundle), _ptr(headers), _ptr(workspace),
                                      workspace.numel(), _stream_ptr(stream))
     _check(st, "taco_compress_shards")
+    return bundle, headers
+
+
+def taco_compress_shards_noalloc(x: torch.Tensor, block: int,
+                                 target_energy: float = DEFAULT_TARGET_ENERGY,
+                                 variant: int = VARIANT_DUAL, bundle: torch.Tensor | None = None,
+                                 headers: torch.Tensor | None = None, stream=None):
+    """taco_compress_shards with the library's static scratch instead of a workspace.
+
+    For callers that cannot allocate device memory where they compress; pass
+    preallocated ``bundle`` and ``headers`` to allocate nothing at all. At most
+    8 shards; calls that overlap on the GPU share the scratch and race.
+    """
+    if x.dtype != torch.bfloat16 or not x.is_cuda or x.dim() != 3 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous bf16 CUDA tensor [P, N, h]")
+    P, N, h = x.shape
+    if bundle is None:
+        bundle = torch.empty((P, max(shard_bytes(N, h, block), 1)), dtype=torch.uint8, device=x.device)
+    if headers is None:
+        headers = torch.empty((P, HEADER_BYTES), dtype=torch.uint8, device=x.device)
+    st = _lib().taco_compress_shards_noalloc(_ptr(x), P, N, h, block, float(target_energy), variant,
+                                             _ptr(bundle), _ptr(headers), _stream_ptr(stream))
+    _check(st, "taco_compress_shards_noalloc")
     return bundle, headers
 
 

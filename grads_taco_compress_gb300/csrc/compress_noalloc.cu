@@ -1,0 +1,84 @@
+// taco_compress_shards_noalloc: compress without a caller-provided workspace.
+//
+// Some callers cannot allocate device memory at the point where they
+// compress: a communication library's progress thread or collective callback
+// that must not call cudaMalloc (it can synchronise the device or deadlock
+// against work in flight), or a runtime whose memory is owned by an external
+// pool. This entry point needs no workspace from them: the per-CTA partials
+// and arrival counters that write the per-tensor header live in the static
+// device array below, which every GPU that loads this library keeps until the
+// process exits.
+
+#include <cmath>
+#include <mutex>
+
+#include "taco_launch.h"
+
+namespace {
+
+// Room for TACO_NOALLOC_MAX_SHARDS shards of compress workspace (131,200 B).
+constexpr size_t kNoallocScratchBytes =
+    static_cast<size_t>(TACO_NOALLOC_MAX_SHARDS) * taco::kWorkspaceShardStride;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::once_flag g_scratch_once[kMaxDevices];
+void* g_scratch_ptr[kMaxDevices];
+cudaError_t g_scratch_err[kMaxDevices];
+
+// Device address of the scratch array on the current device. In host code
+// `g_noalloc_scratch` is only a host-side stand-in, so the address is looked up
+// once per device, with that device current.
+cudaError_t scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::call_once(g_scratch_once[dev], [dev]() {
+    void* p = nullptr;
+    g_scratch_err[dev] = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    g_scratch_ptr[dev] = p;
+  });
+  if (g_scratch_err[dev] != cudaSuccess) return g_scratch_err[dev];
+  *out = g_scratch_ptr[dev];
+  return cudaSuccess;
+}
+
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+extern "C" taco_status taco_compress_shards_noalloc(const void* x_bf16, int P, int64_t N, int64_t h,
+                                                    int block, float target_energy, int variant,
+                                                    void* bundle_out, taco_header* headers_out,
+                                                    void* stream) {
+  // Checks that taco_compress_shards makes too, taken first so that a rejected
+  // call enqueues nothing (not even the scratch clear below).
+  if (block != 64 && block != 128 && block != 256) return TACO_ERR_BLOCK;
+  if (N < 0 || h <= 0 || h % block != 0 || (N > 0 && N > (int64_t{1} << 40) / h)) return TACO_ERR_SHAPE;
+  if (P < 1 || P > TACO_MAX_SHARDS) return TACO_ERR_ARG;
+  if (P > TACO_NOALLOC_MAX_SHARDS) return TACO_ERR_WORKSPACE;   // beyond the static scratch
+  if (variant != TACO_VARIANT_DUAL && variant != TACO_VARIANT_ABSMAX) return TACO_ERR_ARG;
+  if (!(target_energy > 0.0f) || !std::isfinite(target_energy)) return TACO_ERR_ARG;
+  if (!headers_out) return TACO_ERR_NULL;
+  if (!aligned(headers_out, 8)) return TACO_ERR_ALIGN;
+  if (N > 0) {
+    if (!x_bf16 || !bundle_out) return TACO_ERR_NULL;
+    if (!aligned(x_bf16, 16) || !aligned(bundle_out, 16)) return TACO_ERR_ALIGN;
+    const uintptr_t xa = reinterpret_cast<uintptr_t>(x_bf16), ba = reinterpret_cast<uintptr_t>(bundle_out);
+    const size_t in_bytes = static_cast<size_t>(P) * N * h * 2;
+    const size_t out_bytes = static_cast<size_t>(P) * taco_shard_bytes(N, h, block);
+    if (xa < ba + out_bytes && ba < xa + in_bytes) return TACO_ERR_ARG;   // overlapping buffers
+  }
+
+  void* scratch = nullptr;
+  if (scratch_address(&scratch) != cudaSuccess) return TACO_ERR_CUDA;
+  const size_t need = static_cast<size_t>(P) * taco::kWorkspaceShardStride;
+  // The arrival counters must start at zero; the array keeps whatever the
+  // previous call (on any stream) left in it.
+  if (cudaMemsetAsync(scratch, 0, need, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return TACO_ERR_CUDA;
+  return taco_compress_shards(x_bf16, P, N, h, block, target_energy, variant, bundle_out,
+                              headers_out, scratch, need, stream);
+}

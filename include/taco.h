@@ -121,6 +121,32 @@ taco_status taco_compress_shards(const void* x_bf16, int P, int64_t N, int64_t h
                                  void* workspace, size_t workspace_bytes,
                                  void* stream);
 
+/* ---- taco_compress_shards_noalloc -----------------------------------------
+ * The paper has no counterpart to this entry point: it exists for callers
+ * that cannot allocate device memory when they compress (a communication
+ * library's progress thread or collective callback, where cudaMalloc may
+ * synchronise the device or deadlock against work in flight; a runtime
+ * whose memory belongs to an external pool). It is taco_compress_shards
+ * without the workspace argument: the per-CTA partials and counters live in
+ * a static device array of the library (TACO_NOALLOC_MAX_SHARDS * 16,400 =
+ * 131,200 bytes), which every GPU that loads the library holds until the
+ * process exits. The caller still passes x, the bundle and the headers.
+ *   - P > TACO_NOALLOC_MAX_SHARDS returns TACO_ERR_WORKSPACE (the request does
+ *     not fit the static scratch); other errors as taco_compress_shards, and a
+ *     rejected call enqueues nothing.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Each call clears the counters it uses with cudaMemsetAsync on `stream`
+ *     and then launches the compress kernel; it allocates nothing.
+ *   - All calls share the one array, so calls that overlap on the GPU (other
+ *     streams, other threads) race on it: order them. */
+#define TACO_NOALLOC_MAX_SHARDS 8
+taco_status taco_compress_shards_noalloc(const void* x_bf16, int P, int64_t N, int64_t h,
+                                         int block, float target_energy, int variant,
+                                         void* bundle_out, taco_header* headers_out,
+                                         void* stream);
+
 /* ---- taco_decompress_reduce ---------------------------------------------
  * Reconstruct and sum P shards of one bundle (device, 16-byte aligned, the
  * layout above, all compressed from [N, h] tensors with the same block)
