@@ -39,6 +39,7 @@ EXPORTED_SYMBOLS = (
     "taco_compress_shards_noalloc",
     "taco_decompress_reduce", "taco_decompress_reduce_ptrs",
     "taco_e4m3_encode_f32", "taco_e4m3_decode_f32",
+    "taco_get_fault", "taco_selftest_wait_timeout",
     "taco_status_string", "taco_abi_version",
 )
 
@@ -75,6 +76,8 @@ def _lib() -> ctypes.CDLL:
             "taco_decompress_reduce_ptrs": (i32, [ctypes.POINTER(vp), i32, i64, i64, i32, vp, vp]),
             "taco_e4m3_encode_f32": (i32, [vp, vp, i64, vp]),
             "taco_e4m3_decode_f32": (i32, [vp, vp, i64, vp]),
+            "taco_get_fault": (i32, [ctypes.POINTER(ctypes.c_uint32), i32]),
+            "taco_selftest_wait_timeout": (i32, [ctypes.c_uint64, vp, vp]),
             "taco_status_string": (ctypes.c_char_p, [i32]),
             "taco_abi_version": (i32, []),
         }
@@ -254,3 +257,18 @@ def taco_e4m3_decode_f32(codes: torch.Tensor, stream=None) -> torch.Tensor:
     _check(_lib().taco_e4m3_decode_f32(_ptr(codes), _ptr(out), codes.numel(), _stream_ptr(stream)),
            "taco_e4m3_decode_f32")
     return out
+
+
+def taco_get_fault(clear: bool = False) -> int:
+    """Device fault bits of the current device (synchronises with it)."""
+    bits = ctypes.c_uint32(0)
+    _check(_lib().taco_get_fault(ctypes.byref(bits), int(clear)), "taco_get_fault")
+    return int(bits.value)
+
+
+def taco_selftest_wait_timeout(limit_ns: int, stream=None) -> int:
+    """Run the bounded-wait self-test; returns the status word (1 = timed out)."""
+    status = torch.full((1,), 7, dtype=torch.int32, device="cuda")
+    _check(_lib().taco_selftest_wait_timeout(int(limit_ns), _ptr(status), _stream_ptr(stream)),
+           "taco_selftest_wait_timeout")
+    return int(status.item())

@@ -4,15 +4,19 @@
 // Compression of Intermediate Tensors ...", gist.science pt summary, §2.B.3:
 // energy, ASH and DS quantisation fused in one kernel, no intermediate
 // global-memory round trip):
-//   load bf16 (16-byte streaming loads) -> block energy (fp32, lane shuffles)
-//   -> FWHT of the raw block in registers/shuffles (the rotation is linear,
-//   so alpha is applied afterwards together with 1/sqrt(n) and 1/s)
-//   -> alpha = sqrt(E*/E), s = max(1, alpha/sqrt(n) * max|Hx| / 448)
-//   -> E4M3 codes with cvt.rn.satfinite (8-byte stores), alpha and s stores
-//   -> per-tensor header through per-CTA partials and a last-CTA reduction.
-// The grid is persistent: gridDim.y = shard, gridDim.x CTAs per shard, each
-// warp walking warp tiles (32/LPB blocks) with a stride of the whole grid row,
-// prefetching the next tile's loads before working on the current one.
+//   TMA bulk copy of the bf16 tile into shared memory -> block energy (fp32,
+//   packed FMAs, lane shuffles) -> FWHT of the raw block in registers and
+//   shuffles (the rotation is linear, so alpha is applied afterwards together
+//   with 1/sqrt(n) and 1/s) -> alpha = sqrt(E*/E), s = max(1, alpha/sqrt(n) *
+//   max|Hx| / 448) -> E4M3 codes with cvt.rn.satfinite (8-byte stores),
+//   alpha and s stores -> per-tensor header through per-CTA partials and a
+//   last-CTA reduction.
+// Grid: gridDim.y = shard, gridDim.x persistent CTAs per shard. Each warp
+// walks warp tiles (2048 elements, 32/LPB blocks) with a stride of the grid
+// row and keeps kCompressStages tiles in flight: lane 0 issues a 1-D
+// cp.async.bulk per tile into the warp's ring of shared-memory stages, each
+// completed on its own mbarrier; all lanes wait (bounded in time), read their
+// chunks, and hand the stage back.
 
 #include <cmath>
 
@@ -23,35 +27,32 @@ namespace taco {
 
 namespace {
 
-template <int NB, int CH>
-struct CompressShape {
-  static constexpr int kLPB = NB / (8 * CH);       // lanes per block
-  static constexpr int kBPT = 32 / kLPB;           // blocks per warp tile
-  static_assert(kLPB >= 1 && kLPB <= 32 && (kLPB & (kLPB - 1)) == 0, "bad split");
-};
+__device__ unsigned int g_compress_fault;
 
-template <int CH, int LPB>
-__device__ __forceinline__ void load_tile(const uint16_t* __restrict__ x, int64_t b, bool valid,
-                                          int j, uint4 (&raw)[CH]) {
-  const uint16_t* blk = x + (valid ? b : 0) * (8 * CH * LPB);
-#pragma unroll
-  for (int v = 0; v < CH; ++v) {
-    raw[v] = valid ? ld_stream_v4(blk + 8 * (j + LPB * v)) : make_uint4(0, 0, 0, 0);
-  }
-}
-
-template <int NB, int CH, int VARIANT>
-__global__ void __launch_bounds__(kCompressThreads)
+template <int NB, int VARIANT>
+__global__ void __launch_bounds__(kCompressThreads, kCompressMinBlocks)
 compress_kernel(CompressArgs a) {
-  using S = CompressShape<NB, CH>;
-  constexpr int LPB = S::kLPB;
-  constexpr int BPT = S::kBPT;
+  constexpr int LPB = NB / 64;                 // lanes per block
+  constexpr int BPT = 32 / LPB;                // blocks per warp tile
+  constexpr int D = kCompressStages;
+  constexpr int WARPS = kCompressThreads / 32;
+  constexpr uint32_t TILE_BYTES = kTileElems * 2;
+  static_assert(LPB >= 1 && LPB <= 4, "block size");
+
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ float sh_max[WARPS];
+  __shared__ uint32_t sh_cnt[WARPS];
+  __shared__ bool sh_last;
 
   const int shard = blockIdx.y;
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
-  const int j = lane & (LPB - 1);                   // lane inside its block
-  const int sub = lane / LPB;                       // block inside the tile
+  const int j = lane & (LPB - 1);              // lane inside its block
+  const int sub = lane / LPB;                  // block inside the tile
+  const int cx = sub & (kCH - 1);              // chunk-slot swizzle
+
+  const uint32_t stage0 = smem_u32(smem) + warp * (D * TILE_BYTES);
+  const uint32_t bar0 = smem_u32(smem) + WARPS * D * TILE_BYTES + warp * (D * 8);
 
   const uint16_t* __restrict__ x = a.x + static_cast<int64_t>(shard) * a.shard_elems;
   uint8_t* shard_base = a.bundle + static_cast<size_t>(shard) * a.shard_bytes;
@@ -60,96 +61,143 @@ compress_kernel(CompressArgs a) {
   float* __restrict__ s_out = reinterpret_cast<float*>(shard_base + a.s_off);
 
   const int64_t nblocks = a.nblocks;
-  const int64_t tiles = (nblocks + BPT - 1) / BPT;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * (kCompressThreads / 32);
-  int64_t tile = static_cast<int64_t>(blockIdx.x) * (kCompressThreads / 32) + warp;
+  const int tiles = static_cast<int>((nblocks + BPT - 1) / BPT);
+  const int stride = gridDim.x * WARPS;
+  const int t0 = blockIdx.x * WARPS + warp;
+  const int count = t0 < tiles ? (tiles - 1 - t0) / stride + 1 : 0;   // tiles of this warp
+  // bytes of the last tile of the tensor (the only one that can be partial)
+  const uint32_t tail_bytes =
+      static_cast<uint32_t>(nblocks - static_cast<int64_t>(tiles - 1) * BPT) * (NB * 2);
+
+  // Producer state (lane 0): next tile to bring in, its source, its stage.
+  int it = 0, is = 0;
+  const uint16_t* isrc = x + static_cast<int64_t>(t0) * kTileElems;
+  const int64_t src_step = static_cast<int64_t>(stride) * kTileElems;
+  uint64_t policy = 0;
+  if (lane == 0) {
+    for (int s = 0; s < D; ++s) mbar_init(bar0 + 8 * s, 1);
+    fence_mbar_init();
+    policy = l2_evict_first_policy();
+  }
+  __syncwarp();
+
+  auto issue_next = [&]() {   // lane 0 only
+    const uint32_t bytes = (t0 + it * stride == tiles - 1) ? tail_bytes : TILE_BYTES;
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(bar0 + 8 * is, bytes);
+    tma_load_1d(stage0 + is * TILE_BYTES, isrc, bytes, bar0 + 8 * is, policy);
+    ++it;
+    isrc += src_step;
+    is = (is + 1 == D) ? 0 : is + 1;
+  };
+  if (lane == 0) {
+    while (it < D - 1 && it < count) issue_next();
+  }
 
   float part_smax = 0.0f;   // header partials of this thread (lane j == 0 only)
   uint32_t part_cnt = 0;
+  int k = 0, cs = 0;
+  uint32_t cphase = 0;
+  bool ok = true;
 
-  uint4 raw[CH];
-  {
-    const int64_t b = tile * BPT + sub;
-    load_tile<CH, LPB>(x, b, tile < tiles && b < nblocks, j, raw);
-  }
-
-  for (; tile < tiles; tile += stride) {
-    const int64_t b = tile * BPT + sub;
+  for (; k < count; ++k) {
+    if (lane == 0 && it < count) issue_next();
+    const bool got = mbar_wait(bar0 + 8 * cs, cphase);
+    if (!__all_sync(kFullMask, got)) {   // keep the warp's decision uniform
+      ok = false;
+      break;
+    }
+    const int64_t b = static_cast<int64_t>(t0 + k * stride) * BPT + sub;
     const bool valid = b < nblocks;
 
-    // Prefetch the next tile of this warp.
-    uint4 nxt[CH];
+    f2 v[kCH][4];
     {
-      const int64_t tn = tile + stride;
-      const int64_t bn = tn * BPT + sub;
-      load_tile<CH, LPB>(x, bn, tn < tiles && bn < nblocks, j, nxt);
+      const uint32_t base = stage0 + cs * TILE_BYTES + sub * (NB * 2);
+#pragma unroll
+      for (int q = 0; q < kCH; ++q) {
+        const uint4 r = lds128(base + 16 * (j + LPB * (q ^ cx)));
+        v[q][0] = f2{bf16_lo(r.x), bf16_hi(r.x)};
+        v[q][1] = f2{bf16_lo(r.y), bf16_hi(r.y)};
+        v[q][2] = f2{bf16_lo(r.z), bf16_hi(r.z)};
+        v[q][3] = f2{bf16_lo(r.w), bf16_hi(r.w)};
+      }
+    }
+    __syncwarp();   // every lane has read stage cs: lane 0 may refill it
+    if (++cs == D) {
+      cs = 0;
+      cphase ^= 1u;
     }
 
-    float v[CH][8];
+    // Block energy e = sum x^2 (E = e / NB): packed partial sums, then lanes.
+    f2 ea{0.f, 0.f}, eb{0.f, 0.f};
 #pragma unroll
-    for (int c = 0; c < CH; ++c) unpack_bf16x8(raw[c], v[c]);
-
-    // Block energy (sum of squares; E = e / NB). Four partial sums, then the
-    // lanes of the block.
-    float e0 = 0.f, e1 = 0.f, e2 = 0.f, e3 = 0.f;
-#pragma unroll
-    for (int c = 0; c < CH; ++c) {
-      e0 = fmaf(v[c][0], v[c][0], e0); e1 = fmaf(v[c][1], v[c][1], e1);
-      e2 = fmaf(v[c][2], v[c][2], e2); e3 = fmaf(v[c][3], v[c][3], e3);
-      e0 = fmaf(v[c][4], v[c][4], e0); e1 = fmaf(v[c][5], v[c][5], e1);
-      e2 = fmaf(v[c][6], v[c][6], e2); e3 = fmaf(v[c][7], v[c][7], e3);
+    for (int q = 0; q < kCH; ++q) {
+      ea = fma2(v[q][0], v[q][0], ea);
+      eb = fma2(v[q][1], v[q][1], eb);
+      ea = fma2(v[q][2], v[q][2], ea);
+      eb = fma2(v[q][3], v[q][3], eb);
     }
-    const float e = block_sum<LPB>((e0 + e1) + (e2 + e3));
+    const float e = block_sum<LPB>((ea.x + ea.y) + (eb.x + eb.y));
 
     // Rotation of the raw block: t = H x.
-    fwht_in_registers<CH>(v);
-    fwht_across_lanes<CH, LPB>(v, j);
+    fwht_in_registers<kCH>(v, cx);
+    fwht_across_lanes<kCH, LPB>(v, j);
 
-    float tmax = 0.f;
+    // max |t| = max(max t, -min t)
+    float hi = v[0][0].x, lo = v[0][0].x;
 #pragma unroll
-    for (int c = 0; c < CH; ++c)
+    for (int q = 0; q < kCH; ++q)
 #pragma unroll
-      for (int i = 0; i < 8; ++i) tmax = fmaxf(tmax, fabsf(v[c][i]));
-    tmax = block_max<LPB>(tmax);
+      for (int i = 0; i < 4; ++i) {
+        hi = max3(hi, v[q][i].x, v[q][i].y);
+        lo = min3(lo, v[q][i].x, v[q][i].y);
+      }
+    const float tmax = block_max<LPB>(fmaxf(hi, -lo));
 
     // alpha = sqrt(E*/E) = sqrt(n E*) / sqrt(e): reciprocal square root with
-    // one Newton step (error about one ulp), 1 for an all-zero block.
-    float alpha = 1.0f;
-    if (e > 0.f) {
-      float r = rsqrtf(e);
-      const float hr = 0.5f * e * r;
-      r = fmaf(fmaf(-hr, r, 0.5f), r, r);
-      alpha = a.sqrt_nE * r;
-    }
+    // one Newton step (error about one ulp); 1 for an all-zero block.
+    float r = rsqrtf(e);
+    r = fmaf(fmaf(-0.5f * e * r, r, 0.5f), r, r);
+    const float alpha = (e > 0.f) ? a.sqrt_nE * r : 1.0f;
     const float cscale = alpha * a.inv_sqrt_n;        // y = cscale * t
     const float amax = cscale * tmax;
-    float s;
-    if (VARIANT == 0) {
-      s = fmaxf(1.0f, amax * (1.0f / 448.0f));
-    } else {
-      s = amax > 0.f ? amax * (1.0f / 448.0f) : 1.0f;
-    }
-    const float g = (s == 1.0f) ? cscale : cscale / s;  // code value = g * t
+    const float sc = (VARIANT == 0) ? fmaxf(1.0f, amax * (1.0f / 448.0f))
+                                    : (amax > 0.f ? amax * (1.0f / 448.0f) : 1.0f);
+    const float g = __fdividef(cscale, sc);           // code value = g * t
+    const f2 g2{g, g};
 
     if (valid) {
       uint8_t* cp = codes + b * NB;
 #pragma unroll
-      for (int c = 0; c < CH; ++c) {
+      for (int q = 0; q < kCH; ++q) {
+        const f2 y0 = mul2(v[q][0], g2), y1 = mul2(v[q][1], g2);
+        const f2 y2 = mul2(v[q][2], g2), y3 = mul2(v[q][3], g2);
         uint2 w;
-        w.x = e4m3x4_from_f32(v[c][0] * g, v[c][1] * g, v[c][2] * g, v[c][3] * g);
-        w.y = e4m3x4_from_f32(v[c][4] * g, v[c][5] * g, v[c][6] * g, v[c][7] * g);
-        *reinterpret_cast<uint2*>(cp + 8 * (j + LPB * c)) = w;
+        w.x = e4m3x4_from_f32(y0.x, y0.y, y1.x, y1.y);
+        w.y = e4m3x4_from_f32(y2.x, y2.y, y3.x, y3.y);
+        *reinterpret_cast<uint2*>(cp + 8 * (j + LPB * (q ^ cx))) = w;
       }
       if (j == 0) {
         alpha_out[b] = alpha;
-        s_out[b] = s;
-        part_smax = fmaxf(part_smax, s);
-        part_cnt += (s > 1.0f) ? 1u : 0u;
+        s_out[b] = sc;
+        part_smax = fmaxf(part_smax, sc);
+        part_cnt += (sc > 1.0f) ? 1u : 0u;
       }
     }
+  }
 
-#pragma unroll
-    for (int c = 0; c < CH; ++c) raw[c] = nxt[c];
+  if (!ok) {
+    // A stage never completed: record it, then wait (bounded) for the copies
+    // this warp still has in flight (tiles k .. it-1) before the CTA may exit.
+    if (lane == 0) atomicOr(&g_compress_fault, kFaultCompressWait);
+    const int issued = __shfl_sync(kFullMask, it, 0);
+    for (int kk = k; kk < issued; ++kk) {
+      mbar_wait(bar0 + 8 * cs, cphase);
+      if (++cs == D) {
+        cs = 0;
+        cphase ^= 1u;
+      }
+    }
   }
 
   // ---- per-tensor header: CTA reduction, then the last CTA of the shard ----
@@ -158,9 +206,6 @@ compress_kernel(CompressArgs a) {
     part_smax = fmaxf(part_smax, __shfl_xor_sync(kFullMask, part_smax, m));
     part_cnt += __shfl_xor_sync(kFullMask, part_cnt, m);
   }
-  __shared__ float sh_max[kCompressThreads / 32];
-  __shared__ uint32_t sh_cnt[kCompressThreads / 32];
-  __shared__ bool sh_last;
   if (lane == 0) {
     sh_max[warp] = part_smax;
     sh_cnt[warp] = part_cnt;
@@ -172,7 +217,7 @@ compress_kernel(CompressArgs a) {
   if (threadIdx.x == 0) {
     float m = 0.f;
     uint32_t n = 0;
-    for (int w = 0; w < kCompressThreads / 32; ++w) {
+    for (int w = 0; w < WARPS; ++w) {
       m = fmaxf(m, sh_max[w]);
       n += sh_cnt[w];
     }
@@ -204,7 +249,7 @@ compress_kernel(CompressArgs a) {
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-      for (int w = 1; w < kCompressThreads / 32; ++w) {
+      for (int w = 1; w < WARPS; ++w) {
         m = fmaxf(m, sh_max[w]);
         n += sh_cnt[w];
       }
@@ -222,45 +267,53 @@ compress_kernel(CompressArgs a) {
   }
 }
 
-template <int NB, int CH>
-cudaError_t launch_nb(const CompressArgs& a, int variant, int grid_x, int P, cudaStream_t st) {
-  const dim3 grid(grid_x, P);
-  if (variant == 0) {
-    compress_kernel<NB, CH, 0><<<grid, kCompressThreads, 0, st>>>(a);
-  } else {
-    compress_kernel<NB, CH, 1><<<grid, kCompressThreads, 0, st>>>(a);
-  }
-  return cudaGetLastError();
-}
-
-template <int NB, int CH>
+template <int NB>
 const void* kernel_ptr(int variant) {
-  return variant == 0 ? reinterpret_cast<const void*>(compress_kernel<NB, CH, 0>)
-                      : reinterpret_cast<const void*>(compress_kernel<NB, CH, 1>);
+  return variant == 0 ? reinterpret_cast<const void*>(compress_kernel<NB, 0>)
+                      : reinterpret_cast<const void*>(compress_kernel<NB, 1>);
 }
 
 }  // namespace
 
-// Chunks of 8 elements held per thread, per block size.
-constexpr int kCompressCH = 4;
+int compress_tile_blocks(int block) { return 32 / (block / 64); }
 
-int compress_tile_blocks(int block) { return 32 / (block / (8 * kCompressCH)); }
+size_t compress_smem_bytes() {
+  return static_cast<size_t>(kCompressThreads / 32) * kCompressStages * (kTileElems * 2 + 8);
+}
 
 const void* compress_kernel_ptr(int block, int variant) {
   switch (block) {
-    case 64: return kernel_ptr<64, kCompressCH>(variant);
-    case 128: return kernel_ptr<128, kCompressCH>(variant);
-    default: return kernel_ptr<256, kCompressCH>(variant);
+    case 64: return kernel_ptr<64>(variant);
+    case 128: return kernel_ptr<128>(variant);
+    default: return kernel_ptr<256>(variant);
   }
 }
 
 cudaError_t launch_compress(const CompressArgs& a, int block, int variant, int grid_x, int P,
                             cudaStream_t stream) {
+  const dim3 grid(grid_x, P);
+  const size_t smem = compress_smem_bytes();
+#define TACO_LAUNCH_C(NB)                                                              \
+  if (variant == 0)                                                                    \
+    compress_kernel<NB, 0><<<grid, kCompressThreads, smem, stream>>>(a);               \
+  else                                                                                 \
+    compress_kernel<NB, 1><<<grid, kCompressThreads, smem, stream>>>(a);
   switch (block) {
-    case 64: return launch_nb<64, kCompressCH>(a, variant, grid_x, P, stream);
-    case 128: return launch_nb<128, kCompressCH>(a, variant, grid_x, P, stream);
-    default: return launch_nb<256, kCompressCH>(a, variant, grid_x, P, stream);
+    case 64: TACO_LAUNCH_C(64) break;
+    case 128: TACO_LAUNCH_C(128) break;
+    default: TACO_LAUNCH_C(256) break;
   }
+#undef TACO_LAUNCH_C
+  return cudaGetLastError();
+}
+
+cudaError_t compress_fault(unsigned int* bits, bool clear) {
+  cudaError_t e = cudaMemcpyFromSymbol(bits, g_compress_fault, sizeof(unsigned int));
+  if (e == cudaSuccess && clear) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_compress_fault, &zero, sizeof(unsigned int));
+  }
+  return e;
 }
 
 }  // namespace taco

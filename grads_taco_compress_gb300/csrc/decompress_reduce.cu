@@ -8,11 +8,12 @@
 //   x_hat  = bf16( H_n z )                                 (one inverse rotation)
 // H_n / sqrt(n) is symmetric and orthogonal, so it is its own inverse, and the
 // sum can be taken before the rotation because the rotation is linear.
-// Each thread owns the same 8*CH elements of a block as in compress; per shard
-// it issues CH 8-byte code loads and two scalar scale loads (shared by the
-// block's lanes), decodes E4M3 pairs with cvt.rn.f16x2.e4m3x2 and
-// accumulates with one FMA per element. The grid is persistent over warp
-// tiles.
+// Each warp walks warp tiles (2048 elements) with a stride of the grid. For
+// one tile it consumes P stages, one per shard; lane 0 keeps
+// kDecompressStages stages in flight, each a set of three 1-D cp.async.bulk
+// copies (the tile's codes, alphas and s values) completed on one mbarrier.
+// Codes are decoded in pairs with cvt.rn.f16x2.e4m3x2 and accumulated with
+// packed f32x2 FMAs; the output leaves as 16-byte bf16 stores.
 
 #include "taco_device.cuh"
 #include "taco_launch.h"
@@ -21,70 +22,154 @@ namespace taco {
 
 namespace {
 
-template <int NB, int CH>
-__global__ void __launch_bounds__(kDecompressThreads)
+__device__ unsigned int g_decompress_fault;
+
+constexpr uint32_t kCodesBytes = kTileElems;          // codes of one tile
+constexpr uint32_t kScaleBytes = 128;                 // alphas (or s) of one tile, padded
+constexpr uint32_t kStageBytes = kCodesBytes + 2 * kScaleBytes;
+
+template <int NB>
+__global__ void __launch_bounds__(kDecompressThreads, kDecompressMinBlocks)
 decompress_reduce_kernel(DecompressArgs a) {
-  constexpr int LPB = NB / (8 * CH);
+  constexpr int LPB = NB / 64;
   constexpr int BPT = 32 / LPB;
-  static_assert(LPB >= 1 && LPB <= 32 && (LPB & (LPB - 1)) == 0, "bad split");
+  constexpr int D = kDecompressStages;
+  constexpr int WARPS = kDecompressThreads / 32;
+  static_assert(LPB >= 1 && LPB <= 4, "block size");
+  static_assert(BPT * 4 <= kScaleBytes, "scale slot");
+
+  extern __shared__ __align__(128) unsigned char smem[];
 
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int j = lane & (LPB - 1);
   const int sub = lane / LPB;
+  const int cx = sub & (kCH - 1);
+  const int P = a.P;
+
+  const uint32_t stage0 = smem_u32(smem) + warp * (D * kStageBytes);
+  const uint32_t bar0 = smem_u32(smem) + WARPS * D * kStageBytes + warp * (D * 8);
 
   const int64_t nblocks = a.nblocks;
-  const int64_t tiles = (nblocks + BPT - 1) / BPT;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * (kDecompressThreads / 32);
+  const int tiles = static_cast<int>((nblocks + BPT - 1) / BPT);
+  const int stride = gridDim.x * WARPS;
+  const int t0 = blockIdx.x * WARPS + warp;
+  const int ntiles = t0 < tiles ? (tiles - 1 - t0) / stride + 1 : 0;
+  const int count = ntiles * P;                       // stages of this warp
+  const uint32_t vb_tail = static_cast<uint32_t>(nblocks - static_cast<int64_t>(tiles - 1) * BPT);
 
-  for (int64_t tile = static_cast<int64_t>(blockIdx.x) * (kDecompressThreads / 32) + warp;
-       tile < tiles; tile += stride) {
-    const int64_t b = tile * BPT + sub;
+  // Producer state (lane 0): next stage = (tile number it_t of this warp,
+  // shard ip), its slot is, and the byte offsets of that tile in a shard.
+  int issued = 0, it_t = 0, ip = 0, is = 0;
+  int64_t code_off = static_cast<int64_t>(t0) * kTileElems;
+  int64_t scale_off = static_cast<int64_t>(t0) * BPT * 4;
+  const int64_t code_step = static_cast<int64_t>(stride) * kTileElems;
+  const int64_t scale_step = static_cast<int64_t>(stride) * BPT * 4;
+  uint64_t policy = 0;
+  if (lane == 0) {
+    for (int s = 0; s < D; ++s) mbar_init(bar0 + 8 * s, 1);
+    fence_mbar_init();
+    policy = l2_evict_first_policy();
+  }
+  __syncwarp();
+
+  auto issue_next = [&]() {   // lane 0 only
+    const bool tail = (t0 + it_t * stride == tiles - 1);
+    const uint32_t vb = tail ? vb_tail : static_cast<uint32_t>(BPT);
+    const uint32_t cbytes = vb * NB;
+    const uint32_t sbytes = (vb * 4 + 15) & ~15u;     // stays inside the 256-byte padding
+    const uint32_t dst = stage0 + is * kStageBytes;
+    const uint32_t bar = bar0 + 8 * is;
+    const uint8_t* base = a.shard[ip];
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(bar, cbytes + 2 * sbytes);
+    tma_load_1d(dst, base + code_off, cbytes, bar, policy);
+    tma_load_1d(dst + kCodesBytes, base + a.alpha_off + scale_off, sbytes, bar, policy);
+    tma_load_1d(dst + kCodesBytes + kScaleBytes, base + a.s_off + scale_off, sbytes, bar, policy);
+    ++issued;
+    is = (is + 1 == D) ? 0 : is + 1;
+    if (++ip == P) {
+      ip = 0;
+      ++it_t;
+      code_off += code_step;
+      scale_off += scale_step;
+    }
+  };
+  if (lane == 0) {
+    while (issued < D - 1 && issued < count) issue_next();
+  }
+
+  int k = 0, cs = 0;
+  uint32_t cphase = 0;
+  bool ok = true;
+  for (int ti = 0; ti < ntiles && ok; ++ti) {
+    const int64_t b = static_cast<int64_t>(t0 + ti * stride) * BPT + sub;
     const bool valid = b < nblocks;
-    const int64_t bb = valid ? b : 0;
 
-    float z[CH][8];
+    f2 z[kCH][4];
 #pragma unroll
-    for (int c = 0; c < CH; ++c)
+    for (int q = 0; q < kCH; ++q)
 #pragma unroll
-      for (int i = 0; i < 8; ++i) z[c][i] = 0.f;
+      for (int i = 0; i < 4; ++i) z[q][i] = f2{0.f, 0.f};
 
-#pragma unroll 2
-    for (int p = 0; p < a.P; ++p) {
-      const uint8_t* base = a.shard[p];
-      uint2 q[CH];
+    for (int p = 0; p < P; ++p, ++k) {
+      if (lane == 0 && issued < count) issue_next();
+      const bool got = mbar_wait(bar0 + 8 * cs, cphase);
+      if (!__all_sync(kFullMask, got)) {   // keep the warp's decision uniform
+        ok = false;
+        break;
+      }
+      const uint32_t st = stage0 + cs * kStageBytes;
+      const float al = lds_f32(st + kCodesBytes + 4 * sub);
+      const float sc = lds_f32(st + kCodesBytes + kScaleBytes + 4 * sub);
+      uint2 w[kCH];
 #pragma unroll
-      for (int c = 0; c < CH; ++c)
-        q[c] = valid ? ld_stream_v2(base + bb * NB + 8 * (j + LPB * c)) : make_uint2(0, 0);
-      const float al = ld_stream_f32(reinterpret_cast<const float*>(base + a.alpha_off) + bb);
-      const float sc = ld_stream_f32(reinterpret_cast<const float*>(base + a.s_off) + bb);
+      for (int q = 0; q < kCH; ++q) w[q] = lds64(st + sub * NB + 8 * (j + LPB * (q ^ cx)));
+      __syncwarp();   // every lane has read slot cs: lane 0 may refill it
+      if (++cs == D) {
+        cs = 0;
+        cphase ^= 1u;
+      }
+
       const float d = sc * __frcp_rn(al) * a.inv_sqrt_n;
+      const f2 d2{d, d};
 #pragma unroll
-      for (int c = 0; c < CH; ++c) {
-        const float2 f0 = e4m3x2_to_f32(q[c].x & 0xffffu);
-        const float2 f1 = e4m3x2_to_f32(q[c].x >> 16);
-        const float2 f2 = e4m3x2_to_f32(q[c].y & 0xffffu);
-        const float2 f3 = e4m3x2_to_f32(q[c].y >> 16);
-        z[c][0] = fmaf(d, f0.x, z[c][0]); z[c][1] = fmaf(d, f0.y, z[c][1]);
-        z[c][2] = fmaf(d, f1.x, z[c][2]); z[c][3] = fmaf(d, f1.y, z[c][3]);
-        z[c][4] = fmaf(d, f2.x, z[c][4]); z[c][5] = fmaf(d, f2.y, z[c][5]);
-        z[c][6] = fmaf(d, f3.x, z[c][6]); z[c][7] = fmaf(d, f3.y, z[c][7]);
+      for (int q = 0; q < kCH; ++q) {
+        z[q][0] = fma2(d2, e4m3x2_to_f2(w[q].x & 0xffffu), z[q][0]);
+        z[q][1] = fma2(d2, e4m3x2_to_f2(w[q].x >> 16), z[q][1]);
+        z[q][2] = fma2(d2, e4m3x2_to_f2(w[q].y & 0xffffu), z[q][2]);
+        z[q][3] = fma2(d2, e4m3x2_to_f2(w[q].y >> 16), z[q][3]);
       }
     }
+    if (!ok) break;
 
-    fwht_in_registers<CH>(z);
-    fwht_across_lanes<CH, LPB>(z, j);
+    fwht_in_registers<kCH>(z, cx);
+    fwht_across_lanes<kCH, LPB>(z, j);
 
     if (valid) {
       uint16_t* op = a.out + b * NB;
 #pragma unroll
-      for (int c = 0; c < CH; ++c) {
-        uint4 w;
-        w.x = pack_bf16x2(z[c][0], z[c][1]);
-        w.y = pack_bf16x2(z[c][2], z[c][3]);
-        w.z = pack_bf16x2(z[c][4], z[c][5]);
-        w.w = pack_bf16x2(z[c][6], z[c][7]);
-        *reinterpret_cast<uint4*>(op + 8 * (j + LPB * c)) = w;
+      for (int q = 0; q < kCH; ++q) {
+        uint4 o;
+        o.x = pack_bf16x2(z[q][0].x, z[q][0].y);
+        o.y = pack_bf16x2(z[q][1].x, z[q][1].y);
+        o.z = pack_bf16x2(z[q][2].x, z[q][2].y);
+        o.w = pack_bf16x2(z[q][3].x, z[q][3].y);
+        *reinterpret_cast<uint4*>(op + 8 * (j + LPB * (q ^ cx))) = o;
+      }
+    }
+  }
+
+  if (!ok) {
+    // A stage never completed: record it, then wait (bounded) for the copies
+    // this warp still has in flight (stages k .. issued-1) before it exits.
+    if (lane == 0) atomicOr(&g_decompress_fault, kFaultDecompressWait);
+    const int n_issued = __shfl_sync(kFullMask, issued, 0);
+    for (int kk = k; kk < n_issued; ++kk) {
+      mbar_wait(bar0 + 8 * cs, cphase);
+      if (++cs == D) {
+        cs = 0;
+        cphase ^= 1u;
       }
     }
   }
@@ -92,31 +177,37 @@ decompress_reduce_kernel(DecompressArgs a) {
 
 }  // namespace
 
-constexpr int kDecompressCH = 4;
+int decompress_tile_blocks(int block) { return 32 / (block / 64); }
 
-int decompress_tile_blocks(int block) { return 32 / (block / (8 * kDecompressCH)); }
+size_t decompress_smem_bytes() {
+  return static_cast<size_t>(kDecompressThreads / 32) * kDecompressStages * (kStageBytes + 8);
+}
 
 const void* decompress_kernel_ptr(int block) {
   switch (block) {
-    case 64: return reinterpret_cast<const void*>(decompress_reduce_kernel<64, kDecompressCH>);
-    case 128: return reinterpret_cast<const void*>(decompress_reduce_kernel<128, kDecompressCH>);
-    default: return reinterpret_cast<const void*>(decompress_reduce_kernel<256, kDecompressCH>);
+    case 64: return reinterpret_cast<const void*>(decompress_reduce_kernel<64>);
+    case 128: return reinterpret_cast<const void*>(decompress_reduce_kernel<128>);
+    default: return reinterpret_cast<const void*>(decompress_reduce_kernel<256>);
   }
 }
 
 cudaError_t launch_decompress(const DecompressArgs& a, int block, int grid, cudaStream_t stream) {
+  const size_t smem = decompress_smem_bytes();
   switch (block) {
-    case 64:
-      decompress_reduce_kernel<64, kDecompressCH><<<grid, kDecompressThreads, 0, stream>>>(a);
-      break;
-    case 128:
-      decompress_reduce_kernel<128, kDecompressCH><<<grid, kDecompressThreads, 0, stream>>>(a);
-      break;
-    default:
-      decompress_reduce_kernel<256, kDecompressCH><<<grid, kDecompressThreads, 0, stream>>>(a);
-      break;
+    case 64: decompress_reduce_kernel<64><<<grid, kDecompressThreads, smem, stream>>>(a); break;
+    case 128: decompress_reduce_kernel<128><<<grid, kDecompressThreads, smem, stream>>>(a); break;
+    default: decompress_reduce_kernel<256><<<grid, kDecompressThreads, smem, stream>>>(a); break;
   }
   return cudaGetLastError();
+}
+
+cudaError_t decompress_fault(unsigned int* bits, bool clear) {
+  cudaError_t e = cudaMemcpyFromSymbol(bits, g_decompress_fault, sizeof(unsigned int));
+  if (e == cudaSuccess && clear) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_decompress_fault, &zero, sizeof(unsigned int));
+  }
+  return e;
 }
 
 }  // namespace taco

@@ -9,9 +9,6 @@
 
 namespace taco {
 
-cudaError_t launch_e4m3_encode(const float* in, uint8_t* out, int64_t n, cudaStream_t st);
-cudaError_t launch_e4m3_decode(const uint8_t* in, float* out, int64_t n, cudaStream_t st);
-
 namespace {
 
 constexpr int64_t kMaxElements = int64_t{1} << 40;   // per shard
@@ -57,13 +54,23 @@ cudaError_t device_info(const DeviceInfo** out) {
     DeviceInfo& d = g_info[dev];
     cudaError_t err = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
     const int blocks[3] = {64, 128, 256};
+    const int csmem = static_cast<int>(compress_smem_bytes());
+    const int dsmem = static_cast<int>(decompress_smem_bytes());
     for (int b = 0; b < 3 && err == cudaSuccess; ++b) {
-      for (int v = 0; v < 2 && err == cudaSuccess; ++v)
-        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &d.occ_compress[b][v], compress_kernel_ptr(blocks[b], v), kCompressThreads, 0);
-      if (err == cudaSuccess)
-        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &d.occ_decompress[b], decompress_kernel_ptr(blocks[b]), kDecompressThreads, 0);
+      for (int v = 0; v < 2 && err == cudaSuccess; ++v) {
+        const void* k = compress_kernel_ptr(blocks[b], v);
+        err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, csmem);
+        if (err == cudaSuccess)
+          err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ_compress[b][v], k,
+                                                              kCompressThreads, csmem);
+      }
+      if (err == cudaSuccess) {
+        const void* k = decompress_kernel_ptr(blocks[b]);
+        err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dsmem);
+        if (err == cudaSuccess)
+          err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ_decompress[b], k,
+                                                              kDecompressThreads, dsmem);
+      }
     }
     g_info_err[dev] = err;
   });
@@ -252,6 +259,25 @@ taco_status taco_e4m3_decode_f32(const uint8_t* in, float* out, int64_t n, void*
   if (!in || !out) return TACO_ERR_NULL;
   if (!aligned(out, 4)) return TACO_ERR_ALIGN;
   return launch_e4m3_decode(in, out, n, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? TACO_OK
+             : TACO_ERR_CUDA;
+}
+
+taco_status taco_get_fault(uint32_t* bits, int clear) {
+  if (!bits) return TACO_ERR_NULL;
+  unsigned int c = 0, d = 0, t = 0;
+  if (compress_fault(&c, clear != 0) != cudaSuccess) return TACO_ERR_CUDA;
+  if (decompress_fault(&d, clear != 0) != cudaSuccess) return TACO_ERR_CUDA;
+  if (selftest_fault(&t, clear != 0) != cudaSuccess) return TACO_ERR_CUDA;
+  *bits = c | d | t;
+  return TACO_OK;
+}
+
+taco_status taco_selftest_wait_timeout(uint64_t limit_ns, uint32_t* status_dev, void* stream) {
+  if (!status_dev) return TACO_ERR_NULL;
+  if (!aligned(status_dev, 4)) return TACO_ERR_ALIGN;
+  if (limit_ns == 0 || limit_ns > 2000000000ull) return TACO_ERR_ARG;
+  return launch_selftest_wait(limit_ns, status_dev, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? TACO_OK
              : TACO_ERR_CUDA;
 }

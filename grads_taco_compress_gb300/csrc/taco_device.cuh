@@ -1,17 +1,19 @@
 // Device helpers shared by the compress and decompress-reduce kernels.
 //
 // Element ownership inside one block of NB elements (both kernels):
-//   a block is spread over LPB = NB / (8*CH) consecutive lanes of a warp; lane
-//   j (0 <= j < LPB) of the block holds CH chunks of 8 contiguous elements,
-//   chunk slot v holding block chunk c = j + LPB*v, i.e. elements 8c .. 8c+7.
-//   Element index e = 8c + k therefore has
-//     bits 0..2                  -> k  (register index inside a chunk)
-//     bits 3 .. 3+log2(LPB)-1    -> j  (lane inside the block)
-//     the remaining high bits    -> v  (chunk slot)
+//   a block is spread over LPB = NB / 64 consecutive lanes of a warp (each
+//   lane holds 64 elements); lane j (0 <= j < LPB) of the block holds 8
+//   chunks of 8 contiguous elements. Register slot v (0..7) of lane j holds
+//   block chunk  j + LPB * (v ^ c),  c = (block index in the warp tile) & 7.
+//   The XOR by c makes the 16-byte shared-memory reads of a warp hit distinct
+//   banks when the tile was copied contiguously into shared memory.
+//   Element index e = 8 * chunk + k therefore has
+//     bits 0..2                  -> k        (register index inside a chunk)
+//     bits 3 .. 3+log2(LPB)-1    -> j        (lane inside the block)
+//     bits 3+log2(LPB) ..        -> v ^ c    (chunk slot)
 // The Sylvester Hadamard transform H_NB = H_2 (x) ... (x) H_2 acts on each
-// index bit independently, so the bits held in registers are transformed in
-// registers and the lane bits with warp shuffles. Every warp load of a chunk
-// slot reads LPB*16 contiguous bytes of each block (whole 32-byte sectors).
+// index bit independently: the bits held in registers are transformed in
+// registers (packed f32x2 arithmetic), the lane bits with warp shuffles.
 #pragma once
 
 #include <cstdint>
@@ -21,40 +23,58 @@
 namespace taco {
 
 constexpr unsigned kFullMask = 0xffffffffu;
+constexpr int kCH = 8;                       // chunks of 8 elements per lane
+constexpr int kTileElems = 32 * 8 * kCH;     // elements of one warp tile (2048)
 
-// ---------------------------------------------------------------- loads ----
-__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
-  uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
+// Wall-clock limit of one wait on an mbarrier before the kernel gives up.
+constexpr unsigned long long kWaitLimitNs = 1000ull * 1000ull * 1000ull;   // 1 s
+
+// Device fault bits (taco_get_fault in taco.h).
+constexpr unsigned kFaultCompressWait = 1u;
+constexpr unsigned kFaultDecompressWait = 2u;
+constexpr unsigned kFaultSelftestWait = 4u;
+
+// ------------------------------------------------------------- f32 pairs ----
+// Two fp32 values in one 64-bit register pair, for the packed f32x2 ALU ops.
+struct __align__(8) f2 {
+  float x, y;
+};
+
+__device__ __forceinline__ unsigned long long as_u64(f2 v) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(v.x), "f"(v.y));
   return r;
 }
-
-__device__ __forceinline__ uint2 ld_stream_v2(const void* p) {
-  uint2 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
-               : "=r"(r.x), "=r"(r.y)
-               : "l"(p));
-  return r;
+__device__ __forceinline__ f2 as_f2(unsigned long long r) {
+  f2 v;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+  return v;
 }
-
-__device__ __forceinline__ float ld_stream_f32(const float* p) {
-  float r;
-  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(r) : "l"(p));
-  return r;
+__device__ __forceinline__ f2 add2(f2 a, f2 b) {
+  unsigned long long r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(as_u64(a)), "l"(as_u64(b)));
+  return as_f2(r);
+}
+__device__ __forceinline__ f2 sub2(f2 a, f2 b) {
+  unsigned long long r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(as_u64(a)), "l"(as_u64(b)));
+  return as_f2(r);
+}
+__device__ __forceinline__ f2 mul2(f2 a, f2 b) {
+  unsigned long long r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(as_u64(a)), "l"(as_u64(b)));
+  return as_f2(r);
+}
+// a * b + c, one rounding per lane
+__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
+  unsigned long long r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(as_u64(a)), "l"(as_u64(b)), "l"(as_u64(c)));
+  return as_f2(r);
 }
 
 // ----------------------------------------------------------- bf16 <-> f32 --
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
-__device__ __forceinline__ void unpack_bf16x8(const uint4& r, float (&x)[8]) {
-  x[0] = bf16_lo(r.x); x[1] = bf16_hi(r.x);
-  x[2] = bf16_lo(r.y); x[3] = bf16_hi(r.y);
-  x[4] = bf16_lo(r.z); x[5] = bf16_hi(r.z);
-  x[6] = bf16_lo(r.w); x[7] = bf16_hi(r.w);
-}
 
 // Two fp32 -> bf16x2, round to nearest even (lo in the low half).
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -78,42 +98,137 @@ __device__ __forceinline__ uint32_t e4m3x4_from_f32(float a, float b, float c, f
 }
 
 // Two E4M3 codes (low byte first) -> two exact fp32 values.
-__device__ __forceinline__ float2 e4m3x2_to_f32(uint32_t two_codes) {
+__device__ __forceinline__ f2 e4m3x2_to_f2(uint32_t two_codes) {
   uint32_t h2;
   const uint16_t c = static_cast<uint16_t>(two_codes);
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
-  return __half22float2(*reinterpret_cast<const __half2*>(&h2));
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+  return f2{f.x, f.y};
+}
+
+// ------------------------------------------------- shared memory / TMA ----
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 r;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(addr));
+  return r;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 r;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(addr));
+  return r;
+}
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+  float r;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(r) : "r"(addr));
+  return r;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
+}
+// Make initialised barriers visible to the async (TMA) proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+// Order this thread's earlier generic-proxy shared-memory accesses before
+// later async-proxy (TMA) writes to the same buffer.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes)
+               : "memory");
+}
+// 1-D bulk copy global -> shared (TMA), completion counted on `bar`.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void tma_load_1d(uint32_t dst, const void* src, uint32_t bytes,
+                                            uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;"
+      :: "r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy) : "memory");
+}
+// L2 policy for data read once: evict first.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase of `bar` with parity `parity`; false after `limit_ns`
+// of wall-clock time without completion.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+  return true;
 }
 
 // ---------------------------------------------------------- block FWHT -----
-// Butterflies on the index bits held in registers: bits 0..2 inside each
-// chunk, then the chunk-slot bits. Unnormalised (H_NB, entries +-1).
+// Butterflies on the index bits held in registers (unnormalised H, entries
+// +-1). x[q][i] is the f32 pair (elements 2i, 2i+1) of register chunk q.
+// `c` is the lane's chunk-slot XOR: register chunk q holds chunk slot q ^ c,
+// so for the slot bits the register holding the lower slot of a pair depends
+// on c; that butterfly is written as two fmas with a lane-constant sign.
 template <int CH>
-__device__ __forceinline__ void fwht_in_registers(float (&x)[CH][8]) {
+__device__ __forceinline__ void fwht_in_registers(f2 (&x)[CH][4], int c) {
 #pragma unroll
-  for (int v = 0; v < CH; ++v) {
+  for (int q = 0; q < CH; ++q) {
+    // element bit 0: inside each pair
 #pragma unroll
-    for (int m = 1; m < 8; m <<= 1) {
+    for (int i = 0; i < 4; ++i) {
+      const float a = x[q][i].x, b = x[q][i].y;
+      x[q][i] = f2{a + b, a - b};
+    }
+    // element bits 1 and 2: whole pairs
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+    for (int m = 1; m < 4; m <<= 1) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
         if ((i & m) == 0) {
-          const float a = x[v][i], b = x[v][i + m];
-          x[v][i] = a + b;
-          x[v][i + m] = a - b;
+          const f2 a = x[q][i], b = x[q][i + m];
+          x[q][i] = add2(a, b);
+          x[q][i + m] = sub2(a, b);
         }
       }
     }
   }
+  // chunk-slot bits
 #pragma unroll
   for (int m = 1; m < CH; m <<= 1) {
+    const float sg = (c & m) ? -1.0f : 1.0f;
+    const f2 sgn{sg, sg}, nsgn{-sg, -sg};
 #pragma unroll
-    for (int v = 0; v < CH; ++v) {
-      if ((v & m) == 0) {
+    for (int q = 0; q < CH; ++q) {
+      if ((q & m) == 0) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float a = x[v][i], b = x[v + m][i];
-          x[v][i] = a + b;
-          x[v + m][i] = a - b;
+        for (int i = 0; i < 4; ++i) {
+          const f2 a = x[q][i], b = x[q + m][i];
+          x[q][i] = fma2(a, sgn, b);       // c&m == 0: a + b ; else b - a
+          x[q + m][i] = fma2(b, nsgn, a);  // c&m == 0: a - b ; else a + b
         }
       }
     }
@@ -124,16 +239,17 @@ __device__ __forceinline__ void fwht_in_registers(float (&x)[CH][8]) {
 // partner keeps a - b (a = the element with the bit clear). One exact
 // multiply by +-1 and one rounded add, as in the register stages.
 template <int CH, int LPB>
-__device__ __forceinline__ void fwht_across_lanes(float (&x)[CH][8], int j) {
+__device__ __forceinline__ void fwht_across_lanes(f2 (&x)[CH][4], int j) {
 #pragma unroll
   for (int m = 1; m < LPB; m <<= 1) {
-    const float sgn = (j & m) ? -1.0f : 1.0f;
+    const float sg = (j & m) ? -1.0f : 1.0f;
+    const f2 sgn{sg, sg};
 #pragma unroll
-    for (int v = 0; v < CH; ++v) {
+    for (int q = 0; q < CH; ++q) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float p = __shfl_xor_sync(kFullMask, x[v][i], m);
-        x[v][i] = fmaf(x[v][i], sgn, p);
+      for (int i = 0; i < 4; ++i) {
+        const f2 p{__shfl_xor_sync(kFullMask, x[q][i].x, m), __shfl_xor_sync(kFullMask, x[q][i].y, m)};
+        x[q][i] = fma2(x[q][i], sgn, p);
       }
     }
   }
@@ -152,6 +268,17 @@ __device__ __forceinline__ float block_max(float v) {
 #pragma unroll
   for (int m = 1; m < LPB; m <<= 1) v = fmaxf(v, __shfl_xor_sync(kFullMask, v, m));
   return v;
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+__device__ __forceinline__ float min3(float a, float b, float c) {
+  float r;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
 }  // namespace taco

@@ -11,7 +11,11 @@
 namespace taco {
 
 constexpr int kCompressThreads = 256;
+constexpr int kCompressMinBlocks = 2;     // CTAs per SM the register budget allows
+constexpr int kCompressStages = 3;        // warp tiles (4 KB each) in flight per warp
 constexpr int kDecompressThreads = 256;
+constexpr int kDecompressMinBlocks = 2;
+constexpr int kDecompressStages = 4;      // (tile, shard) stages in flight per warp
 
 // Workspace of compress: per shard one arrival counter (16 bytes) followed by
 // one (max s, count) pair per CTA of the shard's grid row.
@@ -46,12 +50,21 @@ struct DecompressArgs {
 };
 
 int compress_tile_blocks(int block);
+size_t compress_smem_bytes();
 const void* compress_kernel_ptr(int block, int variant);
 cudaError_t launch_compress(const CompressArgs& a, int block, int variant, int grid_x, int P,
                             cudaStream_t stream);
+cudaError_t compress_fault(unsigned int* bits, bool clear);
 
 int decompress_tile_blocks(int block);
+size_t decompress_smem_bytes();
 const void* decompress_kernel_ptr(int block);
 cudaError_t launch_decompress(const DecompressArgs& a, int block, int grid, cudaStream_t stream);
+cudaError_t decompress_fault(unsigned int* bits, bool clear);
+
+cudaError_t launch_e4m3_encode(const float* in, uint8_t* out, int64_t n, cudaStream_t st);
+cudaError_t launch_e4m3_decode(const uint8_t* in, float* out, int64_t n, cudaStream_t st);
+cudaError_t launch_selftest_wait(unsigned long long limit_ns, uint32_t* status, cudaStream_t st);
+cudaError_t selftest_fault(unsigned int* bits, bool clear);
 
 }  // namespace taco

@@ -178,6 +178,25 @@ taco_status taco_decompress_reduce_ptrs(const void* const* shards, int P, int64_
 taco_status taco_e4m3_encode_f32(const float* in, uint8_t* out, int64_t n, void* stream);
 taco_status taco_e4m3_decode_f32(const uint8_t* in, float* out, int64_t n, void* stream);
 
+/* ---- Device faults ---------------------------------------------------------
+ * The kernels wait on shared-memory barriers for their bulk copies; each wait
+ * gives up after one second of wall-clock time, sets a bit in a device-side
+ * fault word of the library, lets the copies still in flight land (again
+ * bounded) and returns, so that a fault never hangs the GPU. Bits:
+ *   TACO_FAULT_COMPRESS_WAIT, TACO_FAULT_DECOMPRESS_WAIT, TACO_FAULT_SELFTEST_WAIT.
+ * taco_get_fault reads (and with clear != 0 resets) the word of the current
+ * device; it synchronises with the device. */
+#define TACO_FAULT_COMPRESS_WAIT 1u
+#define TACO_FAULT_DECOMPRESS_WAIT 2u
+#define TACO_FAULT_SELFTEST_WAIT 4u
+taco_status taco_get_fault(uint32_t* bits, int clear);
+
+/* Self-test of that time-out path: one warp waits on a barrier that nothing
+ * completes, for limit_ns (1 .. 2e9) nanoseconds, then writes 1 to
+ * *status_dev (a device word) and sets TACO_FAULT_SELFTEST_WAIT; 0 would
+ * mean the wait completed, which it cannot. */
+taco_status taco_selftest_wait_timeout(uint64_t limit_ns, uint32_t* status_dev, void* stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* taco_status_string(taco_status status);
 

@@ -148,3 +148,12 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(tb, "_LIB", None)
     with pytest.raises(RuntimeError, match="not built"):
         tb.shard_bytes(4, 256, 128)
+
+
+@no_gpu_only
+def test_fault_api_rejects(lib):
+    assert lib.taco_get_fault(None, 0) == NULL
+    assert lib.taco_selftest_wait_timeout(1000, None, None) == NULL
+    assert lib.taco_selftest_wait_timeout(1000, A + 2, None) == ALIGN
+    assert lib.taco_selftest_wait_timeout(0, A, None) == ARG
+    assert lib.taco_selftest_wait_timeout(3_000_000_000, A, None) == ARG

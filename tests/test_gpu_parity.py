@@ -173,7 +173,6 @@ def test_compress_deterministic_and_workspace_reset():
     b2, h2 = tb.taco_compress_shards(x, w.block, workspace=ws)
     torch.cuda.synchronize()
     assert torch.equal(b1, b2) and torch.equal(h1, h2)
-    assert int(ws.count_nonzero()) == 0 or bool((ws.view(-1)[:4] == 0).all())
     counters = ws.view(torch.uint8).reshape(2, -1)[:, :4]
     assert int(counters.count_nonzero()) == 0
 
@@ -316,3 +315,8 @@ def test_full_size_decompress_reduce_sampled(name):
     want = O.decompress_reduce(codes[:, rows], alpha[:, rows], s[:, rows], w.block)
     parity.compare_recon(O.bf16_bits_to_f64(got[rows]), O.bf16_bits_to_f64(want))
     assert np.all(np.isfinite(O.bf16_bits_to_f64(got)))
+
+
+def test_no_kernel_wait_timed_out():
+    """After every launch above, no bounded wait of any kernel gave up."""
+    assert tb.taco_get_fault() == 0
