@@ -34,7 +34,7 @@ assert HEADER_DTYPE.itemsize == HEADER_BYTES
 
 #: every symbol include/taco.h declares
 EXPORTED_SYMBOLS = (
-    "taco_shard_bytes", "taco_shard_alpha_offset", "taco_shard_s_offset",
+    "taco_shard_bytes", "taco_shard_scales_offset",
     "taco_workspace_bytes", "taco_compress", "taco_compress_shards",
     "taco_compress_shards_noalloc",
     "taco_decompress_reduce", "taco_decompress_reduce_ptrs",
@@ -66,8 +66,7 @@ def _lib() -> ctypes.CDLL:
                                  ctypes.c_void_p, ctypes.c_float)
         sig = {
             "taco_shard_bytes": (sz, [i64, i64, i32]),
-            "taco_shard_alpha_offset": (sz, [i64, i64, i32]),
-            "taco_shard_s_offset": (sz, [i64, i64, i32]),
+            "taco_shard_scales_offset": (sz, [i64, i64, i32]),
             "taco_workspace_bytes": (sz, [i32]),
             "taco_compress": (i32, [vp, i64, i64, i32, f32, i32, vp, vp, vp, sz, vp]),
             "taco_compress_shards": (i32, [vp, i32, i64, i64, i32, f32, i32, vp, vp, vp, sz, vp]),
@@ -113,9 +112,9 @@ def shard_bytes(N: int, h: int, block: int) -> int:
     return int(_lib().taco_shard_bytes(N, h, block))
 
 
-def shard_offsets(N: int, h: int, block: int) -> tuple[int, int]:
-    lib = _lib()
-    return int(lib.taco_shard_alpha_offset(N, h, block)), int(lib.taco_shard_s_offset(N, h, block))
+def shard_scales_offset(N: int, h: int, block: int) -> int:
+    """Byte offset of the (alpha, s) pairs inside a shard."""
+    return int(_lib().taco_shard_scales_offset(N, h, block))
 
 
 def workspace_bytes(P: int) -> int:
@@ -130,13 +129,12 @@ def new_workspace(P: int = MAX_SHARDS, device=None) -> torch.Tensor:
 def shard_views(bundle: torch.Tensor, P: int, N: int, h: int, block: int):
     """Views (codes u8 [P,N,h], alpha f32 [P,N,K], s f32 [P,N,K]) into a bundle."""
     sb = shard_bytes(N, h, block)
-    a_off, s_off = shard_offsets(N, h, block)
+    off = shard_scales_offset(N, h, block)
     K = h // block
     flat = bundle.view(torch.uint8).reshape(-1)[: P * sb].view(P, sb)
     codes = flat[:, : N * h].reshape(P, N, h)
-    alpha = flat[:, a_off: a_off + 4 * N * K].view(torch.float32).view(P, N, K)
-    s = flat[:, s_off: s_off + 4 * N * K].view(torch.float32).view(P, N, K)
-    return codes, alpha, s
+    scales = flat[:, off: off + 8 * N * K].view(torch.float32).view(P, N, K, 2)
+    return codes, scales[..., 0], scales[..., 1]
 
 
 def parse_headers(headers: torch.Tensor) -> np.ndarray:

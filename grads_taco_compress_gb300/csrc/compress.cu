@@ -9,8 +9,8 @@
 //   shuffles (the rotation is linear, so alpha is applied afterwards together
 //   with 1/sqrt(n) and 1/s) -> alpha = sqrt(E*/E), s = max(1, alpha/sqrt(n) *
 //   max|Hx| / 448) -> E4M3 codes with cvt.rn.satfinite (8-byte stores),
-//   alpha and s stores -> per-tensor header through per-CTA partials and a
-//   last-CTA reduction.
+//   one (alpha, s) pair store per block -> per-tensor header through per-CTA
+//   partials and a last-CTA reduction.
 // Grid: gridDim.y = shard, gridDim.x persistent CTAs per shard. Each warp
 // walks warp tiles (2048 elements, 32/LPB blocks) with a stride of the grid
 // row and keeps kCompressStages tiles in flight: lane 0 issues a 1-D
@@ -57,8 +57,7 @@ compress_kernel(CompressArgs a) {
   const uint16_t* __restrict__ x = a.x + static_cast<int64_t>(shard) * a.shard_elems;
   uint8_t* shard_base = a.bundle + static_cast<size_t>(shard) * a.shard_bytes;
   uint8_t* __restrict__ codes = shard_base;
-  float* __restrict__ alpha_out = reinterpret_cast<float*>(shard_base + a.alpha_off);
-  float* __restrict__ s_out = reinterpret_cast<float*>(shard_base + a.s_off);
+  float2* __restrict__ scales_out = reinterpret_cast<float2*>(shard_base + a.scales_off);
 
   const int64_t nblocks = a.nblocks;
   const int tiles = static_cast<int>((nblocks + BPT - 1) / BPT);
@@ -69,30 +68,30 @@ compress_kernel(CompressArgs a) {
   const uint32_t tail_bytes =
       static_cast<uint32_t>(nblocks - static_cast<int64_t>(tiles - 1) * BPT) * (NB * 2);
 
-  // Producer state (lane 0): next tile to bring in, its source, its stage.
-  int it = 0, is = 0;
-  const uint16_t* isrc = x + static_cast<int64_t>(t0) * kTileElems;
-  const int64_t src_step = static_cast<int64_t>(stride) * kTileElems;
-  uint64_t policy = 0;
   if (lane == 0) {
     for (int s = 0; s < D; ++s) mbar_init(bar0 + 8 * s, 1);
     fence_mbar_init();
-    policy = l2_evict_first_policy();
   }
   __syncwarp();
+  const uint64_t policy = l2_evict_first_policy();
 
-  auto issue_next = [&]() {   // lane 0 only
-    const uint32_t bytes = (t0 + it * stride == tiles - 1) ? tail_bytes : TILE_BYTES;
-    fence_proxy_async_smem();
-    mbar_arrive_expect_tx(bar0 + 8 * is, bytes);
-    tma_load_1d(stage0 + is * TILE_BYTES, isrc, bytes, bar0 + 8 * is, policy);
+  // Producer state, kept identical in every lane (lane 0 issues the copy):
+  // next tile number `it` of this warp, its source and its stage.
+  int it = 0, is = 0;
+  const uint16_t* isrc = x + static_cast<int64_t>(t0) * kTileElems;
+  const int64_t src_step = static_cast<int64_t>(stride) * kTileElems;
+  auto issue_next = [&]() {
+    if (lane == 0) {
+      const uint32_t bytes = (t0 + it * stride == tiles - 1) ? tail_bytes : TILE_BYTES;
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(bar0 + 8 * is, bytes);
+      tma_load_1d(stage0 + is * TILE_BYTES, isrc, bytes, bar0 + 8 * is, policy);
+    }
     ++it;
     isrc += src_step;
     is = (is + 1 == D) ? 0 : is + 1;
   };
-  if (lane == 0) {
-    while (it < D - 1 && it < count) issue_next();
-  }
+  while (it < D - 1 && it < count) issue_next();
 
   float part_smax = 0.0f;   // header partials of this thread (lane j == 0 only)
   uint32_t part_cnt = 0;
@@ -101,7 +100,7 @@ compress_kernel(CompressArgs a) {
   bool ok = true;
 
   for (; k < count; ++k) {
-    if (lane == 0 && it < count) issue_next();
+    if (it < count) issue_next();
     const bool got = mbar_wait(bar0 + 8 * cs, cphase);
     if (!__all_sync(kFullMask, got)) {   // keep the warp's decision uniform
       ok = false;
@@ -128,38 +127,42 @@ compress_kernel(CompressArgs a) {
       cphase ^= 1u;
     }
 
-    // Block energy e = sum x^2 (E = e / NB): packed partial sums, then lanes.
-    f2 ea{0.f, 0.f}, eb{0.f, 0.f};
+    // Block energy e = sum x^2 (E = e / NB): four packed accumulators, then
+    // the lanes of the block.
+    f2 ea[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
-    for (int q = 0; q < kCH; ++q) {
-      ea = fma2(v[q][0], v[q][0], ea);
-      eb = fma2(v[q][1], v[q][1], eb);
-      ea = fma2(v[q][2], v[q][2], ea);
-      eb = fma2(v[q][3], v[q][3], eb);
-    }
-    const float e = block_sum<LPB>((ea.x + ea.y) + (eb.x + eb.y));
+    for (int q = 0; q < kCH; ++q)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) ea[i] = fma2(v[q][i], v[q][i], ea[i]);
+    const f2 e01 = add2(ea[0], ea[1]), e23 = add2(ea[2], ea[3]);
+    const float e = block_sum<LPB>((e01.x + e01.y) + (e23.x + e23.y));
+
+    // alpha = sqrt(E*/E) = sqrt(n E*) / sqrt(e): reciprocal square root with
+    // one Newton step (error about one ulp); 1 for an all-zero block. It does
+    // not depend on the rotation, so its latency overlaps the FWHT.
+    float r = rsqrtf(e);
+    r = fmaf(fmaf(-0.5f * e * r, r, 0.5f), r, r);
+    const float alpha = (e > 0.f) ? a.sqrt_nE * r : 1.0f;
+    const float cscale = alpha * a.inv_sqrt_n;        // y = cscale * t
 
     // Rotation of the raw block: t = H x.
     fwht_in_registers<kCH>(v, cx);
     fwht_across_lanes<kCH, LPB>(v, j);
 
-    // max |t| = max(max t, -min t)
-    float hi = v[0][0].x, lo = v[0][0].x;
+    // max |t| = max(max t, -min t): a tree of 3-input max / min per chunk,
+    // then over the chunks.
+    float hq[kCH], lq[kCH];
 #pragma unroll
-    for (int q = 0; q < kCH; ++q)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        hi = max3(hi, v[q][i].x, v[q][i].y);
-        lo = min3(lo, v[q][i].x, v[q][i].y);
-      }
+    for (int q = 0; q < kCH; ++q) {
+      hq[q] = max3(max3(v[q][0].x, v[q][0].y, v[q][1].x), max3(v[q][1].y, v[q][2].x, v[q][2].y),
+                   fmaxf(v[q][3].x, v[q][3].y));
+      lq[q] = min3(min3(v[q][0].x, v[q][0].y, v[q][1].x), min3(v[q][1].y, v[q][2].x, v[q][2].y),
+                   fminf(v[q][3].x, v[q][3].y));
+    }
+    const float hi = max3(max3(hq[0], hq[1], hq[2]), max3(hq[3], hq[4], hq[5]), fmaxf(hq[6], hq[7]));
+    const float lo = min3(min3(lq[0], lq[1], lq[2]), min3(lq[3], lq[4], lq[5]), fminf(lq[6], lq[7]));
     const float tmax = block_max<LPB>(fmaxf(hi, -lo));
 
-    // alpha = sqrt(E*/E) = sqrt(n E*) / sqrt(e): reciprocal square root with
-    // one Newton step (error about one ulp); 1 for an all-zero block.
-    float r = rsqrtf(e);
-    r = fmaf(fmaf(-0.5f * e * r, r, 0.5f), r, r);
-    const float alpha = (e > 0.f) ? a.sqrt_nE * r : 1.0f;
-    const float cscale = alpha * a.inv_sqrt_n;        // y = cscale * t
     const float amax = cscale * tmax;
     const float sc = (VARIANT == 0) ? fmaxf(1.0f, amax * (1.0f / 448.0f))
                                     : (amax > 0.f ? amax * (1.0f / 448.0f) : 1.0f);
@@ -178,8 +181,7 @@ compress_kernel(CompressArgs a) {
         *reinterpret_cast<uint2*>(cp + 8 * (j + LPB * (q ^ cx))) = w;
       }
       if (j == 0) {
-        alpha_out[b] = alpha;
-        s_out[b] = sc;
+        scales_out[b] = make_float2(alpha, sc);
         part_smax = fmaxf(part_smax, sc);
         part_cnt += (sc > 1.0f) ? 1u : 0u;
       }
@@ -190,8 +192,7 @@ compress_kernel(CompressArgs a) {
     // A stage never completed: record it, then wait (bounded) for the copies
     // this warp still has in flight (tiles k .. it-1) before the CTA may exit.
     if (lane == 0) atomicOr(&g_compress_fault, kFaultCompressWait);
-    const int issued = __shfl_sync(kFullMask, it, 0);
-    for (int kk = k; kk < issued; ++kk) {
+    for (int kk = k; kk < it; ++kk) {
       mbar_wait(bar0 + 8 * cs, cphase);
       if (++cs == D) {
         cs = 0;

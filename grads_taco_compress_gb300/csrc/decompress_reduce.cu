@@ -10,8 +10,8 @@
 // sum can be taken before the rotation because the rotation is linear.
 // Each warp walks warp tiles (2048 elements) with a stride of the grid. For
 // one tile it consumes P stages, one per shard; lane 0 keeps
-// kDecompressStages stages in flight, each a set of three 1-D cp.async.bulk
-// copies (the tile's codes, alphas and s values) completed on one mbarrier.
+// kDecompressStages stages in flight, each a pair of 1-D cp.async.bulk
+// copies (the tile's codes and its (alpha, s) pairs) completed on one mbarrier.
 // Codes are decoded in pairs with cvt.rn.f16x2.e4m3x2 and accumulated with
 // packed f32x2 FMAs; the output leaves as 16-byte bf16 stores.
 
@@ -25,8 +25,8 @@ namespace {
 __device__ unsigned int g_decompress_fault;
 
 constexpr uint32_t kCodesBytes = kTileElems;          // codes of one tile
-constexpr uint32_t kScaleBytes = 128;                 // alphas (or s) of one tile, padded
-constexpr uint32_t kStageBytes = kCodesBytes + 2 * kScaleBytes;
+constexpr uint32_t kScaleBytes = 256;                 // (alpha, s) pairs of one tile
+constexpr uint32_t kStageBytes = kCodesBytes + kScaleBytes;
 
 template <int NB>
 __global__ void __launch_bounds__(kDecompressThreads, kDecompressMinBlocks)
@@ -36,7 +36,7 @@ decompress_reduce_kernel(DecompressArgs a) {
   constexpr int D = kDecompressStages;
   constexpr int WARPS = kDecompressThreads / 32;
   static_assert(LPB >= 1 && LPB <= 4, "block size");
-  static_assert(BPT * 4 <= kScaleBytes, "scale slot");
+  static_assert(BPT * 8 <= kScaleBytes, "scale slot");
 
   extern __shared__ __align__(128) unsigned char smem[];
 
@@ -58,34 +58,35 @@ decompress_reduce_kernel(DecompressArgs a) {
   const int count = ntiles * P;                       // stages of this warp
   const uint32_t vb_tail = static_cast<uint32_t>(nblocks - static_cast<int64_t>(tiles - 1) * BPT);
 
-  // Producer state (lane 0): next stage = (tile number it_t of this warp,
-  // shard ip), its slot is, and the byte offsets of that tile in a shard.
-  int issued = 0, it_t = 0, ip = 0, is = 0;
-  int64_t code_off = static_cast<int64_t>(t0) * kTileElems;
-  int64_t scale_off = static_cast<int64_t>(t0) * BPT * 4;
-  const int64_t code_step = static_cast<int64_t>(stride) * kTileElems;
-  const int64_t scale_step = static_cast<int64_t>(stride) * BPT * 4;
-  uint64_t policy = 0;
   if (lane == 0) {
     for (int s = 0; s < D; ++s) mbar_init(bar0 + 8 * s, 1);
     fence_mbar_init();
-    policy = l2_evict_first_policy();
   }
   __syncwarp();
+  const uint64_t policy = l2_evict_first_policy();
 
-  auto issue_next = [&]() {   // lane 0 only
-    const bool tail = (t0 + it_t * stride == tiles - 1);
-    const uint32_t vb = tail ? vb_tail : static_cast<uint32_t>(BPT);
-    const uint32_t cbytes = vb * NB;
-    const uint32_t sbytes = (vb * 4 + 15) & ~15u;     // stays inside the 256-byte padding
-    const uint32_t dst = stage0 + is * kStageBytes;
-    const uint32_t bar = bar0 + 8 * is;
-    const uint8_t* base = a.shard[ip];
-    fence_proxy_async_smem();
-    mbar_arrive_expect_tx(bar, cbytes + 2 * sbytes);
-    tma_load_1d(dst, base + code_off, cbytes, bar, policy);
-    tma_load_1d(dst + kCodesBytes, base + a.alpha_off + scale_off, sbytes, bar, policy);
-    tma_load_1d(dst + kCodesBytes + kScaleBytes, base + a.s_off + scale_off, sbytes, bar, policy);
+  // Producer state, kept identical in every lane (lane 0 issues the copies):
+  // next stage = (tile number it_t of this warp, shard ip), its slot is, and
+  // the byte offsets of that tile inside a shard.
+  int issued = 0, it_t = 0, ip = 0, is = 0;
+  int64_t code_off = static_cast<int64_t>(t0) * kTileElems;
+  int64_t scale_off = a.scales_off + static_cast<int64_t>(t0) * BPT * 8;
+  const int64_t code_step = static_cast<int64_t>(stride) * kTileElems;
+  const int64_t scale_step = static_cast<int64_t>(stride) * BPT * 8;
+  auto issue_next = [&]() {
+    if (lane == 0) {
+      const bool tail = (t0 + it_t * stride == tiles - 1);
+      const uint32_t vb = tail ? vb_tail : static_cast<uint32_t>(BPT);
+      const uint32_t cbytes = vb * NB;
+      const uint32_t sbytes = (vb * 8 + 15) & ~15u;   // stays inside the 256-byte padding
+      const uint32_t dst = stage0 + is * kStageBytes;
+      const uint32_t bar = bar0 + 8 * is;
+      const uint8_t* base = a.shard[ip];
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(bar, cbytes + sbytes);
+      tma_load_1d(dst, base + code_off, cbytes, bar, policy);
+      tma_load_1d(dst + kCodesBytes, base + scale_off, sbytes, bar, policy);
+    }
     ++issued;
     is = (is + 1 == D) ? 0 : is + 1;
     if (++ip == P) {
@@ -95,9 +96,7 @@ decompress_reduce_kernel(DecompressArgs a) {
       scale_off += scale_step;
     }
   };
-  if (lane == 0) {
-    while (issued < D - 1 && issued < count) issue_next();
-  }
+  while (issued < D - 1 && issued < count) issue_next();
 
   int k = 0, cs = 0;
   uint32_t cphase = 0;
@@ -113,15 +112,14 @@ decompress_reduce_kernel(DecompressArgs a) {
       for (int i = 0; i < 4; ++i) z[q][i] = f2{0.f, 0.f};
 
     for (int p = 0; p < P; ++p, ++k) {
-      if (lane == 0 && issued < count) issue_next();
+      if (issued < count) issue_next();
       const bool got = mbar_wait(bar0 + 8 * cs, cphase);
       if (!__all_sync(kFullMask, got)) {   // keep the warp's decision uniform
         ok = false;
         break;
       }
       const uint32_t st = stage0 + cs * kStageBytes;
-      const float al = lds_f32(st + kCodesBytes + 4 * sub);
-      const float sc = lds_f32(st + kCodesBytes + kScaleBytes + 4 * sub);
+      const uint2 as = lds64(st + kCodesBytes + 8 * sub);   // (alpha, s) of the block
       uint2 w[kCH];
 #pragma unroll
       for (int q = 0; q < kCH; ++q) w[q] = lds64(st + sub * NB + 8 * (j + LPB * (q ^ cx)));
@@ -131,7 +129,9 @@ decompress_reduce_kernel(DecompressArgs a) {
         cphase ^= 1u;
       }
 
-      const float d = sc * __frcp_rn(al) * a.inv_sqrt_n;
+      // s / alpha / sqrt(n); alpha >= 2^-126 and < 2^126 for every finite
+      // input the compress kernel accepts, inside __fdividef's range.
+      const float d = __fdividef(__uint_as_float(as.y), __uint_as_float(as.x)) * a.inv_sqrt_n;
       const f2 d2{d, d};
 #pragma unroll
       for (int q = 0; q < kCH; ++q) {
@@ -164,8 +164,7 @@ decompress_reduce_kernel(DecompressArgs a) {
     // A stage never completed: record it, then wait (bounded) for the copies
     // this warp still has in flight (stages k .. issued-1) before it exits.
     if (lane == 0) atomicOr(&g_decompress_fault, kFaultDecompressWait);
-    const int n_issued = __shfl_sync(kFullMask, issued, 0);
-    for (int kk = k; kk < n_issued; ++kk) {
+    for (int kk = k; kk < issued; ++kk) {
       mbar_wait(bar0 + 8 * cs, cphase);
       if (++cs == D) {
         cs = 0;

@@ -80,16 +80,15 @@ cudaError_t device_info(const DeviceInfo** out) {
 }
 
 struct Layout {
-  size_t alpha_off, s_off, bytes;
+  size_t scales_off, bytes;
 };
 
 Layout shard_layout(int64_t N, int64_t h, int block) {
   const size_t elems = static_cast<size_t>(N) * static_cast<size_t>(h);
   const size_t nblk = elems / static_cast<size_t>(block);
   Layout l;
-  l.alpha_off = pad256(elems);
-  l.s_off = l.alpha_off + pad256(4 * nblk);
-  l.bytes = l.s_off + pad256(4 * nblk);
+  l.scales_off = pad256(elems);
+  l.bytes = l.scales_off + pad256(8 * nblk);
   return l;
 }
 
@@ -110,8 +109,7 @@ taco_status decompress_common(const uint8_t* const* shards, int P, int64_t N, in
     if (overlap(shards[p], l.bytes, out, out_bytes)) return TACO_ERR_ARG;
     a.shard[p] = shards[p];
   }
-  a.alpha_off = l.alpha_off;
-  a.s_off = l.s_off;
+  a.scales_off = l.scales_off;
   a.P = P;
   a.nblocks = N * h / block;
   a.out = static_cast<uint16_t*>(out);
@@ -142,14 +140,9 @@ size_t taco_shard_bytes(int64_t N, int64_t h, int block) {
   return shard_layout(N, h, block).bytes;
 }
 
-size_t taco_shard_alpha_offset(int64_t N, int64_t h, int block) {
+size_t taco_shard_scales_offset(int64_t N, int64_t h, int block) {
   if (check_shape(N, h, block) != TACO_OK) return 0;
-  return shard_layout(N, h, block).alpha_off;
-}
-
-size_t taco_shard_s_offset(int64_t N, int64_t h, int block) {
-  if (check_shape(N, h, block) != TACO_OK) return 0;
-  return shard_layout(N, h, block).s_off;
+  return shard_layout(N, h, block).scales_off;
 }
 
 size_t taco_workspace_bytes(int P) {
@@ -185,8 +178,7 @@ taco_status taco_compress_shards(const void* x_bf16, int P, int64_t N, int64_t h
   a.nblocks = N * h / block;
   a.bundle = static_cast<uint8_t*>(bundle_out);
   a.shard_bytes = l.bytes;
-  a.alpha_off = l.alpha_off;
-  a.s_off = l.s_off;
+  a.scales_off = l.scales_off;
   a.headers = headers_out;
   a.workspace = static_cast<uint8_t*>(workspace);
   a.N = N;

@@ -28,8 +28,7 @@ struct CompressArgs {
   int64_t nblocks;          // N * h / block
   uint8_t* bundle;          // P shards
   size_t shard_bytes;
-  size_t alpha_off;
-  size_t s_off;
+  size_t scales_off;        // (alpha, s) float2 per block
   taco_header* headers;     // [P]
   uint8_t* workspace;
   int64_t N;
@@ -41,8 +40,7 @@ struct CompressArgs {
 
 struct DecompressArgs {
   const uint8_t* shard[TACO_MAX_SHARDS];   // shard p base
-  size_t alpha_off;
-  size_t s_off;
+  size_t scales_off;
   int P;
   int64_t nblocks;
   uint16_t* out;            // [N][h] bf16

@@ -77,16 +77,16 @@ typedef struct taco_header {
 
 /* ---- Shard layout -------------------------------------------------------
  * One compressed tensor ("shard") is one contiguous byte range:
- *   [codes: N*h bytes, E4M3, row-major][pad to 256]
- *   [alpha: N*(h/n) fp32, block order][pad to 256]
- *   [s:     N*(h/n) fp32, block order][pad to 256]
+ *   [codes:  N*h bytes, E4M3, row-major][pad to 256]
+ *   [scales: N*(h/n) pairs of fp32 (alpha, s), block order][pad to 256]
+ * The two scales of a block are adjacent because every reader needs both
+ * (TACO pt summary §2.B.2: reconstruction uses alpha_k and s_k together).
  * A bundle is P shards back to back, shard p at p * taco_shard_bytes(...);
  * it is the receive buffer of the ReduceScatter half of the two-shot
- * AllReduce (TACO pt summary, §2.B.3). Every part starts 256-byte aligned
- * relative to the shard start. Returns 0 for invalid arguments. */
+ * AllReduce (TACO pt summary, §2.B.3). Both parts start 256-byte aligned
+ * relative to the shard start. Return 0 for invalid arguments. */
 size_t taco_shard_bytes(int64_t N, int64_t h, int block);
-size_t taco_shard_alpha_offset(int64_t N, int64_t h, int block);
-size_t taco_shard_s_offset(int64_t N, int64_t h, int block);
+size_t taco_shard_scales_offset(int64_t N, int64_t h, int block);
 
 /* Bytes of device workspace that compress needs for P shards. The
  * workspace holds per-CTA partial maxima and arrival counters used to write

@@ -54,11 +54,9 @@ def test_shard_layout(lib):
     for N, h, n in [(512, 1024, 128), (8192, 1600, 64), (16384, 3584, 128), (1, 64, 64), (3, 768, 256),
                     (0, 256, 128)]:
         K = h // n
-        a = pad(N * h)
-        s = a + pad(4 * N * K)
-        assert lib.taco_shard_alpha_offset(N, h, n) == a
-        assert lib.taco_shard_s_offset(N, h, n) == s
-        assert lib.taco_shard_bytes(N, h, n) == s + pad(4 * N * K)
+        off = pad(N * h)
+        assert lib.taco_shard_scales_offset(N, h, n) == off
+        assert lib.taco_shard_bytes(N, h, n) == off + pad(8 * N * K)
     for N, h, n in [(4, 100, 64), (4, 128, 100), (-1, 128, 64), (4, 0, 64)]:
         assert lib.taco_shard_bytes(N, h, n) == 0
     assert lib.taco_workspace_bytes(0) == 0 and lib.taco_workspace_bytes(17) == 0

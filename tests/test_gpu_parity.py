@@ -34,12 +34,12 @@ def bundle_from_arrays(codes, alpha, s, block) -> torch.Tensor:
     """Lay out (codes, alpha, s) [P,...] in the shard format, on the device."""
     P, N, h = codes.shape
     sb = tb.shard_bytes(N, h, block)
-    a_off, s_off = tb.shard_offsets(N, h, block)
+    off = tb.shard_scales_offset(N, h, block)
     buf = np.zeros((P, max(sb, 1)), dtype=np.uint8)
     for p in range(P):
         buf[p, : N * h] = codes[p].reshape(-1)
-        buf[p, a_off: a_off + alpha[p].nbytes] = np.ascontiguousarray(alpha[p], np.float32).view(np.uint8).reshape(-1)
-        buf[p, s_off: s_off + s[p].nbytes] = np.ascontiguousarray(s[p], np.float32).view(np.uint8).reshape(-1)
+        pairs = np.stack([np.asarray(alpha[p], np.float32), np.asarray(s[p], np.float32)], axis=-1)
+        buf[p, off: off + pairs.nbytes] = np.ascontiguousarray(pairs).view(np.uint8).reshape(-1)
     return torch.from_numpy(buf).cuda()
 
 
