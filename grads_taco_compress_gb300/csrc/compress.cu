@@ -8,15 +8,17 @@
 //   packed FMAs, lane shuffles) -> FWHT of the raw block in registers and
 //   shuffles (the rotation is linear, so alpha is applied afterwards together
 //   with 1/sqrt(n) and 1/s) -> alpha = sqrt(E*/E), s = max(1, alpha/sqrt(n) *
-//   max|Hx| / 448) -> E4M3 codes with cvt.rn.satfinite (8-byte stores),
+//   max|Hx| / 448) -> E4M3 codes with cvt.rn.satfinite, written into the
+//   tile's shared-memory stage and stored with one TMA bulk store per tile,
 //   one (alpha, s) pair store per block -> per-tensor header through per-CTA
 //   partials and a last-CTA reduction.
 // Grid: gridDim.y = shard, gridDim.x persistent CTAs per shard. Each warp
 // walks warp tiles (2048 elements, 32/LPB blocks) with a stride of the grid
 // row and keeps kCompressStages tiles in flight: lane 0 issues a 1-D
 // cp.async.bulk per tile into the warp's ring of shared-memory stages, each
-// completed on its own mbarrier; all lanes wait (bounded in time), read their
-// chunks, and hand the stage back.
+// completed on its own mbarrier; all lanes wait (bounded in time) and read
+// their chunks; the stage then holds the tile's codes until their bulk store
+// has read them, and is refilled one tile later.
 
 #include <cmath>
 
@@ -91,7 +93,7 @@ compress_kernel(CompressArgs a) {
     isrc += src_step;
     is = (is + 1 == D) ? 0 : is + 1;
   };
-  while (it < D - 1 && it < count) issue_next();
+  while (it < D && it < count) issue_next();
 
   float part_smax = 0.0f;   // header partials of this thread (lane j == 0 only)
   uint32_t part_cnt = 0;
@@ -100,18 +102,19 @@ compress_kernel(CompressArgs a) {
   bool ok = true;
 
   for (; k < count; ++k) {
-    if (it < count) issue_next();
     const bool got = mbar_wait(bar0 + 8 * cs, cphase);
     if (!__all_sync(kFullMask, got)) {   // keep the warp's decision uniform
       ok = false;
       break;
     }
-    const int64_t b = static_cast<int64_t>(t0 + k * stride) * BPT + sub;
+    const int64_t b0 = static_cast<int64_t>(t0 + k * stride) * BPT;   // first block of the tile
+    const int64_t b = b0 + sub;
     const bool valid = b < nblocks;
+    const uint32_t stage = stage0 + cs * TILE_BYTES;
 
     f2 v[kCH][4];
     {
-      const uint32_t base = stage0 + cs * TILE_BYTES + sub * (NB * 2);
+      const uint32_t base = stage + sub * (NB * 2);
 #pragma unroll
       for (int q = 0; q < kCH; ++q) {
         const uint4 r = lds128(base + 16 * (j + LPB * (q ^ cx)));
@@ -121,7 +124,6 @@ compress_kernel(CompressArgs a) {
         v[q][3] = f2{bf16_lo(r.w), bf16_hi(r.w)};
       }
     }
-    __syncwarp();   // every lane has read stage cs: lane 0 may refill it
     if (++cs == D) {
       cs = 0;
       cphase ^= 1u;
@@ -169,8 +171,11 @@ compress_kernel(CompressArgs a) {
     const float g = __fdividef(cscale, sc);           // code value = g * t
     const f2 g2{g, g};
 
-    if (valid) {
-      uint8_t* cp = codes + b * NB;
+    // Codes go back into the stage this tile came from (the tile's codes are
+    // half its bytes), then leave as one bulk store.
+    __syncwarp();   // every lane has read the stage before any lane overwrites it
+    {
+      const uint32_t base = stage + sub * NB;
 #pragma unroll
       for (int q = 0; q < kCH; ++q) {
         const f2 y0 = mul2(v[q][0], g2), y1 = mul2(v[q][1], g2);
@@ -178,13 +183,26 @@ compress_kernel(CompressArgs a) {
         uint2 w;
         w.x = e4m3x4_from_f32(y0.x, y0.y, y1.x, y1.y);
         w.y = e4m3x4_from_f32(y2.x, y2.y, y3.x, y3.y);
-        *reinterpret_cast<uint2*>(cp + 8 * (j + LPB * (q ^ cx))) = w;
+        sts64(base + 8 * (j + LPB * (q ^ cx)), w);
       }
-      if (j == 0) {
-        scales_out[b] = make_float2(alpha, sc);
-        part_smax = fmaxf(part_smax, sc);
-        part_cnt += (sc > 1.0f) ? 1u : 0u;
-      }
+    }
+    if (valid && j == 0) {
+      scales_out[b] = make_float2(alpha, sc);            // 8 contiguous bytes per lane
+      part_smax = fmaxf(part_smax, sc);
+      part_cnt += (sc > 1.0f) ? 1u : 0u;
+    }
+    fence_proxy_async_smem();   // this lane's codes are visible to the bulk store
+    __syncwarp();
+    if (lane == 0) {
+      const int64_t left = nblocks - b0;
+      const uint32_t cbytes = static_cast<uint32_t>(left < BPT ? left : BPT) * NB;
+      tma_store_1d(codes + b0 * NB, stage, cbytes);
+      bulk_commit();
+    }
+    // Refill the stage of the previous tile once its codes have left it.
+    if (k >= 1 && it < count) {
+      if (lane == 0) bulk_wait_read<1>();
+      issue_next();
     }
   }
 
@@ -200,6 +218,7 @@ compress_kernel(CompressArgs a) {
       }
     }
   }
+  if (lane == 0) bulk_wait_all();   // the codes have been written before the CTA exits
 
   // ---- per-tensor header: CTA reduction, then the last CTA of the shard ----
 #pragma unroll

@@ -13,7 +13,8 @@
 // kDecompressStages stages in flight, each a pair of 1-D cp.async.bulk
 // copies (the tile's codes and its (alpha, s) pairs) completed on one mbarrier.
 // Codes are decoded in pairs with cvt.rn.f16x2.e4m3x2 and accumulated with
-// packed f32x2 FMAs; the output leaves as 16-byte bf16 stores.
+// packed f32x2 FMAs; the bf16 output tile is assembled in shared memory and
+// leaves as one TMA bulk store.
 
 #include "taco_device.cuh"
 #include "taco_launch.h"
@@ -27,6 +28,7 @@ __device__ unsigned int g_decompress_fault;
 constexpr uint32_t kCodesBytes = kTileElems;          // codes of one tile
 constexpr uint32_t kScaleBytes = 256;                 // (alpha, s) pairs of one tile
 constexpr uint32_t kStageBytes = kCodesBytes + kScaleBytes;
+constexpr uint32_t kOutBytes = kTileElems * 2;        // bf16 output of one tile
 
 template <int NB>
 __global__ void __launch_bounds__(kDecompressThreads, kDecompressMinBlocks)
@@ -49,6 +51,8 @@ decompress_reduce_kernel(DecompressArgs a) {
 
   const uint32_t stage0 = smem_u32(smem) + warp * (D * kStageBytes);
   const uint32_t bar0 = smem_u32(smem) + WARPS * D * kStageBytes + warp * (D * 8);
+  // this warp's output tile (bf16), written out with one bulk store per tile
+  const uint32_t out0 = smem_u32(smem) + WARPS * D * (kStageBytes + 8) + warp * kOutBytes;
 
   const int64_t nblocks = a.nblocks;
   const int tiles = static_cast<int>((nblocks + BPT - 1) / BPT);
@@ -102,8 +106,7 @@ decompress_reduce_kernel(DecompressArgs a) {
   uint32_t cphase = 0;
   bool ok = true;
   for (int ti = 0; ti < ntiles && ok; ++ti) {
-    const int64_t b = static_cast<int64_t>(t0 + ti * stride) * BPT + sub;
-    const bool valid = b < nblocks;
+    const int64_t b0 = static_cast<int64_t>(t0 + ti * stride) * BPT;   // first block of the tile
 
     f2 z[kCH][4];
 #pragma unroll
@@ -146,8 +149,11 @@ decompress_reduce_kernel(DecompressArgs a) {
     fwht_in_registers<kCH>(z, cx);
     fwht_across_lanes<kCH, LPB>(z, j);
 
-    if (valid) {
-      uint16_t* op = a.out + b * NB;
+    // Output tile through shared memory and one bulk store (contiguous).
+    if (lane == 0) bulk_wait_read<0>();   // the previous tile's store has read the buffer
+    __syncwarp();
+    {
+      const uint32_t base = out0 + sub * (NB * 2);
 #pragma unroll
       for (int q = 0; q < kCH; ++q) {
         uint4 o;
@@ -155,8 +161,16 @@ decompress_reduce_kernel(DecompressArgs a) {
         o.y = pack_bf16x2(z[q][1].x, z[q][1].y);
         o.z = pack_bf16x2(z[q][2].x, z[q][2].y);
         o.w = pack_bf16x2(z[q][3].x, z[q][3].y);
-        *reinterpret_cast<uint4*>(op + 8 * (j + LPB * (q ^ cx))) = o;
+        sts128(base + 16 * (j + LPB * (q ^ cx)), o);
       }
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      const int64_t left = nblocks - b0;
+      const uint32_t obytes = static_cast<uint32_t>(left < BPT ? left : BPT) * (NB * 2);
+      tma_store_1d(a.out + b0 * NB, out0, obytes);
+      bulk_commit();
     }
   }
 
@@ -172,6 +186,7 @@ decompress_reduce_kernel(DecompressArgs a) {
       }
     }
   }
+  if (lane == 0) bulk_wait_all();   // the output has been written before the CTA exits
 }
 
 }  // namespace
@@ -179,7 +194,8 @@ decompress_reduce_kernel(DecompressArgs a) {
 int decompress_tile_blocks(int block) { return 32 / (block / 64); }
 
 size_t decompress_smem_bytes() {
-  return static_cast<size_t>(kDecompressThreads / 32) * kDecompressStages * (kStageBytes + 8);
+  return static_cast<size_t>(kDecompressThreads / 32) *
+         (kDecompressStages * (kStageBytes + 8) + kOutBytes);
 }
 
 const void* decompress_kernel_ptr(int block) {
