@@ -284,7 +284,11 @@ def run_taco(args, w) -> None:
     torch.cuda.synchronize()
 
     steps = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    # Kernel durations: CUDA events around both launches of every SAMPLE-th
+    # timed step (events between launches cost a little; the step time comes
+    # from the events bracketing the whole timed region).
+    SAMPLE = 8
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(0, steps, SAMPLE)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     uuid = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
     sampler = start_clock_sampler(f"GPU-{uuid}" if uuid else None)
@@ -295,12 +299,16 @@ def run_taco(args, w) -> None:
     start.record(stream)
     for i in range(steps):
         k = i % R
-        e = ev[i]
-        e[0].record(stream)
-        compress(k)
-        e[1].record(stream)
-        decompress(k, (k + 1) % R)
-        e[2].record(stream)
+        if i % SAMPLE == 0:
+            e = ev[i // SAMPLE]
+            e[0].record(stream)
+            compress(k)
+            e[1].record(stream)
+            decompress(k, (k + 1) % R)
+            e[2].record(stream)
+        else:
+            compress(k)
+            decompress(k, (k + 1) % R)
     end.record(stream)
     torch.cuda.synchronize()
     if world > 1:

@@ -13,8 +13,9 @@
 //   one (alpha, s) pair store per block -> per-tensor header through per-CTA
 //   partials and a last-CTA reduction.
 // Grid: gridDim.y = shard, gridDim.x persistent CTAs per shard. Each warp
-// walks warp tiles (2048 elements, 32/LPB blocks) with a stride of the grid
-// row and keeps kCompressStages tiles in flight: lane 0 issues a 1-D
+// takes an equal contiguous range of the shard's blocks, walks it in warp
+// tiles (2048 elements, 32/LPB blocks) and keeps kCompressStages tiles in
+// flight: lane 0 issues a 1-D
 // cp.async.bulk per tile into the warp's ring of shared-memory stages, each
 // completed on its own mbarrier; all lanes wait (bounded in time) and read
 // their chunks; the stage then holds the tile's codes until their bulk store
@@ -62,13 +63,11 @@ compress_kernel(CompressArgs a) {
   float2* __restrict__ scales_out = reinterpret_cast<float2*>(shard_base + a.scales_off);
 
   const int64_t nblocks = a.nblocks;
-  const int tiles = static_cast<int>((nblocks + BPT - 1) / BPT);
-  const int stride = gridDim.x * WARPS;
-  const int t0 = blockIdx.x * WARPS + warp;
-  const int count = t0 < tiles ? (tiles - 1 - t0) / stride + 1 : 0;   // tiles of this warp
-  // bytes of the last tile of the tensor (the only one that can be partial)
-  const uint32_t tail_bytes =
-      static_cast<uint32_t>(nblocks - static_cast<int64_t>(tiles - 1) * BPT) * (NB * 2);
+  // This warp's contiguous share of the shard's blocks, walked tile by tile.
+  int64_t lo, hi;
+  warp_block_range(nblocks, static_cast<int64_t>(blockIdx.x) * WARPS + warp,
+                   static_cast<int64_t>(gridDim.x) * WARPS, lo, hi);
+  const int count = static_cast<int>((hi - lo + BPT - 1) / BPT);   // tiles of this warp
 
   if (lane == 0) {
     for (int s = 0; s < D; ++s) mbar_init(bar0 + 8 * s, 1);
@@ -76,21 +75,23 @@ compress_kernel(CompressArgs a) {
   }
   __syncwarp();
   const uint64_t policy = l2_evict_first_policy();
+  grid_launch_dependents();
+  grid_dependency_wait();   // no global access before the preceding grid is done
 
   // Producer state, kept identical in every lane (lane 0 issues the copy):
   // next tile number `it` of this warp, its source and its stage.
   int it = 0, is = 0;
-  const uint16_t* isrc = x + static_cast<int64_t>(t0) * kTileElems;
-  const int64_t src_step = static_cast<int64_t>(stride) * kTileElems;
+  const uint16_t* isrc = x + lo * NB;
   auto issue_next = [&]() {
     if (lane == 0) {
-      const uint32_t bytes = (t0 + it * stride == tiles - 1) ? tail_bytes : TILE_BYTES;
+      const int64_t left = hi - (lo + static_cast<int64_t>(it) * BPT);
+      const uint32_t bytes = static_cast<uint32_t>(left < BPT ? left : BPT) * (NB * 2);
       fence_proxy_async_smem();
       mbar_arrive_expect_tx(bar0 + 8 * is, bytes);
       tma_load_1d(stage0 + is * TILE_BYTES, isrc, bytes, bar0 + 8 * is, policy);
     }
     ++it;
-    isrc += src_step;
+    isrc += BPT * NB;
     is = (is + 1 == D) ? 0 : is + 1;
   };
   while (it < D && it < count) issue_next();
@@ -107,9 +108,9 @@ compress_kernel(CompressArgs a) {
       ok = false;
       break;
     }
-    const int64_t b0 = static_cast<int64_t>(t0 + k * stride) * BPT;   // first block of the tile
+    const int64_t b0 = lo + static_cast<int64_t>(k) * BPT;   // first block of the tile
     const int64_t b = b0 + sub;
-    const bool valid = b < nblocks;
+    const bool valid = b < hi;
     const uint32_t stage = stage0 + cs * TILE_BYTES;
 
     f2 v[kCH][4];
@@ -194,7 +195,7 @@ compress_kernel(CompressArgs a) {
     fence_proxy_async_smem();   // this lane's codes are visible to the bulk store
     __syncwarp();
     if (lane == 0) {
-      const int64_t left = nblocks - b0;
+      const int64_t left = hi - b0;
       const uint32_t cbytes = static_cast<uint32_t>(left < BPT ? left : BPT) * NB;
       tma_store_1d(codes + b0 * NB, stage, cbytes);
       bulk_commit();
@@ -311,20 +312,24 @@ const void* compress_kernel_ptr(int block, int variant) {
 
 cudaError_t launch_compress(const CompressArgs& a, int block, int variant, int grid_x, int P,
                             cudaStream_t stream) {
-  const dim3 grid(grid_x, P);
-  const size_t smem = compress_smem_bytes();
-#define TACO_LAUNCH_C(NB)                                                              \
-  if (variant == 0)                                                                    \
-    compress_kernel<NB, 0><<<grid, kCompressThreads, smem, stream>>>(a);               \
-  else                                                                                 \
-    compress_kernel<NB, 1><<<grid, kCompressThreads, smem, stream>>>(a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid_x, P);
+  cfg.blockDim = dim3(kCompressThreads);
+  cfg.dynamicSmemBytes = compress_smem_bytes();
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void (*kern)(CompressArgs) = nullptr;
   switch (block) {
-    case 64: TACO_LAUNCH_C(64) break;
-    case 128: TACO_LAUNCH_C(128) break;
-    default: TACO_LAUNCH_C(256) break;
+    case 64: kern = variant == 0 ? compress_kernel<64, 0> : compress_kernel<64, 1>; break;
+    case 128: kern = variant == 0 ? compress_kernel<128, 0> : compress_kernel<128, 1>; break;
+    default: kern = variant == 0 ? compress_kernel<256, 0> : compress_kernel<256, 1>; break;
   }
-#undef TACO_LAUNCH_C
-  return cudaGetLastError();
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t compress_fault(unsigned int* bits, bool clear) {

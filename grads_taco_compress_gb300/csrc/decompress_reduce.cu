@@ -8,8 +8,9 @@
 //   x_hat  = bf16( H_n z )                                 (one inverse rotation)
 // H_n / sqrt(n) is symmetric and orthogonal, so it is its own inverse, and the
 // sum can be taken before the rotation because the rotation is linear.
-// Each warp walks warp tiles (2048 elements) with a stride of the grid. For
-// one tile it consumes P stages, one per shard; lane 0 keeps
+// Each warp takes an equal contiguous range of the blocks and walks it in
+// warp tiles (2048 elements). For one tile it consumes P stages, one per
+// shard; lane 0 keeps
 // kDecompressStages stages in flight, each a pair of 1-D cp.async.bulk
 // copies (the tile's codes and its (alpha, s) pairs) completed on one mbarrier.
 // Codes are decoded in pairs with cvt.rn.f16x2.e4m3x2 and accumulated with
@@ -55,49 +56,46 @@ decompress_reduce_kernel(DecompressArgs a) {
   const uint32_t out0 = smem_u32(smem) + WARPS * D * (kStageBytes + 8) + warp * kOutBytes;
 
   const int64_t nblocks = a.nblocks;
-  const int tiles = static_cast<int>((nblocks + BPT - 1) / BPT);
-  const int stride = gridDim.x * WARPS;
-  const int t0 = blockIdx.x * WARPS + warp;
-  const int ntiles = t0 < tiles ? (tiles - 1 - t0) / stride + 1 : 0;
+  // This warp's contiguous share of the blocks, walked tile by tile.
+  int64_t lo, hi;
+  warp_block_range(nblocks, static_cast<int64_t>(blockIdx.x) * WARPS + warp,
+                   static_cast<int64_t>(gridDim.x) * WARPS, lo, hi);
+  const int ntiles = static_cast<int>((hi - lo + BPT - 1) / BPT);
   const int count = ntiles * P;                       // stages of this warp
-  const uint32_t vb_tail = static_cast<uint32_t>(nblocks - static_cast<int64_t>(tiles - 1) * BPT);
 
   if (lane == 0) {
     for (int s = 0; s < D; ++s) mbar_init(bar0 + 8 * s, 1);
     fence_mbar_init();
   }
   __syncwarp();
-  const uint64_t policy = l2_evict_first_policy();
+  grid_launch_dependents();
+  grid_dependency_wait();   // no global access before the preceding grid is done
 
   // Producer state, kept identical in every lane (lane 0 issues the copies):
   // next stage = (tile number it_t of this warp, shard ip), its slot is, and
   // the byte offsets of that tile inside a shard.
   int issued = 0, it_t = 0, ip = 0, is = 0;
-  int64_t code_off = static_cast<int64_t>(t0) * kTileElems;
-  int64_t scale_off = a.scales_off + static_cast<int64_t>(t0) * BPT * 8;
-  const int64_t code_step = static_cast<int64_t>(stride) * kTileElems;
-  const int64_t scale_step = static_cast<int64_t>(stride) * BPT * 8;
   auto issue_next = [&]() {
     if (lane == 0) {
-      const bool tail = (t0 + it_t * stride == tiles - 1);
-      const uint32_t vb = tail ? vb_tail : static_cast<uint32_t>(BPT);
+      const int64_t left = hi - (lo + static_cast<int64_t>(it_t) * BPT);
+      const uint32_t vb = static_cast<uint32_t>(left < BPT ? left : BPT);
       const uint32_t cbytes = vb * NB;
       const uint32_t sbytes = (vb * 8 + 15) & ~15u;   // stays inside the 256-byte padding
       const uint32_t dst = stage0 + is * kStageBytes;
       const uint32_t bar = bar0 + 8 * is;
+      const int64_t tb0 = lo + static_cast<int64_t>(it_t) * BPT;
       const uint8_t* base = a.shard[ip];
+      const uint64_t policy = l2_evict_first_policy();
       fence_proxy_async_smem();
       mbar_arrive_expect_tx(bar, cbytes + sbytes);
-      tma_load_1d(dst, base + code_off, cbytes, bar, policy);
-      tma_load_1d(dst + kCodesBytes, base + scale_off, sbytes, bar, policy);
+      tma_load_1d(dst, base + tb0 * NB, cbytes, bar, policy);
+      tma_load_1d(dst + kCodesBytes, base + a.scales_off + tb0 * 8, sbytes, bar, policy);
     }
     ++issued;
     is = (is + 1 == D) ? 0 : is + 1;
     if (++ip == P) {
       ip = 0;
       ++it_t;
-      code_off += code_step;
-      scale_off += scale_step;
     }
   };
   while (issued < D - 1 && issued < count) issue_next();
@@ -106,7 +104,7 @@ decompress_reduce_kernel(DecompressArgs a) {
   uint32_t cphase = 0;
   bool ok = true;
   for (int ti = 0; ti < ntiles && ok; ++ti) {
-    const int64_t b0 = static_cast<int64_t>(t0 + ti * stride) * BPT;   // first block of the tile
+    const int64_t b0 = lo + static_cast<int64_t>(ti) * BPT;   // first block of the tile
 
     f2 z[kCH][4];
 #pragma unroll
@@ -167,7 +165,7 @@ decompress_reduce_kernel(DecompressArgs a) {
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-      const int64_t left = nblocks - b0;
+      const int64_t left = hi - b0;
       const uint32_t obytes = static_cast<uint32_t>(left < BPT ? left : BPT) * (NB * 2);
       tma_store_1d(a.out + b0 * NB, out0, obytes);
       bulk_commit();
@@ -207,13 +205,21 @@ const void* decompress_kernel_ptr(int block) {
 }
 
 cudaError_t launch_decompress(const DecompressArgs& a, int block, int grid, cudaStream_t stream) {
-  const size_t smem = decompress_smem_bytes();
-  switch (block) {
-    case 64: decompress_reduce_kernel<64><<<grid, kDecompressThreads, smem, stream>>>(a); break;
-    case 128: decompress_reduce_kernel<128><<<grid, kDecompressThreads, smem, stream>>>(a); break;
-    default: decompress_reduce_kernel<256><<<grid, kDecompressThreads, smem, stream>>>(a); break;
-  }
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kDecompressThreads);
+  cfg.dynamicSmemBytes = decompress_smem_bytes();
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void (*kern)(DecompressArgs) = block == 64    ? decompress_reduce_kernel<64>
+                                 : block == 128 ? decompress_reduce_kernel<128>
+                                                : decompress_reduce_kernel<256>;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t decompress_fault(unsigned int* bits, bool clear) {

@@ -187,6 +187,26 @@ __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Programmatic dependent launch: wait until the preceding grid in the stream
+// has completed and its memory is visible (before any global access), and
+// let the next grid in the stream begin its launch.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Contiguous block range [lo, hi) of warp w out of W for nblocks blocks:
+// equal shares rounded to multiples of 4 blocks (keeps every TMA address of
+// the range 16-byte aligned), the last warp taking the remainder.
+__device__ __forceinline__ void warp_block_range(int64_t nblocks, int64_t w, int64_t W,
+                                                 int64_t& lo, int64_t& hi) {
+  lo = (nblocks * w / W) & ~int64_t{3};
+  hi = (w + 1 == W) ? nblocks : ((nblocks * (w + 1) / W) & ~int64_t{3});
+  if (hi < lo) hi = lo;
+}
+
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
