@@ -162,9 +162,9 @@ compress_kernel(CompressArgs a) {
       lq[q] = min3(min3(v[q][0].x, v[q][0].y, v[q][1].x), min3(v[q][1].y, v[q][2].x, v[q][2].y),
                    fminf(v[q][3].x, v[q][3].y));
     }
-    const float hi = max3(max3(hq[0], hq[1], hq[2]), max3(hq[3], hq[4], hq[5]), fmaxf(hq[6], hq[7]));
-    const float lo = min3(min3(lq[0], lq[1], lq[2]), min3(lq[3], lq[4], lq[5]), fminf(lq[6], lq[7]));
-    const float tmax = block_max<LPB>(fmaxf(hi, -lo));
+    const float thi = max3(max3(hq[0], hq[1], hq[2]), max3(hq[3], hq[4], hq[5]), fmaxf(hq[6], hq[7]));
+    const float tlo = min3(min3(lq[0], lq[1], lq[2]), min3(lq[3], lq[4], lq[5]), fminf(lq[6], lq[7]));
+    const float tmax = block_max<LPB>(fmaxf(thi, -tlo));
 
     const float amax = cscale * tmax;
     const float sc = (VARIANT == 0) ? fmaxf(1.0f, amax * (1.0f / 448.0f))
