@@ -284,11 +284,6 @@ def run_taco(args, w) -> None:
     torch.cuda.synchronize()
 
     steps = args.steps
-    # Kernel durations: CUDA events around both launches of every SAMPLE-th
-    # timed step (events between launches cost a little; the step time comes
-    # from the events bracketing the whole timed region).
-    SAMPLE = 8
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(0, steps, SAMPLE)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     uuid = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
     sampler = start_clock_sampler(f"GPU-{uuid}" if uuid else None)
@@ -299,25 +294,32 @@ def run_taco(args, w) -> None:
     start.record(stream)
     for i in range(steps):
         k = i % R
-        if i % SAMPLE == 0:
-            e = ev[i // SAMPLE]
-            e[0].record(stream)
-            compress(k)
-            e[1].record(stream)
-            decompress(k, (k + 1) % R)
-            e[2].record(stream)
-        else:
-            compress(k)
-            decompress(k, (k + 1) % R)
+        compress(k)
+        decompress(k, (k + 1) % R)
     end.record(stream)
     torch.cuda.synchronize()
+
+    # Launch duration of each kernel: its own timed region of back-to-back
+    # launches on the same stream and buffers (events between the two kernels
+    # of a step would break the launch overlap the step enjoys).
+    kern_iters = max(100, steps // 2)
+
+    def region(fn):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(kern_iters):
+            fn(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / kern_iters * 1e-3
+
+    t_c = region(lambda i: compress(i % R))
+    t_d = region(lambda i: decompress(i % R, (i + 1) % R))
     if world > 1:
         dist.barrier()
     clocks = stop_clock_sampler(sampler)
     local_ms = start.elapsed_time(end)
     max_ms = reduce_max_over_ranks(local_ms, dev)
-    t_c = statistics.fmean(e[0].elapsed_time(e[1]) for e in ev) * 1e-3
-    t_d = statistics.fmean(e[1].elapsed_time(e[2]) for e in ev) * 1e-3
 
     # ---- end to end through the public API, host buffers in and out ----
     x_pin = torch.from_numpy(x_host.view(np.int16)).view(torch.bfloat16).pin_memory()

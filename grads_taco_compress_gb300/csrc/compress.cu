@@ -13,9 +13,9 @@
 //   one (alpha, s) pair store per block -> per-tensor header through per-CTA
 //   partials and a last-CTA reduction.
 // Grid: gridDim.y = shard, gridDim.x persistent CTAs per shard. Each warp
-// takes an equal contiguous range of the shard's blocks, walks it in warp
-// tiles (2048 elements, 32/LPB blocks) and keeps kCompressStages tiles in
-// flight: lane 0 issues a 1-D
+// walks warp tiles (2048 elements, 32/LPB blocks) in grid-stride rounds and
+// then an even share of the blocks left over (WarpWork), keeping
+// kCompressStages tiles in flight: lane 0 issues a 1-D
 // cp.async.bulk per tile into the warp's ring of shared-memory stages, each
 // completed on its own mbarrier; all lanes wait (bounded in time) and read
 // their chunks; the stage then holds the tile's codes until their bulk store
@@ -63,11 +63,9 @@ compress_kernel(CompressArgs a) {
   float2* __restrict__ scales_out = reinterpret_cast<float2*>(shard_base + a.scales_off);
 
   const int64_t nblocks = a.nblocks;
-  // This warp's contiguous share of the shard's blocks, walked tile by tile.
-  int64_t lo, hi;
-  warp_block_range(nblocks, static_cast<int64_t>(blockIdx.x) * WARPS + warp,
-                   static_cast<int64_t>(gridDim.x) * WARPS, lo, hi);
-  const int count = static_cast<int>((hi - lo + BPT - 1) / BPT);   // tiles of this warp
+  const WarpWork ww(nblocks, static_cast<int64_t>(blockIdx.x) * WARPS + warp,
+                    static_cast<int64_t>(gridDim.x) * WARPS, BPT);
+  const int count = ww.count;   // tiles of this warp
 
   if (lane == 0) {
     for (int s = 0; s < D; ++s) mbar_init(bar0 + 8 * s, 1);
@@ -81,17 +79,17 @@ compress_kernel(CompressArgs a) {
   // Producer state, kept identical in every lane (lane 0 issues the copy):
   // next tile number `it` of this warp, its source and its stage.
   int it = 0, is = 0;
-  const uint16_t* isrc = x + lo * NB;
   auto issue_next = [&]() {
     if (lane == 0) {
-      const int64_t left = hi - (lo + static_cast<int64_t>(it) * BPT);
-      const uint32_t bytes = static_cast<uint32_t>(left < BPT ? left : BPT) * (NB * 2);
+      int64_t tb0;
+      int tvb;
+      ww.tile(it, tb0, tvb);
+      const uint32_t bytes = static_cast<uint32_t>(tvb) * (NB * 2);
       fence_proxy_async_smem();
       mbar_arrive_expect_tx(bar0 + 8 * is, bytes);
-      tma_load_1d(stage0 + is * TILE_BYTES, isrc, bytes, bar0 + 8 * is, policy);
+      tma_load_1d(stage0 + is * TILE_BYTES, x + tb0 * NB, bytes, bar0 + 8 * is, policy);
     }
     ++it;
-    isrc += BPT * NB;
     is = (is + 1 == D) ? 0 : is + 1;
   };
   while (it < D && it < count) issue_next();
@@ -108,9 +106,11 @@ compress_kernel(CompressArgs a) {
       ok = false;
       break;
     }
-    const int64_t b0 = lo + static_cast<int64_t>(k) * BPT;   // first block of the tile
+    int64_t b0;   // first block of the tile
+    int vb;       // blocks in the tile
+    ww.tile(k, b0, vb);
     const int64_t b = b0 + sub;
-    const bool valid = b < hi;
+    const bool valid = sub < vb;
     const uint32_t stage = stage0 + cs * TILE_BYTES;
 
     f2 v[kCH][4];
@@ -195,9 +195,7 @@ compress_kernel(CompressArgs a) {
     fence_proxy_async_smem();   // this lane's codes are visible to the bulk store
     __syncwarp();
     if (lane == 0) {
-      const int64_t left = hi - b0;
-      const uint32_t cbytes = static_cast<uint32_t>(left < BPT ? left : BPT) * NB;
-      tma_store_1d(codes + b0 * NB, stage, cbytes);
+      tma_store_1d(codes + b0 * NB, stage, static_cast<uint32_t>(vb) * NB);
       bulk_commit();
     }
     // Refill the stage of the previous tile once its codes have left it.

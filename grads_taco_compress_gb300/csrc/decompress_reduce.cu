@@ -8,9 +8,9 @@
 //   x_hat  = bf16( H_n z )                                 (one inverse rotation)
 // H_n / sqrt(n) is symmetric and orthogonal, so it is its own inverse, and the
 // sum can be taken before the rotation because the rotation is linear.
-// Each warp takes an equal contiguous range of the blocks and walks it in
-// warp tiles (2048 elements). For one tile it consumes P stages, one per
-// shard; lane 0 keeps
+// Each warp walks warp tiles (2048 elements) in grid-stride rounds and then
+// an even share of the blocks left over (WarpWork). For one tile it consumes
+// P stages, one per shard; lane 0 keeps
 // kDecompressStages stages in flight, each a pair of 1-D cp.async.bulk
 // copies (the tile's codes and its (alpha, s) pairs) completed on one mbarrier.
 // Codes are decoded in pairs with cvt.rn.f16x2.e4m3x2 and accumulated with
@@ -56,11 +56,9 @@ decompress_reduce_kernel(DecompressArgs a) {
   const uint32_t out0 = smem_u32(smem) + WARPS * D * (kStageBytes + 8) + warp * kOutBytes;
 
   const int64_t nblocks = a.nblocks;
-  // This warp's contiguous share of the blocks, walked tile by tile.
-  int64_t lo, hi;
-  warp_block_range(nblocks, static_cast<int64_t>(blockIdx.x) * WARPS + warp,
-                   static_cast<int64_t>(gridDim.x) * WARPS, lo, hi);
-  const int ntiles = static_cast<int>((hi - lo + BPT - 1) / BPT);
+  const WarpWork ww(nblocks, static_cast<int64_t>(blockIdx.x) * WARPS + warp,
+                    static_cast<int64_t>(gridDim.x) * WARPS, BPT);
+  const int ntiles = ww.count;
   const int count = ntiles * P;                       // stages of this warp
 
   if (lane == 0) {
@@ -77,13 +75,14 @@ decompress_reduce_kernel(DecompressArgs a) {
   int issued = 0, it_t = 0, ip = 0, is = 0;
   auto issue_next = [&]() {
     if (lane == 0) {
-      const int64_t left = hi - (lo + static_cast<int64_t>(it_t) * BPT);
-      const uint32_t vb = static_cast<uint32_t>(left < BPT ? left : BPT);
+      int64_t tb0;
+      int tvb;
+      ww.tile(it_t, tb0, tvb);
+      const uint32_t vb = static_cast<uint32_t>(tvb);
       const uint32_t cbytes = vb * NB;
       const uint32_t sbytes = (vb * 8 + 15) & ~15u;   // stays inside the 256-byte padding
       const uint32_t dst = stage0 + is * kStageBytes;
       const uint32_t bar = bar0 + 8 * is;
-      const int64_t tb0 = lo + static_cast<int64_t>(it_t) * BPT;
       const uint8_t* base = a.shard[ip];
       const uint64_t policy = l2_evict_first_policy();
       fence_proxy_async_smem();
@@ -104,7 +103,9 @@ decompress_reduce_kernel(DecompressArgs a) {
   uint32_t cphase = 0;
   bool ok = true;
   for (int ti = 0; ti < ntiles && ok; ++ti) {
-    const int64_t b0 = lo + static_cast<int64_t>(ti) * BPT;   // first block of the tile
+    int64_t b0;   // first block of the tile
+    int vb;       // blocks in the tile
+    ww.tile(ti, b0, vb);
 
     f2 z[kCH][4];
 #pragma unroll
@@ -165,9 +166,7 @@ decompress_reduce_kernel(DecompressArgs a) {
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-      const int64_t left = hi - b0;
-      const uint32_t obytes = static_cast<uint32_t>(left < BPT ? left : BPT) * (NB * 2);
-      tma_store_1d(a.out + b0 * NB, out0, obytes);
+      tma_store_1d(a.out + b0 * NB, out0, static_cast<uint32_t>(vb) * (NB * 2));
       bulk_commit();
     }
   }

@@ -197,15 +197,42 @@ __device__ __forceinline__ void grid_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Contiguous block range [lo, hi) of warp w out of W for nblocks blocks:
-// equal shares rounded to multiples of 4 blocks (keeps every TMA address of
-// the range 16-byte aligned), the last warp taking the remainder.
-__device__ __forceinline__ void warp_block_range(int64_t nblocks, int64_t w, int64_t W,
-                                                 int64_t& lo, int64_t& hi) {
-  lo = (nblocks * w / W) & ~int64_t{3};
-  hi = (w + 1 == W) ? nblocks : ((nblocks * (w + 1) / W) & ~int64_t{3});
-  if (hi < lo) hi = lo;
-}
+// Work of warp w out of W over nblocks blocks, in tiles of BPT blocks:
+//   * `rounds` full rounds in grid-stride order (round r, tile r*W + w), so
+//     that at any time the warps of the grid stream one contiguous window;
+//   * then the blocks left over, split evenly: warp w takes the contiguous
+//     range [rlo, rhi) of them, with boundaries on multiples of 4 blocks
+//     (every TMA address stays 16-byte aligned), walked in tiles of <= BPT.
+// Every block belongs to exactly one tile of one warp.
+struct WarpWork {
+  int64_t w, W, bpt;
+  int64_t rounds;      // full grid-stride rounds
+  int64_t rem0;        // first block after the full rounds
+  int64_t rlo, rhi;    // this warp's share of the rest, relative to rem0
+  int count;           // tiles of this warp
+
+  __device__ __forceinline__ WarpWork(int64_t nblocks, int64_t w_, int64_t W_, int bpt_)
+      : w(w_), W(W_), bpt(bpt_) {
+    rounds = nblocks / (W * bpt);
+    rem0 = rounds * W * bpt;
+    const int64_t rest = nblocks - rem0;
+    rlo = (rest * w / W) & ~int64_t{3};
+    rhi = (w + 1 == W) ? rest : ((rest * (w + 1) / W) & ~int64_t{3});
+    if (rhi < rlo) rhi = rlo;
+    count = static_cast<int>(rounds + (rhi - rlo + bpt - 1) / bpt);
+  }
+  // first block and number of blocks of this warp's tile k (0 <= k < count)
+  __device__ __forceinline__ void tile(int k, int64_t& b0, int& vb) const {
+    if (k < rounds) {
+      b0 = (static_cast<int64_t>(k) * W + w) * bpt;
+      vb = static_cast<int>(bpt);
+    } else {
+      b0 = rem0 + rlo + (k - rounds) * bpt;
+      const int64_t left = rem0 + rhi - b0;
+      vb = static_cast<int>(left < bpt ? left : bpt);
+    }
+  }
+};
 
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
   unsigned long long t;
