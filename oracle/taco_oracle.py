@@ -28,6 +28,9 @@ Decompress-reduce ([PT] §2.B.2 "Reconstruction"; the reduce of the
 ReduceScatter half of the two-shot AllReduce, [PT] §2.B.3):
   x_hat = bf16_RNE( sum_p (1/alpha_p) (H_n^T / sqrt(n)) (s_p * dec(q_p)) )
 in fp64, inverting each shard on its own and summing: the plain definition.
+Reduce-recompress (the reduced chunk compressed again for the AllGather,
+[PT] §2.B.3): the compress steps applied to the fp64 x_hat above, before
+any rounding to bf16.
 
 Readings taken where the pages are silent (each one is a choice):
   * dual scale: alpha_k sets the block energy before rotation (the
@@ -188,13 +191,26 @@ def compress_stages(x_bits: np.ndarray, block: int,
     per-tensor ``header`` dict.
     """
     x_bits = np.asarray(x_bits, dtype=np.uint16)
-    N, h = x_bits.shape
+    return compress_values_stages(bf16_bits_to_f64(x_bits), block, target_energy, variant)
+
+
+def compress_values_stages(x_values: np.ndarray, block: int,
+                           target_energy: float = DEFAULT_TARGET_ENERGY,
+                           variant: int = VARIANT_DUAL) -> dict:
+    """The same steps on real values [N, h] (float64) instead of bf16 inputs.
+
+    Used for the compression of a reduced tensor that never went through a
+    bf16 buffer (the ReduceScatter output recompressed for the AllGather,
+    TACO pt summary §2.B.3).
+    """
+    x_values = np.asarray(x_values, dtype=np.float64)
+    N, h = x_values.shape
     n = block
     _check_shape(h, n)
     if variant not in (VARIANT_DUAL, VARIANT_ABSMAX):
         raise ValueError("unknown variant")
     K = h // n
-    x = bf16_bits_to_f64(x_bits).reshape(N, K, n)
+    x = x_values.reshape(N, K, n)
 
     # 1. block energy: raw second moment, mean over the block ([PT] §2.B.1)
     energy = np.sum(x * x, axis=-1) / n
@@ -277,6 +293,24 @@ def decompress_reduce(codes: np.ndarray, alpha: np.ndarray, s: np.ndarray,
                       block: int) -> np.ndarray:
     """bf16 bit patterns [N,h] of the reduced reconstruction (one RNE)."""
     return f64_to_bf16_bits(decompress_reduce_f64(codes, alpha, s, block))
+
+
+# --------------------------------------------------------------------------
+# Reduce then recompress (the step between ReduceScatter and AllGather)
+# --------------------------------------------------------------------------
+def reduce_recompress(codes: np.ndarray, alpha: np.ndarray, s: np.ndarray, block: int,
+                      target_energy: float = DEFAULT_TARGET_ENERGY,
+                      variant: int = VARIANT_DUAL):
+    """Compress the sum of the P reconstructions without rounding it to bf16.
+
+    In the two-shot AllReduce ([PT] §2.B.3) each rank reduces the P chunks
+    it received and compresses the reduced chunk again for the AllGather.
+    The plain definition: x_hat = decompress_reduce_f64(...) in fp64, then
+    the compress steps on those values. Returns (codes, alpha, s, header).
+    """
+    x_hat = decompress_reduce_f64(codes, alpha, s, block)
+    st = compress_values_stages(x_hat, block, target_energy, variant)
+    return st["codes"], st["alpha"], st["s"], st["header"]
 
 
 # --------------------------------------------------------------------------

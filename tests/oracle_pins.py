@@ -269,6 +269,54 @@ def check_reduce_linearity(O):
         assert np.allclose(got, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max()), (n, P)
 
 
+def check_recompress_spike_blocks(O):
+    """A reduced spike block is a spike again: the same +-64 codes, exactly."""
+    rng = np.random.default_rng(13)
+    for n in (64, 128, 256):
+        xv = np.zeros((3, 2 * n), dtype=np.float32)
+        for r in range(3):
+            xv[r, int(rng.integers(2 * n))] = (-1.0) ** r * 0.375 * (r + 1)
+        x = _bf16_bits(xv)
+        codes, alpha, s, _ = O.compress(x, n, E_STAR)
+        rc, ra, rs, _ = O.reduce_recompress(codes[None], alpha[None], s[None], n, E_STAR)
+        assert np.array_equal(rc, codes), n
+        assert np.allclose(ra, alpha, rtol=2e-7) and np.array_equal(rs, s), n
+
+
+def check_recompress_scale_invariance(O):
+    """Summing a shard with itself doubles x_hat: alpha halves, codes and s stay."""
+    rng = np.random.default_rng(14)
+    for n in (64, 128, 256):
+        N, h = 16, 2 * n
+        codes = rng.integers(0, 256, size=(1, N, h)).astype(np.uint8)
+        codes[(codes & 0x7F) == 0x7F] = 0x21
+        alpha = np.exp(rng.uniform(0, 8, size=(1, N, h // n))).astype(np.float32)
+        s = np.maximum(1.0, np.exp(rng.normal(0, 0.3, size=(1, N, h // n)))).astype(np.float32)
+        c1, a1, s1, _ = O.reduce_recompress(codes, alpha, s, n, E_STAR)
+        c2, a2, s2, _ = O.reduce_recompress(np.concatenate([codes, codes]), np.concatenate([alpha, alpha]),
+                                            np.concatenate([s, s]), n, E_STAR)
+        assert np.mean(c1 == c2) > 0.9999, n
+        assert np.allclose(a2, a1 / 2, rtol=2e-7), n
+        assert np.allclose(s2, s1, rtol=2e-7), n
+
+
+def check_recompress_reconstructs(O):
+    """Decoding the recompressed shard gives back x_hat within E4M3 error."""
+    rng = np.random.default_rng(15)
+    n, P, N, h = 128, 3, 24, 512
+    xs = np.stack([_random_bf16(rng, (N, h), 0.02) for _ in range(P)])
+    parts = [O.compress(xs[p], n, E_STAR) for p in range(P)]
+    codes = np.stack([c for c, _, _, _ in parts])
+    alpha = np.stack([a for _, a, _, _ in parts])
+    s = np.stack([sc for _, _, sc, _ in parts])
+    x_hat = O.decompress_reduce_f64(codes, alpha, s, n)
+    rc, ra, rs, hdr = O.reduce_recompress(codes, alpha, s, n, E_STAR)
+    back = O.decompress_one_f64(rc, ra, rs, n)
+    rel = np.linalg.norm(back - x_hat) / np.linalg.norm(x_hat)
+    assert 0.005 < rel < 0.04, rel
+    assert hdr["N"] == N and hdr["h"] == h and hdr["n_clamped"] == int(np.count_nonzero(rs > 1))
+
+
 def check_roundtrip_error(O):
     """One shard round trip: the error of a 3-bit-mantissa code, not more."""
     rng = np.random.default_rng(9)

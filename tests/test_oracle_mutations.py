@@ -34,6 +34,10 @@ MUTATIONS = {
     "decode_not_normalised": ("u = (w @ H) / math.sqrt(n)", "u = (w @ H) / n"),
     "bf16_truncates": ("np.rint(np.ldexp(v[finite], -q))", "np.trunc(np.ldexp(v[finite], -q))"),
     "reduce_drops_last_shard": ("for p in range(P):", "for p in range(P - 1):"),
+    "recompress_first_shard_only": ("x_hat = decompress_reduce_f64(codes, alpha, s, block)",
+                                    "x_hat = decompress_reduce_f64(codes[:1], alpha[:1], s[:1], block)"),
+    "recompress_skips_alpha": ("    st = compress_values_stages(x_hat, block, target_energy, variant)\n    return st[\"codes\"], st[\"alpha\"]",
+                               "    st = compress_values_stages(x_hat, block, target_energy, variant)\n    return st[\"codes\"], st[\"alpha\"] * 0 + 1"),
 }
 
 
