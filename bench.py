@@ -315,6 +315,19 @@ def run_taco(args, w) -> None:
 
     t_c = region(lambda i: compress(i % R))
     t_d = region(lambda i: decompress(i % R, (i + 1) % R))
+    # the fused reduce -> recompress of the same bundles (next step of the
+    # two-shot AllReduce), compressed sum only
+    rc_shards = [torch.empty(sb, dtype=torch.uint8, device=dev) for _ in range(R)]
+    rc_hdr = torch.empty(taco.HEADER_BYTES, dtype=torch.uint8, device=dev)
+    ws1 = taco.new_workspace(1, dev)
+
+    def recompress(k, src):
+        st = lib.taco_reduce_recompress(bp[src], P, N, h, n, E, 0, rc_shards[k].data_ptr(),
+                                        rc_hdr.data_ptr(), None, ws1.data_ptr(), ws1.numel(), sptr)
+        if st:
+            raise taco.TacoError(st, "taco_reduce_recompress")
+
+    t_r = region(lambda i: recompress(i % R, (i + 1) % R))
     if world > 1:
         dist.barrier()
     clocks = stop_clock_sampler(sampler)
@@ -352,6 +365,7 @@ def run_taco(args, w) -> None:
         peak_src = "measured" if peaks.get("hbm_gbs") else "fallback"
         c_bytes = P * N * h * 3 + P * N * K * 8
         d_bytes = P * N * h + P * N * K * 8 + N * h * 2
+        r_bytes = (P + 1) * (N * h + N * K * 8)
         kern = {
             "compress": {"us": round(t_c * 1e6, 3), "alg_bytes": c_bytes,
                          "hbm_gbs": round(c_bytes / t_c / 1e9, 1),
@@ -361,6 +375,10 @@ def run_taco(args, w) -> None:
                                   "hbm_gbs": round(d_bytes / t_d / 1e9, 1),
                                   "bf16_in_gbs": round(in_bytes / t_d / 1e9, 1),
                                   "frac": round(d_bytes / t_d / 1e9 / hbm, 4)},
+            "reduce_recompress": {"us": round(t_r * 1e6, 3), "alg_bytes": r_bytes,
+                                  "hbm_gbs": round(r_bytes / t_r / 1e9, 1),
+                                  "bf16_in_gbs": round(in_bytes / t_r / 1e9, 1),
+                                  "frac": round(r_bytes / t_r / 1e9 / hbm, 4)},
         }
         dom = "compress" if t_c >= t_d else "decompress_reduce"
         achieved = kern[dom]["hbm_gbs"]

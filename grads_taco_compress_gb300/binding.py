@@ -38,6 +38,7 @@ EXPORTED_SYMBOLS = (
     "taco_workspace_bytes", "taco_compress", "taco_compress_shards",
     "taco_compress_shards_noalloc",
     "taco_decompress_reduce", "taco_decompress_reduce_ptrs",
+    "taco_reduce_recompress", "taco_reduce_recompress_ptrs",
     "taco_e4m3_encode_f32", "taco_e4m3_decode_f32",
     "taco_get_fault", "taco_selftest_wait_timeout",
     "taco_status_string", "taco_abi_version",
@@ -73,6 +74,9 @@ def _lib() -> ctypes.CDLL:
             "taco_compress_shards_noalloc": (i32, [vp, i32, i64, i64, i32, f32, i32, vp, vp, vp]),
             "taco_decompress_reduce": (i32, [vp, i32, i64, i64, i32, vp, vp]),
             "taco_decompress_reduce_ptrs": (i32, [ctypes.POINTER(vp), i32, i64, i64, i32, vp, vp]),
+            "taco_reduce_recompress": (i32, [vp, i32, i64, i64, i32, f32, i32, vp, vp, vp, vp, sz, vp]),
+            "taco_reduce_recompress_ptrs": (i32, [ctypes.POINTER(vp), i32, i64, i64, i32, f32, i32,
+                                                  vp, vp, vp, vp, sz, vp]),
             "taco_e4m3_encode_f32": (i32, [vp, vp, i64, vp]),
             "taco_e4m3_decode_f32": (i32, [vp, vp, i64, vp]),
             "taco_get_fault": (i32, [ctypes.POINTER(ctypes.c_uint32), i32]),
@@ -237,6 +241,55 @@ def taco_decompress_reduce_ptrs(shards, N: int, h: int, block: int,
     st = _lib().taco_decompress_reduce_ptrs(arr, P, N, h, block, _ptr(out), _stream_ptr(stream))
     _check(st, "taco_decompress_reduce_ptrs")
     return out
+
+
+def taco_reduce_recompress(bundle: torch.Tensor, P: int, N: int, h: int, block: int,
+                           target_energy: float = DEFAULT_TARGET_ENERGY, variant: int = VARIANT_DUAL,
+                           shard: torch.Tensor | None = None, header: torch.Tensor | None = None,
+                           out: torch.Tensor | None = None, want_bf16: bool = False,
+                           workspace: torch.Tensor | None = None, stream=None):
+    """Sum the P shards of a bundle and compress the sum into one shard.
+
+    Returns (shard u8, header u8 [40], bf16 sum or None).
+    """
+    if not bundle.is_cuda:
+        raise ValueError("bundle must be a CUDA tensor")
+    dev = bundle.device
+    if shard is None:
+        shard = torch.empty(max(shard_bytes(N, h, block), 1), dtype=torch.uint8, device=dev)
+    if header is None:
+        header = torch.empty(HEADER_BYTES, dtype=torch.uint8, device=dev)
+    if out is None and want_bf16:
+        out = torch.empty((N, h), dtype=torch.bfloat16, device=dev)
+    if workspace is None:
+        workspace = new_workspace(1, dev)
+    st = _lib().taco_reduce_recompress(_ptr(bundle), P, N, h, block, float(target_energy), variant,
+                                       _ptr(shard), _ptr(header), _ptr(out), _ptr(workspace),
+                                       workspace.numel(), _stream_ptr(stream))
+    _check(st, "taco_reduce_recompress")
+    return shard, header, out
+
+
+def taco_reduce_recompress_ptrs(shards, N: int, h: int, block: int,
+                                target_energy: float = DEFAULT_TARGET_ENERGY,
+                                variant: int = VARIANT_DUAL, shard: torch.Tensor | None = None,
+                                header: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                                workspace: torch.Tensor | None = None, stream=None):
+    """As taco_reduce_recompress with P separate shard tensors."""
+    P = len(shards)
+    dev = shards[0].device
+    if shard is None:
+        shard = torch.empty(max(shard_bytes(N, h, block), 1), dtype=torch.uint8, device=dev)
+    if header is None:
+        header = torch.empty(HEADER_BYTES, dtype=torch.uint8, device=dev)
+    if workspace is None:
+        workspace = new_workspace(1, dev)
+    arr = (ctypes.c_void_p * max(P, 1))(*[_ptr(s) for s in shards])
+    st = _lib().taco_reduce_recompress_ptrs(arr, P, N, h, block, float(target_energy), variant,
+                                            _ptr(shard), _ptr(header), _ptr(out), _ptr(workspace),
+                                            workspace.numel(), _stream_ptr(stream))
+    _check(st, "taco_reduce_recompress_ptrs")
+    return shard, header, out
 
 
 def taco_e4m3_encode_f32(x: torch.Tensor, stream=None) -> torch.Tensor:

@@ -43,9 +43,6 @@ compress_kernel(CompressArgs a) {
   static_assert(LPB >= 1 && LPB <= 4, "block size");
 
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ float sh_max[WARPS];
-  __shared__ uint32_t sh_cnt[WARPS];
-  __shared__ bool sh_last;
 
   const int shard = blockIdx.y;
   const int lane = threadIdx.x & 31;
@@ -220,70 +217,8 @@ compress_kernel(CompressArgs a) {
   if (lane == 0) bulk_wait_all();   // the codes have been written before the CTA exits
 
   // ---- per-tensor header: CTA reduction, then the last CTA of the shard ----
-#pragma unroll
-  for (int m = 16; m >= 1; m >>= 1) {
-    part_smax = fmaxf(part_smax, __shfl_xor_sync(kFullMask, part_smax, m));
-    part_cnt += __shfl_xor_sync(kFullMask, part_cnt, m);
-  }
-  if (lane == 0) {
-    sh_max[warp] = part_smax;
-    sh_cnt[warp] = part_cnt;
-  }
-  __syncthreads();
-
-  uint32_t* counter = reinterpret_cast<uint32_t*>(a.workspace + shard * kWorkspaceShardStride);
-  float2* partials = reinterpret_cast<float2*>(a.workspace + shard * kWorkspaceShardStride + 16);
-  if (threadIdx.x == 0) {
-    float m = 0.f;
-    uint32_t n = 0;
-    for (int w = 0; w < WARPS; ++w) {
-      m = fmaxf(m, sh_max[w]);
-      n += sh_cnt[w];
-    }
-    partials[blockIdx.x] = make_float2(m, __uint_as_float(n));
-    __threadfence();
-    const uint32_t arrived = atomicAdd(counter, 1u);
-    sh_last = (arrived == gridDim.x - 1);
-  }
-  __syncthreads();
-
-  if (sh_last) {
-    __threadfence();
-    float m = 0.f;
-    uint32_t n = 0;
-    for (int i = threadIdx.x; i < static_cast<int>(gridDim.x); i += kCompressThreads) {
-      const float2 p = __ldcg(partials + i);
-      m = fmaxf(m, p.x);
-      n += __float_as_uint(p.y);
-    }
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-      m = fmaxf(m, __shfl_xor_sync(kFullMask, m, o));
-      n += __shfl_xor_sync(kFullMask, n, o);
-    }
-    __syncthreads();
-    if (lane == 0) {
-      sh_max[warp] = m;
-      sh_cnt[warp] = n;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      for (int w = 1; w < WARPS; ++w) {
-        m = fmaxf(m, sh_max[w]);
-        n += sh_cnt[w];
-      }
-      taco_header* hd = a.headers + shard;
-      hd->N = a.N;
-      hd->h = a.h;
-      hd->block = NB;
-      hd->variant = VARIANT;
-      hd->target_energy = a.target_energy;
-      hd->q_max = 448.0f;
-      hd->s_max = m;
-      hd->n_clamped = n;
-      *counter = 0u;   // leave the workspace zero-filled for the next call
-    }
-  }
+  finish_header<kCompressThreads>(part_smax, part_cnt, a.workspace + shard * kWorkspaceShardStride,
+                                  a.headers + shard, a.N, a.h, NB, VARIANT, a.target_energy);
 }
 
 template <int NB>

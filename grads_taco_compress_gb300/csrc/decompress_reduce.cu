@@ -31,7 +31,13 @@ constexpr uint32_t kScaleBytes = 256;                 // (alpha, s) pairs of one
 constexpr uint32_t kStageBytes = kCodesBytes + kScaleBytes;
 constexpr uint32_t kOutBytes = kTileElems * 2;        // bf16 output of one tile
 
-template <int NB>
+// MODE 0: decompress-reduce to bf16.
+// MODE 1: reduce-recompress. The sum x_hat = H z of the P reconstructions is
+// compressed again without leaving the rotated domain: H x_hat = n z and
+// sum x_hat^2 = n sum z^2 (H symmetric, H H = n I), so alpha' = sqrt(E* /
+// sum z^2), the rotated block is alpha' sqrt(n) z and no transform is
+// needed; the bf16 sum is written too when `out` is not null.
+template <int NB, int MODE, int VARIANT>
 __global__ void __launch_bounds__(kDecompressThreads, kDecompressMinBlocks)
 decompress_reduce_kernel(DecompressArgs a) {
   constexpr int LPB = NB / 64;
@@ -102,6 +108,8 @@ decompress_reduce_kernel(DecompressArgs a) {
   int k = 0, cs = 0;
   uint32_t cphase = 0;
   bool ok = true;
+  float part_smax = 0.0f;   // reduce-recompress header partials (lane j == 0)
+  uint32_t part_cnt = 0;
   for (int ti = 0; ti < ntiles && ok; ++ti) {
     int64_t b0;   // first block of the tile
     int vb;       // blocks in the tile
@@ -145,6 +153,62 @@ decompress_reduce_kernel(DecompressArgs a) {
     }
     if (!ok) break;
 
+    if constexpr (MODE == 1) {
+      // energy of x_hat: sum x_hat^2 / n = sum z^2
+      f2 ea[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll
+      for (int q = 0; q < kCH; ++q)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ea[i] = fma2(z[q][i], z[q][i], ea[i]);
+      const f2 e01 = add2(ea[0], ea[1]), e23 = add2(ea[2], ea[3]);
+      const float e = block_sum<LPB>((e01.x + e01.y) + (e23.x + e23.y));
+      float r = rsqrtf(e);
+      r = fmaf(fmaf(-0.5f * e * r, r, 0.5f), r, r);
+      const float alpha = (e > 0.f) ? a.sqrt_E * r : 1.0f;
+      const float cscale = alpha * a.sqrt_n;          // rotated block = cscale * z
+      float hq[kCH], lq[kCH];
+#pragma unroll
+      for (int q = 0; q < kCH; ++q) {
+        hq[q] = max3(max3(z[q][0].x, z[q][0].y, z[q][1].x), max3(z[q][1].y, z[q][2].x, z[q][2].y),
+                     fmaxf(z[q][3].x, z[q][3].y));
+        lq[q] = min3(min3(z[q][0].x, z[q][0].y, z[q][1].x), min3(z[q][1].y, z[q][2].x, z[q][2].y),
+                     fminf(z[q][3].x, z[q][3].y));
+      }
+      const float zhi = max3(max3(hq[0], hq[1], hq[2]), max3(hq[3], hq[4], hq[5]), fmaxf(hq[6], hq[7]));
+      const float zlo = min3(min3(lq[0], lq[1], lq[2]), min3(lq[3], lq[4], lq[5]), fminf(lq[6], lq[7]));
+      const float amax = cscale * block_max<LPB>(fmaxf(zhi, -zlo));
+      const float sc = (VARIANT == 0) ? fmaxf(1.0f, amax * (1.0f / 448.0f))
+                                      : (amax > 0.f ? amax * (1.0f / 448.0f) : 1.0f);
+      const float g = __fdividef(cscale, sc);
+      const f2 g2{g, g};
+      if (lane == 0) bulk_wait_read<0>();   // the previous store has read the buffer
+      __syncwarp();
+      {
+        const uint32_t base = out0 + sub * NB;
+#pragma unroll
+        for (int q = 0; q < kCH; ++q) {
+          const f2 y0 = mul2(z[q][0], g2), y1 = mul2(z[q][1], g2);
+          const f2 y2 = mul2(z[q][2], g2), y3 = mul2(z[q][3], g2);
+          uint2 w;
+          w.x = e4m3x4_from_f32(y0.x, y0.y, y1.x, y1.y);
+          w.y = e4m3x4_from_f32(y2.x, y2.y, y3.x, y3.y);
+          sts64(base + 8 * (j + LPB * (q ^ cx)), w);
+        }
+      }
+      if (sub < vb && j == 0) {
+        reinterpret_cast<float2*>(a.rc_shard + a.scales_off)[b0 + sub] = make_float2(alpha, sc);
+        part_smax = fmaxf(part_smax, sc);
+        part_cnt += (sc > 1.0f) ? 1u : 0u;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_1d(a.rc_shard + b0 * NB, out0, static_cast<uint32_t>(vb) * NB);
+        bulk_commit();
+      }
+      if (a.out == nullptr) continue;
+    }
+
     fwht_in_registers<kCH>(z, cx);
     fwht_across_lanes<kCH, LPB>(z, j);
 
@@ -184,6 +248,10 @@ decompress_reduce_kernel(DecompressArgs a) {
     }
   }
   if (lane == 0) bulk_wait_all();   // the output has been written before the CTA exits
+  if constexpr (MODE == 1) {
+    finish_header<kDecompressThreads>(part_smax, part_cnt, a.workspace, a.rc_header, a.N, a.h, NB,
+                                      VARIANT, a.target_energy);
+  }
 }
 
 }  // namespace
@@ -197,9 +265,24 @@ size_t decompress_smem_bytes() {
 
 const void* decompress_kernel_ptr(int block) {
   switch (block) {
-    case 64: return reinterpret_cast<const void*>(decompress_reduce_kernel<64>);
-    case 128: return reinterpret_cast<const void*>(decompress_reduce_kernel<128>);
-    default: return reinterpret_cast<const void*>(decompress_reduce_kernel<256>);
+    case 64: return reinterpret_cast<const void*>(decompress_reduce_kernel<64, 0, 0>);
+    case 128: return reinterpret_cast<const void*>(decompress_reduce_kernel<128, 0, 0>);
+    default: return reinterpret_cast<const void*>(decompress_reduce_kernel<256, 0, 0>);
+  }
+}
+
+namespace {
+template <int NB>
+void (*recompress_fn(int variant))(DecompressArgs) {
+  return variant == 0 ? decompress_reduce_kernel<NB, 1, 0> : decompress_reduce_kernel<NB, 1, 1>;
+}
+}  // namespace
+
+const void* recompress_kernel_ptr(int block, int variant) {
+  switch (block) {
+    case 64: return reinterpret_cast<const void*>(recompress_fn<64>(variant));
+    case 128: return reinterpret_cast<const void*>(recompress_fn<128>(variant));
+    default: return reinterpret_cast<const void*>(recompress_fn<256>(variant));
   }
 }
 
@@ -214,9 +297,28 @@ cudaError_t launch_decompress(const DecompressArgs& a, int block, int grid, cuda
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  void (*kern)(DecompressArgs) = block == 64    ? decompress_reduce_kernel<64>
-                                 : block == 128 ? decompress_reduce_kernel<128>
-                                                : decompress_reduce_kernel<256>;
+  void (*kern)(DecompressArgs) = block == 64    ? decompress_reduce_kernel<64, 0, 0>
+                                 : block == 128 ? decompress_reduce_kernel<128, 0, 0>
+                                                : decompress_reduce_kernel<256, 0, 0>;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_reduce_recompress(const DecompressArgs& a, int block, int variant, int grid,
+                                     cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kDecompressThreads);
+  cfg.dynamicSmemBytes = decompress_smem_bytes();
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void (*kern)(DecompressArgs) = block == 64    ? recompress_fn<64>(variant)
+                                 : block == 128 ? recompress_fn<128>(variant)
+                                                : recompress_fn<256>(variant);
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
   return e != cudaSuccess ? e : cudaGetLastError();
 }

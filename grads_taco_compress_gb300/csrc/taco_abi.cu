@@ -39,6 +39,7 @@ struct DeviceInfo {
   int sms = 0;
   int occ_compress[3][2] = {};
   int occ_decompress[3] = {};
+  int occ_recompress[3][2] = {};
 };
 
 std::once_flag g_once[kMaxDevices];
@@ -69,6 +70,13 @@ cudaError_t device_info(const DeviceInfo** out) {
         err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dsmem);
         if (err == cudaSuccess)
           err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ_decompress[b], k,
+                                                              kDecompressThreads, dsmem);
+      }
+      for (int v = 0; v < 2 && err == cudaSuccess; ++v) {
+        const void* k = recompress_kernel_ptr(blocks[b], v);
+        err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dsmem);
+        if (err == cudaSuccess)
+          err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ_recompress[b][v], k,
                                                               kDecompressThreads, dsmem);
       }
     }
@@ -124,6 +132,62 @@ taco_status decompress_common(const uint8_t* const* shards, int P, int64_t N, in
   if (grid < 1) grid = 1;
   if (launch_decompress(a, block, static_cast<int>(grid), static_cast<cudaStream_t>(stream)) !=
       cudaSuccess)
+    return TACO_ERR_CUDA;
+  return TACO_OK;
+}
+
+taco_status reduce_recompress_common(const uint8_t* const* shards, int P, int64_t N, int64_t h,
+                                     int block, float target_energy, int variant, void* shard_out,
+                                     taco_header* header_out, void* out, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
+  taco_status st = check_shape(N, h, block);
+  if (st != TACO_OK) return st;
+  if (P < 1 || P > TACO_MAX_SHARDS) return TACO_ERR_ARG;
+  if (variant != TACO_VARIANT_DUAL && variant != TACO_VARIANT_ABSMAX) return TACO_ERR_ARG;
+  if (!(target_energy > 0.0f) || !std::isfinite(target_energy)) return TACO_ERR_ARG;
+  if (!header_out) return TACO_ERR_NULL;
+  if (!workspace || workspace_bytes < kWorkspaceShardStride) return TACO_ERR_WORKSPACE;
+  if (!aligned(header_out, 8) || !aligned(workspace, 16)) return TACO_ERR_ALIGN;
+  const Layout l = shard_layout(N, h, block);
+  const size_t out_bytes = static_cast<size_t>(N) * static_cast<size_t>(h) * 2;
+  DecompressArgs a{};
+  if (N > 0) {
+    if (!shard_out) return TACO_ERR_NULL;
+    if (!aligned(shard_out, 16) || (out && !aligned(out, 16))) return TACO_ERR_ALIGN;
+    if (out && overlap(out, out_bytes, shard_out, l.bytes)) return TACO_ERR_ARG;
+    for (int p = 0; p < P; ++p) {
+      if (!shards[p]) return TACO_ERR_NULL;
+      if (!aligned(shards[p], 16)) return TACO_ERR_ALIGN;
+      if (overlap(shards[p], l.bytes, shard_out, l.bytes)) return TACO_ERR_ARG;
+      if (out && overlap(shards[p], l.bytes, out, out_bytes)) return TACO_ERR_ARG;
+      a.shard[p] = shards[p];
+    }
+  }
+  a.scales_off = l.scales_off;
+  a.P = P;
+  a.nblocks = N * h / block;
+  a.out = static_cast<uint16_t*>(out);
+  a.inv_sqrt_n = static_cast<float>(1.0 / std::sqrt(static_cast<double>(block)));
+  a.rc_shard = static_cast<uint8_t*>(shard_out);
+  a.rc_header = header_out;
+  a.workspace = static_cast<uint8_t*>(workspace);
+  a.N = N;
+  a.h = h;
+  a.target_energy = target_energy;
+  a.sqrt_E = static_cast<float>(std::sqrt(static_cast<double>(target_energy)));
+  a.sqrt_n = static_cast<float>(std::sqrt(static_cast<double>(block)));
+
+  const DeviceInfo* info = nullptr;
+  if (device_info(&info) != cudaSuccess) return TACO_ERR_CUDA;
+  const int tb = decompress_tile_blocks(block);
+  const int64_t tiles = (a.nblocks + tb - 1) / tb;
+  const int64_t needed = (tiles + kDecompressThreads / 32 - 1) / (kDecompressThreads / 32);
+  int64_t grid = static_cast<int64_t>(info->sms) * info->occ_recompress[block_index(block)][variant];
+  if (grid > needed) grid = needed;
+  if (grid > kMaxCtasPerShard) grid = kMaxCtasPerShard;
+  if (grid < 1) grid = 1;
+  if (launch_reduce_recompress(a, block, variant, static_cast<int>(grid),
+                               static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return TACO_ERR_CUDA;
   return TACO_OK;
 }
@@ -233,6 +297,35 @@ taco_status taco_decompress_reduce_ptrs(const void* const* shards, int P, int64_
   const uint8_t* ptrs[TACO_MAX_SHARDS];
   for (int p = 0; p < P; ++p) ptrs[p] = static_cast<const uint8_t*>(shards[p]);
   return decompress_common(ptrs, P, N, h, block, out_bf16, stream);
+}
+
+taco_status taco_reduce_recompress(const void* bundle, int P, int64_t N, int64_t h, int block,
+                                   float target_energy, int variant, void* shard_out,
+                                   taco_header* header_out, void* out_bf16, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  taco_status st = check_shape(N, h, block);
+  if (st != TACO_OK) return st;
+  if (P < 1 || P > TACO_MAX_SHARDS) return TACO_ERR_ARG;
+  if (N > 0 && !bundle) return TACO_ERR_NULL;
+  const size_t sb = shard_layout(N, h, block).bytes;
+  const uint8_t* ptrs[TACO_MAX_SHARDS];
+  for (int p = 0; p < P; ++p) ptrs[p] = static_cast<const uint8_t*>(bundle) + p * sb;
+  return reduce_recompress_common(ptrs, P, N, h, block, target_energy, variant, shard_out,
+                                  header_out, out_bf16, workspace, workspace_bytes, stream);
+}
+
+taco_status taco_reduce_recompress_ptrs(const void* const* shards, int P, int64_t N, int64_t h,
+                                        int block, float target_energy, int variant,
+                                        void* shard_out, taco_header* header_out, void* out_bf16,
+                                        void* workspace, size_t workspace_bytes, void* stream) {
+  taco_status st = check_shape(N, h, block);
+  if (st != TACO_OK) return st;
+  if (P < 1 || P > TACO_MAX_SHARDS) return TACO_ERR_ARG;
+  if (!shards) return TACO_ERR_NULL;
+  const uint8_t* ptrs[TACO_MAX_SHARDS];
+  for (int p = 0; p < P; ++p) ptrs[p] = static_cast<const uint8_t*>(shards[p]);
+  return reduce_recompress_common(ptrs, P, N, h, block, target_energy, variant, shard_out,
+                                  header_out, out_bf16, workspace, workspace_bytes, stream);
 }
 
 taco_status taco_e4m3_encode_f32(const float* in, uint8_t* out, int64_t n, void* stream) {

@@ -20,6 +20,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "taco.h"
+
 namespace taco {
 
 constexpr unsigned kFullMask = 0xffffffffu;
@@ -342,6 +344,83 @@ __device__ __forceinline__ float block_max(float v) {
 #pragma unroll
   for (int m = 1; m < LPB; m <<= 1) v = fmaxf(v, __shfl_xor_sync(kFullMask, v, m));
   return v;
+}
+
+// Per-tensor header of one shard, written in the same launch: every thread
+// brings its (max s, count of s > 1); the CTA reduces them, writes one
+// partial into the shard's workspace and counts its arrival; the last CTA to
+// arrive reduces all partials, writes the header and resets the counter.
+// Workspace of a shard: [uint32 counter | pad to 16 | float2 partial per CTA].
+template <int THREADS>
+__device__ void finish_header(float part_smax, uint32_t part_cnt, uint8_t* ws_shard,
+                              taco_header* hd, int64_t N, int64_t h, int block, int variant,
+                              float target_energy) {
+  constexpr int WARPS = THREADS / 32;
+  __shared__ float sh_max[WARPS];
+  __shared__ uint32_t sh_cnt[WARPS];
+  __shared__ bool sh_last;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) {
+    part_smax = fmaxf(part_smax, __shfl_xor_sync(kFullMask, part_smax, m));
+    part_cnt += __shfl_xor_sync(kFullMask, part_cnt, m);
+  }
+  if (lane == 0) {
+    sh_max[warp] = part_smax;
+    sh_cnt[warp] = part_cnt;
+  }
+  __syncthreads();
+  uint32_t* counter = reinterpret_cast<uint32_t*>(ws_shard);
+  float2* partials = reinterpret_cast<float2*>(ws_shard + 16);
+  if (threadIdx.x == 0) {
+    float m = 0.f;
+    uint32_t n = 0;
+    for (int w = 0; w < WARPS; ++w) {
+      m = fmaxf(m, sh_max[w]);
+      n += sh_cnt[w];
+    }
+    partials[blockIdx.x] = make_float2(m, __uint_as_float(n));
+    __threadfence();
+    const uint32_t arrived = atomicAdd(counter, 1u);
+    sh_last = (arrived == gridDim.x - 1);
+  }
+  __syncthreads();
+  if (!sh_last) return;
+  __threadfence();
+  float m = 0.f;
+  uint32_t n = 0;
+  for (int i = threadIdx.x; i < static_cast<int>(gridDim.x); i += THREADS) {
+    const float2 p = __ldcg(partials + i);
+    m = fmaxf(m, p.x);
+    n += __float_as_uint(p.y);
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    m = fmaxf(m, __shfl_xor_sync(kFullMask, m, o));
+    n += __shfl_xor_sync(kFullMask, n, o);
+  }
+  __syncthreads();
+  if (lane == 0) {
+    sh_max[warp] = m;
+    sh_cnt[warp] = n;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < WARPS; ++w) {
+      m = fmaxf(m, sh_max[w]);
+      n += sh_cnt[w];
+    }
+    hd->N = N;
+    hd->h = h;
+    hd->block = block;
+    hd->variant = variant;
+    hd->target_energy = target_energy;
+    hd->q_max = 448.0f;
+    hd->s_max = m;
+    hd->n_clamped = n;
+    *counter = 0u;   // leave the workspace zero-filled for the next call
+  }
 }
 
 __device__ __forceinline__ float max3(float a, float b, float c) {

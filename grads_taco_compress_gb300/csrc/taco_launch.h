@@ -43,8 +43,17 @@ struct DecompressArgs {
   size_t scales_off;
   int P;
   int64_t nblocks;
-  uint16_t* out;            // [N][h] bf16
+  uint16_t* out;            // [N][h] bf16 (reduce-recompress: may be null)
   float inv_sqrt_n;
+  // reduce-recompress only: the compressed sum and its header
+  uint8_t* rc_shard;        // codes | (alpha, s) pairs, same layout as the inputs
+  taco_header* rc_header;
+  uint8_t* workspace;       // one shard's header workspace
+  int64_t N;
+  int64_t h;
+  float target_energy;
+  float sqrt_E;             // fp32(sqrt(E*))
+  float sqrt_n;             // fp32(sqrt(block))
 };
 
 int compress_tile_blocks(int block);
@@ -58,6 +67,9 @@ int decompress_tile_blocks(int block);
 size_t decompress_smem_bytes();
 const void* decompress_kernel_ptr(int block);
 cudaError_t launch_decompress(const DecompressArgs& a, int block, int grid, cudaStream_t stream);
+const void* recompress_kernel_ptr(int block, int variant);
+cudaError_t launch_reduce_recompress(const DecompressArgs& a, int block, int variant, int grid,
+                                     cudaStream_t stream);
 cudaError_t decompress_fault(unsigned int* bits, bool clear);
 
 cudaError_t launch_e4m3_encode(const float* in, uint8_t* out, int64_t n, cudaStream_t st);

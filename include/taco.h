@@ -168,6 +168,31 @@ taco_status taco_decompress_reduce_ptrs(const void* const* shards, int P, int64_
                                         int64_t h, int block, void* out_bf16,
                                         void* stream);
 
+/* ---- taco_reduce_recompress ---------------------------------------------
+ * The reduced chunk compressed again for the AllGather half of the two-shot
+ * AllReduce (TACO pt summary §2.B.3: compression around ReduceScatter +
+ * AllGather), fused with the reduce: the P shards of `bundle` (as for
+ * taco_decompress_reduce) are summed and the sum x_hat is compressed into
+ * one shard at `shard_out` with its header at `header_out`, with the same
+ * block, target energy and variant rules as taco_compress. x_hat is
+ * compressed as computed, without rounding it to bf16 first. Because the
+ * rotation is shared and orthogonal, this needs no Hadamard transform on the
+ * device: the rotated sum is already at hand. If `out_bf16` is not NULL the
+ * bf16 sum [N, h] is written there as well (bit-identical to
+ * taco_decompress_reduce). `workspace`: at least taco_workspace_bytes(1)
+ * zero-filled bytes, as for compress. No output may overlap an input. */
+taco_status taco_reduce_recompress(const void* bundle, int P, int64_t N, int64_t h, int block,
+                                   float target_energy, int variant, void* shard_out,
+                                   taco_header* header_out, void* out_bf16, void* workspace,
+                                   size_t workspace_bytes, void* stream);
+
+/* The same with the P shards in separate buffers (`shards`: host array of P
+ * device pointers, read before the call returns). */
+taco_status taco_reduce_recompress_ptrs(const void* const* shards, int P, int64_t N, int64_t h,
+                                        int block, float target_energy, int variant,
+                                        void* shard_out, taco_header* header_out, void* out_bf16,
+                                        void* workspace, size_t workspace_bytes, void* stream);
+
 /* ---- E4M3 codec ----------------------------------------------------------
  * Elementwise conversions with the instructions the operator's kernels use
  * (TACO pt summary §2.A: FP8 E4M3 instead of INT8). `in` and `out` are device

@@ -155,3 +155,22 @@ def test_fault_api_rejects(lib):
     assert lib.taco_selftest_wait_timeout(1000, A + 2, None) == ALIGN
     assert lib.taco_selftest_wait_timeout(0, A, None) == ARG
     assert lib.taco_selftest_wait_timeout(3_000_000_000, A, None) == ARG
+
+
+@no_gpu_only
+def test_reduce_recompress_rejects(lib):
+    def call(bundle=A, P=2, N=4, h=256, block=128, E=4096.0, variant=0, shard=A * 64, hdr=A * 128,
+             out=None, ws=A * 256, wsb=WSB):
+        return lib.taco_reduce_recompress(bundle, P, N, h, block, E, variant, shard, hdr, out, ws, wsb, None)
+    assert call(block=100) == BLOCK
+    assert call(h=200, block=64) == SHAPE
+    assert call(P=0) == ARG and call(P=17) == ARG
+    assert call(variant=3) == ARG and call(E=0.0) == ARG and call(E=float("nan")) == ARG
+    assert call(hdr=None) == NULL and call(ws=None) == WS and call(wsb=64) == WS
+    assert call(bundle=None) == NULL and call(shard=None) == NULL
+    assert call(shard=A * 64 + 8) == ALIGN and call(out=A * 512 + 4) == ALIGN
+    assert call(shard=A + 256) == ARG                     # output shard inside the inputs
+    assert call(out=A * 64) == ARG                        # bf16 output over the output shard
+    arr = (ctypes.c_void_p * 2)(A, None)
+    assert lib.taco_reduce_recompress_ptrs(arr, 2, 4, 256, 128, 4096.0, 0, A * 64, A * 128, None,
+                                           A * 256, WSB, None) == NULL
