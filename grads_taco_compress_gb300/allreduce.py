@@ -1,0 +1,82 @@
+"""TACO's compressed two-shot AllReduce among R logical ranks on one GPU.
+
+The two-shot AllReduce of the TACO pages (gist.science pt summary, §2.B.3:
+ReduceScatter + AllGather with the compression operator between the phases)
+over R ranks whose tensors all live on this GPU. Nothing here computes:
+every step is a libtaco call, and the two exchanges are pointer
+permutations, which is what the receive buffers of a real ReduceScatter and
+AllGather would hand to the same calls.
+
+  rank r:  X_r [M, h] = R row chunks of [M/R, h]
+  1. compress      rank r compresses its R chunks         (taco_compress_shards)
+  2. ReduceScatter rank c receives chunk c of every rank  (pointers)
+  3. reduce        rank c sums and recompresses them      (taco_reduce_recompress_ptrs)
+  4. AllGather     every rank receives the R results      (pointers)
+  5. expand        the R chunks to the full [M, h] result (taco_decompress_shards_ptrs)
+
+All ranks end with the same tensor, so step 5 runs once.
+"""
+
+from __future__ import annotations
+
+import torch
+
+from . import binding as tb
+
+
+class EmulatedTwoShotAllReduce:
+    """Preallocated buffers and the launch sequence of one compressed AllReduce."""
+
+    def __init__(self, R: int, M: int, h: int, block: int,
+                 target_energy: float = tb.DEFAULT_TARGET_ENERGY, variant: int = tb.VARIANT_DUAL,
+                 device="cuda"):
+        if not 1 <= R <= tb.MAX_SHARDS:
+            raise ValueError(f"R must be in 1..{tb.MAX_SHARDS}")
+        if M % R:
+            raise ValueError("M must be a multiple of R")
+        self.R, self.M, self.h, self.block = R, M, h, block
+        self.chunk = M // R
+        self.target_energy, self.variant = float(target_energy), variant
+        dev = torch.device(device)
+        sb = tb.shard_bytes(self.chunk, h, block)
+        self.bundles = [torch.empty((R, sb), dtype=torch.uint8, device=dev) for _ in range(R)]
+        self.headers = [torch.empty((R, tb.HEADER_BYTES), dtype=torch.uint8, device=dev) for _ in range(R)]
+        self.reduced = [torch.empty(sb, dtype=torch.uint8, device=dev) for _ in range(R)]
+        self.reduced_headers = [torch.empty(tb.HEADER_BYTES, dtype=torch.uint8, device=dev) for _ in range(R)]
+        self.out = torch.empty((M, h), dtype=torch.bfloat16, device=dev)
+        self.workspace = tb.new_workspace(R, dev)
+        self._graph = None
+
+    def launches(self) -> int:
+        """Kernel launches of one AllReduce."""
+        return 2 * self.R + 1
+
+    def __call__(self, xs: torch.Tensor, stream=None) -> torch.Tensor:
+        """xs: bf16 [R, M, h], rank r's tensor in xs[r]. Returns the reduced [M, h]."""
+        R, c, h, n = self.R, self.chunk, self.h, self.block
+        if xs.shape != (R, self.M, h) or xs.dtype != torch.bfloat16 or not xs.is_contiguous():
+            raise ValueError(f"xs must be a contiguous bf16 tensor of shape {(R, self.M, h)}")
+        for r in range(R):                                            # 1. compress
+            tb.taco_compress_shards(xs[r].view(R, c, h), n, self.target_energy, self.variant,
+                                    bundle=self.bundles[r], headers=self.headers[r],
+                                    workspace=self.workspace, stream=stream)
+        for dst in range(R):                                          # 2.+3. reduce-scatter
+            received = [self.bundles[r][dst] for r in range(R)]
+            tb.taco_reduce_recompress_ptrs(received, c, h, n, self.target_energy, self.variant,
+                                           shard=self.reduced[dst], header=self.reduced_headers[dst],
+                                           workspace=self.workspace, stream=stream)
+        tb.taco_decompress_shards_ptrs(self.reduced, c, h, n,          # 4.+5. all-gather
+                                       out=self.out.view(R, c, h), stream=stream)
+        return self.out
+
+    def capture(self, xs: torch.Tensor) -> torch.cuda.CUDAGraph:
+        """Record one AllReduce of `xs` (fixed address) into a CUDA graph.
+
+        Call the object once outside capture first: the library's one-time
+        per-device set-up cannot run inside a capture.
+        """
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self(xs)
+        self._graph = g
+        return g

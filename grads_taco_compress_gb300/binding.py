@@ -39,6 +39,7 @@ EXPORTED_SYMBOLS = (
     "taco_compress_shards_noalloc",
     "taco_decompress_reduce", "taco_decompress_reduce_ptrs",
     "taco_reduce_recompress", "taco_reduce_recompress_ptrs",
+    "taco_decompress_shards", "taco_decompress_shards_ptrs",
     "taco_e4m3_encode_f32", "taco_e4m3_decode_f32",
     "taco_get_fault", "taco_selftest_wait_timeout",
     "taco_status_string", "taco_abi_version",
@@ -74,6 +75,8 @@ def _lib() -> ctypes.CDLL:
             "taco_compress_shards_noalloc": (i32, [vp, i32, i64, i64, i32, f32, i32, vp, vp, vp]),
             "taco_decompress_reduce": (i32, [vp, i32, i64, i64, i32, vp, vp]),
             "taco_decompress_reduce_ptrs": (i32, [ctypes.POINTER(vp), i32, i64, i64, i32, vp, vp]),
+            "taco_decompress_shards": (i32, [vp, i32, i64, i64, i32, vp, vp]),
+            "taco_decompress_shards_ptrs": (i32, [ctypes.POINTER(vp), i32, i64, i64, i32, vp, vp]),
             "taco_reduce_recompress": (i32, [vp, i32, i64, i64, i32, f32, i32, vp, vp, vp, vp, sz, vp]),
             "taco_reduce_recompress_ptrs": (i32, [ctypes.POINTER(vp), i32, i64, i64, i32, f32, i32,
                                                   vp, vp, vp, vp, sz, vp]),
@@ -240,6 +243,30 @@ def taco_decompress_reduce_ptrs(shards, N: int, h: int, block: int,
     arr = (ctypes.c_void_p * max(P, 1))(*[_ptr(s) for s in shards])
     st = _lib().taco_decompress_reduce_ptrs(arr, P, N, h, block, _ptr(out), _stream_ptr(stream))
     _check(st, "taco_decompress_reduce_ptrs")
+    return out
+
+
+def taco_decompress_shards(bundle: torch.Tensor, P: int, N: int, h: int, block: int,
+                           out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Each of the P shards of a bundle reconstructed on its own: bf16 [P, N, h]."""
+    if not bundle.is_cuda:
+        raise ValueError("bundle must be a CUDA tensor")
+    if out is None:
+        out = torch.empty((P, N, h), dtype=torch.bfloat16, device=bundle.device)
+    st = _lib().taco_decompress_shards(_ptr(bundle), P, N, h, block, _ptr(out), _stream_ptr(stream))
+    _check(st, "taco_decompress_shards")
+    return out
+
+
+def taco_decompress_shards_ptrs(shards, N: int, h: int, block: int,
+                                out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """As taco_decompress_shards with P separate shard tensors."""
+    P = len(shards)
+    if out is None:
+        out = torch.empty((P, N, h), dtype=torch.bfloat16, device=shards[0].device)
+    arr = (ctypes.c_void_p * max(P, 1))(*[_ptr(s) for s in shards])
+    st = _lib().taco_decompress_shards_ptrs(arr, P, N, h, block, _ptr(out), _stream_ptr(stream))
+    _check(st, "taco_decompress_shards_ptrs")
     return out
 
 

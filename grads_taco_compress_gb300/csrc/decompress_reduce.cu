@@ -32,6 +32,8 @@ constexpr uint32_t kStageBytes = kCodesBytes + kScaleBytes;
 constexpr uint32_t kOutBytes = kTileElems * 2;        // bf16 output of one tile
 
 // MODE 0: decompress-reduce to bf16.
+// MODE 2: decompress without a sum: shard blockIdx.y to output rows
+//         blockIdx.y * N .. (the AllGather side of the two-shot AllReduce).
 // MODE 1: reduce-recompress. The sum x_hat = H z of the P reconstructions is
 // compressed again without leaving the rotated domain: H x_hat = n z and
 // sum x_hat^2 = n sum z^2 (H symmetric, H H = n I), so alpha' = sqrt(E* /
@@ -54,7 +56,9 @@ decompress_reduce_kernel(DecompressArgs a) {
   const int j = lane & (LPB - 1);
   const int sub = lane / LPB;
   const int cx = sub & (kCH - 1);
-  const int P = a.P;
+  const int P = (MODE == 2) ? 1 : a.P;
+  const uint8_t* const* shard_of = (MODE == 2) ? a.shard + blockIdx.y : a.shard;
+  uint16_t* const out_base = (MODE == 2) ? a.out + static_cast<int64_t>(blockIdx.y) * a.nblocks * NB : a.out;
 
   const uint32_t stage0 = smem_u32(smem) + warp * (D * kStageBytes);
   const uint32_t bar0 = smem_u32(smem) + WARPS * D * kStageBytes + warp * (D * 8);
@@ -89,7 +93,7 @@ decompress_reduce_kernel(DecompressArgs a) {
       const uint32_t sbytes = (vb * 8 + 15) & ~15u;   // stays inside the 256-byte padding
       const uint32_t dst = stage0 + is * kStageBytes;
       const uint32_t bar = bar0 + 8 * is;
-      const uint8_t* base = a.shard[ip];
+      const uint8_t* base = shard_of[ip];
       const uint64_t policy = l2_evict_first_policy();
       fence_proxy_async_smem();
       mbar_arrive_expect_tx(bar, cbytes + sbytes);
@@ -230,7 +234,7 @@ decompress_reduce_kernel(DecompressArgs a) {
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-      tma_store_1d(a.out + b0 * NB, out0, static_cast<uint32_t>(vb) * (NB * 2));
+      tma_store_1d(out_base + b0 * NB, out0, static_cast<uint32_t>(vb) * (NB * 2));
       bulk_commit();
     }
   }
@@ -302,6 +306,33 @@ cudaError_t launch_decompress(const DecompressArgs& a, int block, int grid, cuda
                                                 : decompress_reduce_kernel<256, 0, 0>;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
   return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_decompress_shards(const DecompressArgs& a, int block, int grid, int P,
+                                     cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, P);
+  cfg.blockDim = dim3(kDecompressThreads);
+  cfg.dynamicSmemBytes = decompress_smem_bytes();
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void (*kern)(DecompressArgs) = block == 64    ? decompress_reduce_kernel<64, 2, 0>
+                                 : block == 128 ? decompress_reduce_kernel<128, 2, 0>
+                                                : decompress_reduce_kernel<256, 2, 0>;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+const void* gather_kernel_ptr(int block) {
+  switch (block) {
+    case 64: return reinterpret_cast<const void*>(decompress_reduce_kernel<64, 2, 0>);
+    case 128: return reinterpret_cast<const void*>(decompress_reduce_kernel<128, 2, 0>);
+    default: return reinterpret_cast<const void*>(decompress_reduce_kernel<256, 2, 0>);
+  }
 }
 
 cudaError_t launch_reduce_recompress(const DecompressArgs& a, int block, int variant, int grid,

@@ -40,6 +40,7 @@ struct DeviceInfo {
   int occ_compress[3][2] = {};
   int occ_decompress[3] = {};
   int occ_recompress[3][2] = {};
+  int occ_gather[3] = {};
 };
 
 std::once_flag g_once[kMaxDevices];
@@ -70,6 +71,13 @@ cudaError_t device_info(const DeviceInfo** out) {
         err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dsmem);
         if (err == cudaSuccess)
           err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ_decompress[b], k,
+                                                              kDecompressThreads, dsmem);
+      }
+      if (err == cudaSuccess) {
+        const void* k = gather_kernel_ptr(blocks[b]);
+        err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dsmem);
+        if (err == cudaSuccess)
+          err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ_gather[b], k,
                                                               kDecompressThreads, dsmem);
       }
       for (int v = 0; v < 2 && err == cudaSuccess; ++v) {
@@ -131,6 +139,43 @@ taco_status decompress_common(const uint8_t* const* shards, int P, int64_t N, in
   if (grid > needed) grid = needed;
   if (grid < 1) grid = 1;
   if (launch_decompress(a, block, static_cast<int>(grid), static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return TACO_ERR_CUDA;
+  return TACO_OK;
+}
+
+taco_status decompress_shards_common(const uint8_t* const* shards, int P, int64_t N, int64_t h,
+                                     int block, void* out, void* stream) {
+  taco_status st = check_shape(N, h, block);
+  if (st != TACO_OK) return st;
+  if (P < 1 || P > TACO_MAX_SHARDS) return TACO_ERR_ARG;
+  if (N == 0) return TACO_OK;
+  if (!out) return TACO_ERR_NULL;
+  if (!aligned(out, 16)) return TACO_ERR_ALIGN;
+  const Layout l = shard_layout(N, h, block);
+  const size_t out_bytes = static_cast<size_t>(P) * N * h * 2;
+  DecompressArgs a{};
+  for (int p = 0; p < P; ++p) {
+    if (!shards[p]) return TACO_ERR_NULL;
+    if (!aligned(shards[p], 16)) return TACO_ERR_ALIGN;
+    if (overlap(shards[p], l.bytes, out, out_bytes)) return TACO_ERR_ARG;
+    a.shard[p] = shards[p];
+  }
+  a.scales_off = l.scales_off;
+  a.P = P;
+  a.nblocks = N * h / block;
+  a.out = static_cast<uint16_t*>(out);
+  a.inv_sqrt_n = static_cast<float>(1.0 / std::sqrt(static_cast<double>(block)));
+  const DeviceInfo* info = nullptr;
+  if (device_info(&info) != cudaSuccess) return TACO_ERR_CUDA;
+  const int tb = decompress_tile_blocks(block);
+  const int64_t tiles = (a.nblocks + tb - 1) / tb;
+  const int64_t needed = (tiles + kDecompressThreads / 32 - 1) / (kDecompressThreads / 32);
+  const int64_t total = static_cast<int64_t>(info->sms) * info->occ_gather[block_index(block)];
+  int64_t gx = (total + P - 1) / P;
+  if (gx > needed) gx = needed;
+  if (gx < 1) gx = 1;
+  if (launch_decompress_shards(a, block, static_cast<int>(gx), P, static_cast<cudaStream_t>(stream)) !=
       cudaSuccess)
     return TACO_ERR_CUDA;
   return TACO_OK;
@@ -297,6 +342,31 @@ taco_status taco_decompress_reduce_ptrs(const void* const* shards, int P, int64_
   const uint8_t* ptrs[TACO_MAX_SHARDS];
   for (int p = 0; p < P; ++p) ptrs[p] = static_cast<const uint8_t*>(shards[p]);
   return decompress_common(ptrs, P, N, h, block, out_bf16, stream);
+}
+
+taco_status taco_decompress_shards(const void* bundle, int P, int64_t N, int64_t h, int block,
+                                   void* out_bf16, void* stream) {
+  taco_status st = check_shape(N, h, block);
+  if (st != TACO_OK) return st;
+  if (P < 1 || P > TACO_MAX_SHARDS) return TACO_ERR_ARG;
+  if (N == 0) return TACO_OK;
+  if (!bundle) return TACO_ERR_NULL;
+  const size_t sb = shard_layout(N, h, block).bytes;
+  const uint8_t* ptrs[TACO_MAX_SHARDS];
+  for (int p = 0; p < P; ++p) ptrs[p] = static_cast<const uint8_t*>(bundle) + p * sb;
+  return decompress_shards_common(ptrs, P, N, h, block, out_bf16, stream);
+}
+
+taco_status taco_decompress_shards_ptrs(const void* const* shards, int P, int64_t N, int64_t h,
+                                        int block, void* out_bf16, void* stream) {
+  taco_status st = check_shape(N, h, block);
+  if (st != TACO_OK) return st;
+  if (P < 1 || P > TACO_MAX_SHARDS) return TACO_ERR_ARG;
+  if (N == 0) return TACO_OK;
+  if (!shards) return TACO_ERR_NULL;
+  const uint8_t* ptrs[TACO_MAX_SHARDS];
+  for (int p = 0; p < P; ++p) ptrs[p] = static_cast<const uint8_t*>(shards[p]);
+  return decompress_shards_common(ptrs, P, N, h, block, out_bf16, stream);
 }
 
 taco_status taco_reduce_recompress(const void* bundle, int P, int64_t N, int64_t h, int block,

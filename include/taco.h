@@ -168,6 +168,21 @@ taco_status taco_decompress_reduce_ptrs(const void* const* shards, int P, int64_
                                         int64_t h, int block, void* out_bf16,
                                         void* stream);
 
+/* ---- taco_decompress_shards ---------------------------------------------
+ * Reconstruct each of the P shards of `bundle` on its own (no sum) into
+ * out_bf16 [P][N][h]: shard p to rows p*N .. p*N+N-1. This is the receive
+ * side of the AllGather half of the two-shot AllReduce (TACO pt summary
+ * §2.B.3), where every rank expands the P reduced chunks into the full
+ * tensor; the reconstruction is that of §2.B.2, the same arithmetic as
+ * taco_decompress_reduce with P = 1 (bit-identical output). One launch.
+ * N == 0 launches nothing. */
+taco_status taco_decompress_shards(const void* bundle, int P, int64_t N, int64_t h, int block,
+                                   void* out_bf16, void* stream);
+
+/* The same with the shards in separate buffers (host array of P pointers). */
+taco_status taco_decompress_shards_ptrs(const void* const* shards, int P, int64_t N, int64_t h,
+                                        int block, void* out_bf16, void* stream);
+
 /* ---- taco_reduce_recompress ---------------------------------------------
  * The reduced chunk compressed again for the AllGather half of the two-shot
  * AllReduce (TACO pt summary §2.B.3: compression around ReduceScatter +

@@ -1,0 +1,60 @@
+"""The emulated compressed two-shot AllReduce against the oracle's pipeline.
+
+The oracle runs the same five steps with its own compress, reduce_recompress
+and decompress on the same rank tensors; the GPU result must match it within
+the reconstruction tolerance and approximate the exact sum within the error
+of two E4M3 quantisations."""
+
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import parity
+from grads_taco_compress_gb300 import workloads as W
+from grads_taco_compress_gb300.allreduce import EmulatedTwoShotAllReduce
+from oracle import taco_oracle as O
+from test_gpu_parity import dev_bf16, host_bits
+
+pytestmark = pytest.mark.gpu
+E_STAR = 4096.0
+
+
+def oracle_allreduce(xs, block):
+    R, M, h = xs.shape
+    c = M // R
+    parts = [[O.compress(xs[r, k * c:(k + 1) * c], block, E_STAR) for k in range(R)] for r in range(R)]
+    out = []
+    for k in range(R):
+        codes = np.stack([parts[r][k][0] for r in range(R)])
+        alpha = np.stack([parts[r][k][1] for r in range(R)])
+        s = np.stack([parts[r][k][2] for r in range(R)])
+        rc, ra, rs, _ = O.reduce_recompress(codes, alpha, s, block, E_STAR)
+        out.append(O.decompress_reduce(rc[None], ra[None], rs[None], block))
+    return np.concatenate(out)
+
+
+@pytest.mark.parametrize("name,R,M", [("gpt2-1.5b-act", 4, 64), ("gpt3-6.7b-act", 8, 48),
+                                      ("gpt3-6.7b-grad", 2, 30), ("tiny-512x1024", 2, 128)])
+def test_allreduce_matches_oracle_pipeline(name, R, M):
+    w = dataclasses.replace(W.WORKLOADS[name], P=R)
+    xs = W.make_shards(w, N=M)                                   # rank r's tensor in xs[r]
+    ar = EmulatedTwoShotAllReduce(R, M, w.h, w.block)
+    got = host_bits(ar(dev_bf16(xs)))
+    want = oracle_allreduce(xs, w.block)
+    parity.compare_recon(O.bf16_bits_to_f64(got), O.bf16_bits_to_f64(want), "allreduce output")
+    exact = O.bf16_bits_to_f64(xs).sum(axis=0)
+    assert parity.rel_rms(O.bf16_bits_to_f64(got), exact) < 0.06
+
+
+def test_allreduce_graph_replay_equals_eager():
+    w = dataclasses.replace(W.WORKLOADS["gpt2-1.5b-act"], P=4)
+    xs = dev_bf16(W.make_shards(w, N=256))
+    ar = EmulatedTwoShotAllReduce(4, 256, w.h, w.block)
+    eager = ar(xs).clone()
+    g = ar.capture(xs)
+    ar.out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(ar.out.view(torch.int16), eager.view(torch.int16))
