@@ -58,3 +58,19 @@ def test_allreduce_graph_replay_equals_eager():
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(ar.out.view(torch.int16), eager.view(torch.int16))
+
+
+@pytest.mark.parametrize("block,P", [(64, 5), (128, 3), (256, 2)])
+def test_decompress_shards_each_shard_alone(block, P):
+    from grads_taco_compress_gb300 import binding as tb
+    from test_gpu_parity import bundle_from_arrays
+    N, h = 19, 3 * block
+    codes, alpha, s = W.make_random_bundle(N, h, block, P, seed=block)
+    bundle = bundle_from_arrays(codes, alpha, s, block)
+    out = tb.taco_decompress_shards(bundle, P, N, h, block)
+    for p in range(P):
+        single = tb.taco_decompress_reduce(bundle[p], 1, N, h, block)
+        torch.cuda.synchronize()
+        assert torch.equal(out[p].view(torch.int16), single.view(torch.int16))
+        want = O.decompress_reduce(codes[p:p + 1], alpha[p:p + 1], s[p:p + 1], block)
+        parity.compare_recon(O.bf16_bits_to_f64(host_bits(out[p])), O.bf16_bits_to_f64(want))
