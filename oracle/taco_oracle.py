@@ -37,7 +37,11 @@ Readings taken where the pages are silent (each one is a choice):
     anti-underflow role of [DE] §3), s_k = max(1, amax/Q_max) is the overflow
     guard that makes the rotated values fit Q_max ([PT] §2.B.2). Variant
     ABSMAX (s_k = amax/Q_max for amax > 0, else 1) is kept for comparison; in
-    it alpha_k cancels from the codes.
+    it alpha_k cancels from the codes. Variant STATIC (one data-independent
+    s = sqrt(n E*)/Q_max for every block of the tensor, a per-tensor scale in
+    the sense of [ZH]) is kept for error studies: after the energy rescale
+    ||y||_2^2 = n E*, so by Cauchy-Schwarz |y_i| <= sqrt(n E*) and no code
+    ever saturates.
   * "energy" is the mean of squares (E* is per element), uncentred.
   * Hadamard: Sylvester natural order, orthonormal scaling 1/sqrt(n), no sign
     flips. The same n-element blocks carry alpha, the rotation and s.
@@ -67,6 +71,8 @@ Q_MAX = 448.0
 DEFAULT_TARGET_ENERGY = 4096.0
 VARIANT_DUAL = 0
 VARIANT_ABSMAX = 1
+VARIANT_STATIC = 2
+VARIANTS = (VARIANT_DUAL, VARIANT_ABSMAX, VARIANT_STATIC)
 BLOCK_SIZES = (64, 128, 256)
 
 
@@ -207,7 +213,7 @@ def compress_values_stages(x_values: np.ndarray, block: int,
     N, h = x_values.shape
     n = block
     _check_shape(h, n)
-    if variant not in (VARIANT_DUAL, VARIANT_ABSMAX):
+    if variant not in VARIANTS:
         raise ValueError("unknown variant")
     K = h // n
     x = x_values.reshape(N, K, n)
@@ -229,8 +235,11 @@ def compress_values_stages(x_values: np.ndarray, block: int,
     amax = np.max(np.abs(y.astype(np.float64)), axis=-1)
     if variant == VARIANT_DUAL:
         s = np.maximum(1.0, amax / Q_MAX).astype(np.float32)
-    else:
+    elif variant == VARIANT_ABSMAX:
         s = np.where(amax > 0, amax / Q_MAX, 1.0).astype(np.float32)
+    else:
+        # one scale for the whole tensor, fixed by E* and n alone
+        s = np.full((N, K), np.float32(static_scale(n, target_energy)), dtype=np.float32)
 
     # 5. FP8 E4M3 codes of y / s_k (the value rounded is an fp32 number)
     ratio = (y.astype(np.float64) / s.astype(np.float64)[..., None]).astype(np.float32)
@@ -245,6 +254,11 @@ def compress_values_stages(x_values: np.ndarray, block: int,
     }
     return {"energy": energy, "alpha": alpha, "y": y, "amax": amax, "s": s,
             "codes": codes, "header": header}
+
+
+def static_scale(block: int, target_energy: float = DEFAULT_TARGET_ENERGY) -> float:
+    """fp32(sqrt(n E*) / Q_max): the STATIC variant's scale of every block."""
+    return float(np.float32(math.sqrt(block * float(target_energy)) / Q_MAX))
 
 
 def compress(x_bits: np.ndarray, block: int,

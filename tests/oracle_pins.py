@@ -248,6 +248,49 @@ def check_absmax_variant(O):
     assert np.mean(c1 == c2) > 0.9999                 # alpha cancels from the codes
 
 
+def check_static_variant(O):
+    """STATIC: one scale sqrt(n E*)/Q_max for every block; Cauchy-Schwarz bound.
+
+    After the energy rescale ||y||^2 = n E*, so |y_i| <= sqrt(n E*): a block
+    equal to a scaled Hadamard row reaches the bound (one code +-448, the rest
+    zero), a spike block spreads evenly (every code +-448/sqrt(n)), and no
+    ratio y/s of any block exceeds 448.
+    """
+    rng = np.random.default_rng(12)
+    for n in (64, 128, 256):
+        s_ref = np.float32(math.sqrt(n * E_STAR) / 448.0)
+        H = O.sylvester_hadamard(n)
+        for c in (0.0078125, -3.5):
+            k = int(rng.integers(n))
+            row = _bf16_bits(np.float32(c) * H[k].astype(np.float32))[None, :]
+            codes, alpha, s, hdr = O.compress(row, n, E_STAR, O.VARIANT_STATIC)
+            assert s[0, 0] == s_ref
+            want = np.zeros(n, dtype=np.int64)
+            want[k] = 0x7E if c > 0 else 0xFE
+            got = codes[0].astype(np.int64)
+            assert got[k] == want[k], (n, c)
+            assert np.all(np.delete(got, k) & 0x7F == 0), (n, c)
+            spike = np.zeros(n, dtype=np.float32)
+            spike[k] = c
+            codes, _, _, _ = O.compress(_bf16_bits(spike)[None, :], n, E_STAR, O.VARIANT_STATIC)
+            mag = np.abs(O.e4m3_decode(codes[0]))
+            target = 448.0 / math.sqrt(n)
+            assert np.all(mag == mag[0])
+            if n in (64, 256):
+                assert mag[0] == target                     # 56 and 28: exact E4M3 values
+            else:
+                assert abs(mag[0] - target) <= 2.0 ** (math.floor(math.log2(target)) - 4)
+        x = _random_bf16(rng, (16, 4 * n), 0.02)
+        x[3, :n] = 0                                          # a zero block keeps alpha = 1
+        st = O.compress_stages(x, n, E_STAR, O.VARIANT_STATIC)
+        assert np.all(st["s"] == s_ref)
+        assert st["alpha"][3, 0] == 1.0 and np.all(st["codes"][3, :n] & 0x7F == 0)
+        ratio = np.abs(st["y"].astype(np.float64) / float(s_ref))
+        assert ratio.max() <= 448.0 * (1 + 1e-6)
+        assert st["header"]["n_clamped"] == (st["s"].size if s_ref > 1.0 else 0)
+        assert st["header"]["s_max"] == float(s_ref)
+
+
 # --------------------------------------------------------------------------
 # Decompress-reduce: sum in the rotated domain, invert once (linearity)
 # --------------------------------------------------------------------------

@@ -36,6 +36,10 @@ MUTATIONS = {
     "reduce_drops_last_shard": ("for p in range(P):", "for p in range(P - 1):"),
     "recompress_first_shard_only": ("x_hat = decompress_reduce_f64(codes, alpha, s, block)",
                                     "x_hat = decompress_reduce_f64(codes[:1], alpha[:1], s[:1], block)"),
+    "static_scale_drops_n": ("math.sqrt(block * float(target_energy)) / Q_MAX",
+                             "math.sqrt(float(target_energy)) / Q_MAX"),
+    "static_scale_per_block_amax": ("np.full((N, K), np.float32(static_scale(n, target_energy)), dtype=np.float32)",
+                                    "np.maximum(1.0, amax / Q_MAX).astype(np.float32)"),
     "recompress_skips_alpha": ("    st = compress_values_stages(x_hat, block, target_energy, variant)\n    return st[\"codes\"], st[\"alpha\"]",
                                "    st = compress_values_stages(x_hat, block, target_energy, variant)\n    return st[\"codes\"], st[\"alpha\"] * 0 + 1"),
 }
