@@ -22,6 +22,7 @@ STATUS_NAMES = {0: "TACO_OK", 1: "TACO_ERR_NULL", 2: "TACO_ERR_SHAPE", 3: "TACO_
                 7: "TACO_ERR_WORKSPACE"}
 VARIANT_DUAL = 0
 VARIANT_ABSMAX = 1
+VARIANT_STATIC = 2
 MAX_SHARDS = 16
 HEADER_BYTES = 40
 DEFAULT_TARGET_ENERGY = 4096.0

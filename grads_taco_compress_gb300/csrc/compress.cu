@@ -8,7 +8,8 @@
 //   packed FMAs, lane shuffles) -> FWHT of the raw block in registers and
 //   shuffles (the rotation is linear, so alpha is applied afterwards together
 //   with 1/sqrt(n) and 1/s) -> alpha = sqrt(E*/E), s = max(1, alpha/sqrt(n) *
-//   max|Hx| / 448) -> E4M3 codes with cvt.rn.satfinite, written into the
+//   max|Hx| / 448) (ABSMAX: without the floor; STATIC: the per-tensor
+//   sqrt(n E*)/448) -> E4M3 codes with cvt.rn.satfinite, written into the
 //   tile's shared-memory stage and stored with one TMA bulk store per tile,
 //   one (alpha, s) pair store per block -> per-tensor header through per-CTA
 //   partials and a last-CTA reduction.
@@ -164,8 +165,9 @@ compress_kernel(CompressArgs a) {
     const float tmax = block_max<LPB>(fmaxf(thi, -tlo));
 
     const float amax = cscale * tmax;
-    const float sc = (VARIANT == 0) ? fmaxf(1.0f, amax * (1.0f / 448.0f))
-                                    : (amax > 0.f ? amax * (1.0f / 448.0f) : 1.0f);
+    const float sc = (VARIANT == 0)   ? fmaxf(1.0f, amax * (1.0f / 448.0f))
+                     : (VARIANT == 1) ? (amax > 0.f ? amax * (1.0f / 448.0f) : 1.0f)
+                                      : a.s_static;
     const float g = __fdividef(cscale, sc);           // code value = g * t
     const f2 g2{g, g};
 
@@ -222,9 +224,8 @@ compress_kernel(CompressArgs a) {
 }
 
 template <int NB>
-const void* kernel_ptr(int variant) {
-  return variant == 0 ? reinterpret_cast<const void*>(compress_kernel<NB, 0>)
-                      : reinterpret_cast<const void*>(compress_kernel<NB, 1>);
+void (*kernel_fn(int variant))(CompressArgs) {
+  return variant == 0 ? compress_kernel<NB, 0> : variant == 1 ? compress_kernel<NB, 1> : compress_kernel<NB, 2>;
 }
 
 }  // namespace
@@ -237,9 +238,9 @@ size_t compress_smem_bytes() {
 
 const void* compress_kernel_ptr(int block, int variant) {
   switch (block) {
-    case 64: return kernel_ptr<64>(variant);
-    case 128: return kernel_ptr<128>(variant);
-    default: return kernel_ptr<256>(variant);
+    case 64: return reinterpret_cast<const void*>(kernel_fn<64>(variant));
+    case 128: return reinterpret_cast<const void*>(kernel_fn<128>(variant));
+    default: return reinterpret_cast<const void*>(kernel_fn<256>(variant));
   }
 }
 
@@ -255,12 +256,9 @@ cudaError_t launch_compress(const CompressArgs& a, int block, int variant, int g
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  void (*kern)(CompressArgs) = nullptr;
-  switch (block) {
-    case 64: kern = variant == 0 ? compress_kernel<64, 0> : compress_kernel<64, 1>; break;
-    case 128: kern = variant == 0 ? compress_kernel<128, 0> : compress_kernel<128, 1>; break;
-    default: kern = variant == 0 ? compress_kernel<256, 0> : compress_kernel<256, 1>; break;
-  }
+  void (*kern)(CompressArgs) = block == 64    ? kernel_fn<64>(variant)
+                               : block == 128 ? kernel_fn<128>(variant)
+                                              : kernel_fn<256>(variant);
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
   return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -59,7 +59,9 @@ extern "C" taco_status taco_compress_shards_noalloc(const void* x_bf16, int P, i
   if (N < 0 || h <= 0 || h % block != 0 || (N > 0 && N > (int64_t{1} << 40) / h)) return TACO_ERR_SHAPE;
   if (P < 1 || P > TACO_MAX_SHARDS) return TACO_ERR_ARG;
   if (P > TACO_NOALLOC_MAX_SHARDS) return TACO_ERR_WORKSPACE;   // beyond the static scratch
-  if (variant != TACO_VARIANT_DUAL && variant != TACO_VARIANT_ABSMAX) return TACO_ERR_ARG;
+  if (variant != TACO_VARIANT_DUAL && variant != TACO_VARIANT_ABSMAX &&
+      variant != TACO_VARIANT_STATIC)
+    return TACO_ERR_ARG;
   if (!(target_energy > 0.0f) || !std::isfinite(target_energy)) return TACO_ERR_ARG;
   if (!headers_out) return TACO_ERR_NULL;
   if (!aligned(headers_out, 8)) return TACO_ERR_ALIGN;

@@ -181,8 +181,9 @@ decompress_reduce_kernel(DecompressArgs a) {
       const float zhi = max3(max3(hq[0], hq[1], hq[2]), max3(hq[3], hq[4], hq[5]), fmaxf(hq[6], hq[7]));
       const float zlo = min3(min3(lq[0], lq[1], lq[2]), min3(lq[3], lq[4], lq[5]), fminf(lq[6], lq[7]));
       const float amax = cscale * block_max<LPB>(fmaxf(zhi, -zlo));
-      const float sc = (VARIANT == 0) ? fmaxf(1.0f, amax * (1.0f / 448.0f))
-                                      : (amax > 0.f ? amax * (1.0f / 448.0f) : 1.0f);
+      const float sc = (VARIANT == 0)   ? fmaxf(1.0f, amax * (1.0f / 448.0f))
+                       : (VARIANT == 1) ? (amax > 0.f ? amax * (1.0f / 448.0f) : 1.0f)
+                                        : a.s_static;
       const float g = __fdividef(cscale, sc);
       const f2 g2{g, g};
       if (lane == 0) bulk_wait_read<0>();   // the previous store has read the buffer
@@ -278,7 +279,9 @@ const void* decompress_kernel_ptr(int block) {
 namespace {
 template <int NB>
 void (*recompress_fn(int variant))(DecompressArgs) {
-  return variant == 0 ? decompress_reduce_kernel<NB, 1, 0> : decompress_reduce_kernel<NB, 1, 1>;
+  return variant == 0   ? decompress_reduce_kernel<NB, 1, 0>
+         : variant == 1 ? decompress_reduce_kernel<NB, 1, 1>
+                        : decompress_reduce_kernel<NB, 1, 2>;
 }
 }  // namespace
 

@@ -18,6 +18,14 @@ inline size_t pad256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
 inline bool valid_block(int block) { return block == 64 || block == 128 || block == 256; }
 
+inline bool valid_variant(int v) {
+  return v == TACO_VARIANT_DUAL || v == TACO_VARIANT_ABSMAX || v == TACO_VARIANT_STATIC;
+}
+
+inline float static_scale(int block, float target_energy) {
+  return static_cast<float>(std::sqrt(static_cast<double>(block) * target_energy) / 448.0);
+}
+
 inline int block_index(int block) { return block == 64 ? 0 : (block == 128 ? 1 : 2); }
 
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -37,9 +45,9 @@ taco_status check_shape(int64_t N, int64_t h, int block) {
 // Per-device launch facts, filled once per device.
 struct DeviceInfo {
   int sms = 0;
-  int occ_compress[3][2] = {};
+  int occ_compress[3][kVariants] = {};
   int occ_decompress[3] = {};
-  int occ_recompress[3][2] = {};
+  int occ_recompress[3][kVariants] = {};
   int occ_gather[3] = {};
 };
 
@@ -59,7 +67,7 @@ cudaError_t device_info(const DeviceInfo** out) {
     const int csmem = static_cast<int>(compress_smem_bytes());
     const int dsmem = static_cast<int>(decompress_smem_bytes());
     for (int b = 0; b < 3 && err == cudaSuccess; ++b) {
-      for (int v = 0; v < 2 && err == cudaSuccess; ++v) {
+      for (int v = 0; v < kVariants && err == cudaSuccess; ++v) {
         const void* k = compress_kernel_ptr(blocks[b], v);
         err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, csmem);
         if (err == cudaSuccess)
@@ -80,7 +88,7 @@ cudaError_t device_info(const DeviceInfo** out) {
           err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ_gather[b], k,
                                                               kDecompressThreads, dsmem);
       }
-      for (int v = 0; v < 2 && err == cudaSuccess; ++v) {
+      for (int v = 0; v < kVariants && err == cudaSuccess; ++v) {
         const void* k = recompress_kernel_ptr(blocks[b], v);
         err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dsmem);
         if (err == cudaSuccess)
@@ -188,7 +196,7 @@ taco_status reduce_recompress_common(const uint8_t* const* shards, int P, int64_
   taco_status st = check_shape(N, h, block);
   if (st != TACO_OK) return st;
   if (P < 1 || P > TACO_MAX_SHARDS) return TACO_ERR_ARG;
-  if (variant != TACO_VARIANT_DUAL && variant != TACO_VARIANT_ABSMAX) return TACO_ERR_ARG;
+  if (!valid_variant(variant)) return TACO_ERR_ARG;
   if (!(target_energy > 0.0f) || !std::isfinite(target_energy)) return TACO_ERR_ARG;
   if (!header_out) return TACO_ERR_NULL;
   if (!workspace || workspace_bytes < kWorkspaceShardStride) return TACO_ERR_WORKSPACE;
@@ -221,6 +229,7 @@ taco_status reduce_recompress_common(const uint8_t* const* shards, int P, int64_
   a.target_energy = target_energy;
   a.sqrt_E = static_cast<float>(std::sqrt(static_cast<double>(target_energy)));
   a.sqrt_n = static_cast<float>(std::sqrt(static_cast<double>(block)));
+  a.s_static = static_scale(block, target_energy);
 
   const DeviceInfo* info = nullptr;
   if (device_info(&info) != cudaSuccess) return TACO_ERR_CUDA;
@@ -266,7 +275,7 @@ taco_status taco_compress_shards(const void* x_bf16, int P, int64_t N, int64_t h
   taco_status st = check_shape(N, h, block);
   if (st != TACO_OK) return st;
   if (P < 1 || P > TACO_MAX_SHARDS) return TACO_ERR_ARG;
-  if (variant != TACO_VARIANT_DUAL && variant != TACO_VARIANT_ABSMAX) return TACO_ERR_ARG;
+  if (!valid_variant(variant)) return TACO_ERR_ARG;
   if (!(target_energy > 0.0f) || !std::isfinite(target_energy)) return TACO_ERR_ARG;
   const double sqrt_nE = std::sqrt(static_cast<double>(block) * target_energy);
   if (!(sqrt_nE < 3.0e38)) return TACO_ERR_ARG;
@@ -295,6 +304,7 @@ taco_status taco_compress_shards(const void* x_bf16, int P, int64_t N, int64_t h
   a.target_energy = target_energy;
   a.sqrt_nE = static_cast<float>(sqrt_nE);
   a.inv_sqrt_n = static_cast<float>(1.0 / std::sqrt(static_cast<double>(block)));
+  a.s_static = static_scale(block, target_energy);
 
   const DeviceInfo* info = nullptr;
   if (device_info(&info) != cudaSuccess) return TACO_ERR_CUDA;

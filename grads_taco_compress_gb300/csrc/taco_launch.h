@@ -16,6 +16,7 @@ constexpr int kCompressStages = 3;        // warp tiles (4 KB each) in flight pe
 constexpr int kDecompressThreads = 256;
 constexpr int kDecompressMinBlocks = 2;
 constexpr int kDecompressStages = 4;      // (tile, shard) stages in flight per warp
+constexpr int kVariants = 3;              // DUAL, ABSMAX, STATIC
 
 // Workspace of compress: per shard one arrival counter (16 bytes) followed by
 // one (max s, count) pair per CTA of the shard's grid row.
@@ -36,6 +37,7 @@ struct CompressArgs {
   float target_energy;
   float sqrt_nE;            // fp32(sqrt(block * E*))
   float inv_sqrt_n;         // fp32(1 / sqrt(block))
+  float s_static;           // fp32(sqrt(block * E*) / 448), STATIC variant
 };
 
 struct DecompressArgs {
@@ -54,6 +56,7 @@ struct DecompressArgs {
   float target_energy;
   float sqrt_E;             // fp32(sqrt(E*))
   float sqrt_n;             // fp32(sqrt(block))
+  float s_static;           // fp32(sqrt(block * E*) / 448), STATIC variant
 };
 
 int compress_tile_blocks(int block);

@@ -51,8 +51,13 @@ typedef enum taco_status {
 
 /* Dual-scale variants. DUAL is the operator above. ABSMAX replaces the
  * overflow guard by s = max|y| / 448 (1 for an all-zero block); alpha then
- * cancels from the codes. It is kept for error studies. */
-enum { TACO_VARIANT_DUAL = 0, TACO_VARIANT_ABSMAX = 1 };
+ * cancels from the codes. STATIC gives every block of the tensor the same
+ * data-independent s = fp32(sqrt(block * E*) / 448): after the energy
+ * rescale the rotated block has squared norm block * E*, so no |y| exceeds
+ * sqrt(block * E*) and no code saturates (a per-tensor scale in the sense of
+ * the euno.news rewrite, Methodology). ABSMAX and STATIC are kept for error
+ * studies. */
+enum { TACO_VARIANT_DUAL = 0, TACO_VARIANT_ABSMAX = 1, TACO_VARIANT_STATIC = 2 };
 
 #define TACO_MAX_SHARDS 16
 #define TACO_Q_MAX 448.0f
@@ -103,7 +108,7 @@ size_t taco_workspace_bytes(int P);
  *   target_energy  E* > 0, the per-element energy of every rescaled block
  *                  (TACO pt summary §2.B.1: "normalise the energy to a
  *                  target level"); 4096 puts the rotated RMS at 64 code units
- *   variant        TACO_VARIANT_DUAL or TACO_VARIANT_ABSMAX
+ *   variant        TACO_VARIANT_DUAL, TACO_VARIANT_ABSMAX or TACO_VARIANT_STATIC
  * N == 0 is valid: no code is written and the header reports s_max = 0. */
 taco_status taco_compress(const void* x_bf16, int64_t N, int64_t h, int block,
                           float target_energy, int variant, void* shard_out,

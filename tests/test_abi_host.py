@@ -73,7 +73,7 @@ def _compress(lib, x=A, P=1, N=4, h=256, block=128, E=4096.0, variant=0, bundle=
     (dict(block=100), BLOCK), (dict(block=32), BLOCK), (dict(block=512), BLOCK),
     (dict(h=130, block=64), SHAPE), (dict(N=-1), SHAPE), (dict(h=0), SHAPE),
     (dict(N=1 << 34, h=1 << 10), SHAPE),
-    (dict(P=0), ARG), (dict(P=17), ARG), (dict(variant=2), ARG), (dict(variant=-1), ARG),
+    (dict(P=0), ARG), (dict(P=17), ARG), (dict(variant=3), ARG), (dict(variant=-1), ARG),
     (dict(E=0.0), ARG), (dict(E=-1.0), ARG), (dict(E=float("nan")), ARG),
     (dict(E=float("inf")), ARG),
     (dict(headers=None), NULL), (dict(ws=None), WS), (dict(wsb=100), WS),

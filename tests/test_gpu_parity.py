@@ -119,7 +119,7 @@ def test_compress_small(name, rows):
 
 
 @pytest.mark.parametrize("block", [64, 128, 256])
-@pytest.mark.parametrize("variant", [tb.VARIANT_DUAL, tb.VARIANT_ABSMAX])
+@pytest.mark.parametrize("variant", [tb.VARIANT_DUAL, tb.VARIANT_ABSMAX, tb.VARIANT_STATIC])
 def test_compress_variants_and_targets(block, variant):
     rng = np.random.default_rng(block + 10 * variant)
     v = rng.laplace(0, 0.02, size=(2, 41, 3 * block))

@@ -58,7 +58,7 @@ def test_recompress_small(name, rows):
 
 
 @pytest.mark.parametrize("block", [64, 128, 256])
-@pytest.mark.parametrize("variant", [tb.VARIANT_DUAL, tb.VARIANT_ABSMAX])
+@pytest.mark.parametrize("variant", [tb.VARIANT_DUAL, tb.VARIANT_ABSMAX, tb.VARIANT_STATIC])
 def test_recompress_random_bundles(block, variant):
     codes, alpha, s = W.make_random_bundle(21, 3 * block, block, 5, seed=block + variant)
     for target in (E_STAR, 2.0):
