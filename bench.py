@@ -329,6 +329,20 @@ def run_taco(args, w) -> None:
 
     t_r = region(lambda i: recompress(i % R, (i + 1) % R))
 
+    # the same compress with the 64-point Hadamard products on the tensor
+    # cores (measured alternative; same outputs within the parity bar)
+    mma_bundles = [torch.empty((P, sb), dtype=torch.uint8, device=dev) for _ in range(R)]
+
+    def compress_mma(k):
+        st = lib.taco_compress_shards_mma(xp[k], P, N, h, n, E, 0, mma_bundles[k].data_ptr(), hp[k],
+                                          ws.data_ptr(), wsb, sptr)
+        if st:
+            raise taco.TacoError(st, "taco_compress_shards_mma")
+
+    for k in range(3):
+        compress_mma(k % R)
+    t_m = region(lambda i: compress_mma(i % R))
+
     # The whole compressed two-shot AllReduce among P logical ranks (the P
     # input tensors of the step), captured in a CUDA graph and replayed.
     from grads_taco_compress_gb300.allreduce import EmulatedTwoShotAllReduce
@@ -388,6 +402,11 @@ def run_taco(args, w) -> None:
                                   "hbm_gbs": round(r_bytes / t_r / 1e9, 1),
                                   "bf16_in_gbs": round(in_bytes / t_r / 1e9, 1),
                                   "frac": round(r_bytes / t_r / 1e9 / hbm, 4)},
+            "compress_mma": {"us": round(t_m * 1e6, 3), "alg_bytes": c_bytes,
+                             "hbm_gbs": round(c_bytes / t_m / 1e9, 1),
+                             "bf16_in_gbs": round(in_bytes / t_m / 1e9, 1),
+                             "frac": round(c_bytes / t_m / 1e9 / hbm, 4),
+                             "note": "tcgen05 tensor-core Hadamard, not in the timed step"},
         }
         kern["emulated_two_shot_allreduce"] = {
             "us": round(t_ar * 1e6, 3), "ranks": P, "tensor": [N, h], "launches": ar.launches(),

@@ -37,7 +37,7 @@ assert HEADER_DTYPE.itemsize == HEADER_BYTES
 EXPORTED_SYMBOLS = (
     "taco_shard_bytes", "taco_shard_scales_offset",
     "taco_workspace_bytes", "taco_compress", "taco_compress_shards",
-    "taco_compress_shards_noalloc",
+    "taco_compress_shards_noalloc", "taco_compress_shards_mma",
     "taco_decompress_reduce", "taco_decompress_reduce_ptrs",
     "taco_reduce_recompress", "taco_reduce_recompress_ptrs",
     "taco_decompress_shards", "taco_decompress_shards_ptrs",
@@ -74,6 +74,7 @@ def _lib() -> ctypes.CDLL:
             "taco_compress": (i32, [vp, i64, i64, i32, f32, i32, vp, vp, vp, sz, vp]),
             "taco_compress_shards": (i32, [vp, i32, i64, i64, i32, f32, i32, vp, vp, vp, sz, vp]),
             "taco_compress_shards_noalloc": (i32, [vp, i32, i64, i64, i32, f32, i32, vp, vp, vp]),
+            "taco_compress_shards_mma": (i32, [vp, i32, i64, i64, i32, f32, i32, vp, vp, vp, sz, vp]),
             "taco_decompress_reduce": (i32, [vp, i32, i64, i64, i32, vp, vp]),
             "taco_decompress_reduce_ptrs": (i32, [ctypes.POINTER(vp), i32, i64, i64, i32, vp, vp]),
             "taco_decompress_shards": (i32, [vp, i32, i64, i64, i32, vp, vp]),
@@ -152,14 +153,8 @@ def parse_headers(headers: torch.Tensor) -> np.ndarray:
 
 
 # -------------------------------------------------------------- operator ----
-def taco_compress_shards(x: torch.Tensor, block: int, target_energy: float = DEFAULT_TARGET_ENERGY,
-                         variant: int = VARIANT_DUAL, bundle: torch.Tensor | None = None,
-                         headers: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
-                         stream=None):
-    """Compress bf16 x [P, N, h] (cuda, contiguous) into a bundle of P shards.
-
-    Returns (bundle u8 [P, shard_bytes], headers u8 [P, 40]).
-    """
+def _compress_shards(entry: str, x: torch.Tensor, block: int, target_energy, variant, bundle,
+                     headers, workspace, stream):
     if x.dtype != torch.bfloat16 or not x.is_cuda or x.dim() != 3 or not x.is_contiguous():
         raise ValueError("x must be a contiguous bf16 CUDA tensor [P, N, h]")
     P, N, h = x.shape
@@ -170,11 +165,32 @@ def taco_compress_shards(x: torch.Tensor, block: int, target_energy: float = DEF
         headers = torch.empty((P, HEADER_BYTES), dtype=torch.uint8, device=x.device)
     if workspace is None:
         workspace = new_workspace(P, x.device)
-    st = _lib().taco_compress_shards(_ptr(x), P, N, h, block, float(target_energy), variant,
-                                     _ptr(bundle), _ptr(headers), _ptr(workspace),
-                                     workspace.numel(), _stream_ptr(stream))
-    _check(st, "taco_compress_shards")
+    st = getattr(_lib(), entry)(_ptr(x), P, N, h, block, float(target_energy), variant,
+                                _ptr(bundle), _ptr(headers), _ptr(workspace),
+                                workspace.numel(), _stream_ptr(stream))
+    _check(st, entry)
     return bundle, headers
+
+
+def taco_compress_shards(x: torch.Tensor, block: int, target_energy: float = DEFAULT_TARGET_ENERGY,
+                         variant: int = VARIANT_DUAL, bundle: torch.Tensor | None = None,
+                         headers: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                         stream=None):
+    """Compress bf16 x [P, N, h] (cuda, contiguous) into a bundle of P shards.
+
+    Returns (bundle u8 [P, shard_bytes], headers u8 [P, 40]).
+    """
+    return _compress_shards("taco_compress_shards", x, block, target_energy, variant, bundle,
+                            headers, workspace, stream)
+
+
+def taco_compress_shards_mma(x: torch.Tensor, block: int, target_energy: float = DEFAULT_TARGET_ENERGY,
+                             variant: int = VARIANT_DUAL, bundle: torch.Tensor | None = None,
+                             headers: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                             stream=None):
+    """taco_compress_shards with the 64-point Hadamard products on the tensor cores."""
+    return _compress_shards("taco_compress_shards_mma", x, block, target_energy, variant, bundle,
+                            headers, workspace, stream)
 
 
 def taco_compress_shards_noalloc(x: torch.Tensor, block: int,

@@ -1,0 +1,596 @@
+// TACO fused compress on the 5th-generation tensor cores (tcgen05 + TMEM),
+// an alternative to the CUDA-core FWHT of compress.cu with the same outputs.
+//
+// The operator is the one of compress.cu ("TACO: Efficient Communication
+// Compression of Intermediate Tensors ...", gist.science pt summary, §2.B.1
+// ASH, §2.B.2 DS, §2.B.3 one fused kernel). What changes is where the
+// Hadamard products run. Sylvester's construction gives
+//   H_n = H_{n/64} (x) H_64,   element e = 64 * chunk + i,
+// so a block of n = 64 * NC elements is rotated in two steps:
+//   1. every 64-element chunk u_c = H_64 x_c is one row of a dense product
+//      D[128 x 64] = A[128 x 64] * H_64^T on the tensor cores: A holds one
+//      chunk of 128 consecutive blocks (bf16, exact), H_64 is +-1 (exact in
+//      bf16), D accumulates in fp32 in tensor memory;
+//   2. t = (H_NC (x) I_64) u, NC - 1 butterfly levels across the chunks,
+//      done in registers by the thread that owns the block.
+// The energy comes from the rotated block (Parseval: sum t^2 = n sum x^2),
+// so no thread reads x itself: alpha = n sqrt(E*) / sqrt(sum t^2).
+//
+// CTA = 10 warps, one CTA per SM (its shared memory does not fit twice):
+//   warp 0     TMA producer: 3-D tensor loads of [128 blocks x 64 elements]
+//              bf16 atoms (16 KB, 128-byte swizzle) into a ring of stages;
+//   warp 1     owns the tensor memory (2 accumulators x n columns) and one
+//              lane issues the MMAs (4 x K=16 per atom), committing each atom
+//              to its stage's "empty" barrier and each tile to "full";
+//   warps 2-9  two epilogue groups of 4 warps; group g takes the CTA's tiles
+//              k with k % 2 == g from accumulator g. Thread (warp w, lane l)
+//              owns block row 32 (w % 4) + l of the tile (the TMEM lanes a
+//              warp may read). It loads its row with tcgen05.ld, finishes the
+//              rotation, computes alpha, s and the codes, writes the codes
+//              into a 64-byte-swizzled staging buffer that one thread stores
+//              with 3-D TMA tensor stores, and stores its (alpha, s) pair.
+// Every wait is bounded in time; a wait that gives up sets a CTA-wide abort
+// flag that ends every role's loop, records kFaultCompressMmaWait and lets
+// the CTA drain its copies and MMAs before it frees the tensor memory.
+
+#include <cmath>
+#include <mutex>
+
+#include <cuda.h>
+
+#include "taco_device.cuh"
+#include "taco_launch.h"
+
+namespace taco {
+
+namespace {
+
+__device__ unsigned int g_compress_mma_fault;
+
+constexpr int kThreads = kCompressMmaThreads;
+constexpr int kStages = 6;                    // 16 KB input atoms in flight per CTA
+constexpr int kRows = 128;                    // blocks per tile (the MMA's M)
+constexpr uint32_t kAtomBytes = kRows * 64 * 2;       // 16 KB of bf16
+constexpr uint32_t kCodeAtomBytes = kRows * 64;       // 8 KB of codes
+constexpr uint32_t kHBytes = 64 * 64 * 2;             // H_64 in bf16
+
+// Shared memory map (offsets from a 1024-byte aligned base).
+template <int NB>
+struct Smem {
+  static constexpr int NC = NB / 64;
+  static constexpr uint32_t stages = 0;
+  static constexpr uint32_t hmat = stages + kStages * kAtomBytes;
+  static constexpr uint32_t codes = hmat + kHBytes;                 // [group][chunk] atoms
+  static constexpr uint32_t bars = codes + 2 * NC * kCodeAtomBytes;
+  // barriers: full[kStages], empty[kStages], tfull[2], tempty[2], mma_done
+  static constexpr uint32_t full = bars;
+  static constexpr uint32_t empty = full + 8 * kStages;
+  static constexpr uint32_t tfull = empty + 8 * kStages;
+  static constexpr uint32_t tempty = tfull + 16;
+  static constexpr uint32_t mma_done = tempty + 16;
+  static constexpr uint32_t tmem_slot = mma_done + 8;
+  static constexpr uint32_t abort_flag = tmem_slot + 4;
+  static constexpr uint32_t end = abort_flag + 4;
+  static constexpr uint32_t bytes = end + 1024;                     // + alignment slack
+};
+
+// ------------------------------------------------------------- tcgen05 ----
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+               :: "r"(slot), "r"(ncols) : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand stored in the
+// 128-byte swizzle layout: 8-row groups of 128-byte rows, 1024 bytes apart.
+//   bits  0-13 start address >> 4      bits 16-29 leading offset >> 4 (unused)
+//   bits 32-45 stride offset >> 4      bits 46-48 0b001 (descriptor version)
+//   bits 49-51 base offset (0: atoms 1024-byte aligned)
+//   bits 61-63 swizzle mode, 2 = 128-byte swizzle
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (uint64_t{1} << 16) |
+         (uint64_t{1024 >> 4} << 32) | (uint64_t{1} << 46) | (uint64_t{2} << 61);
+}
+
+// Instruction descriptor of kind::f16: D f32 (bits 4-5 = 1), A and B bf16
+// (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits
+// 17-22, M >> 4 at bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((64u >> 3) << 17) |
+                            ((static_cast<uint32_t>(kRows) >> 4) << 24);
+
+// D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
+      :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate) : "memory");
+}
+// The barrier at `bar` completes one arrival once every MMA this thread has
+// issued so far has completed.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+               :: "r"(bar) : "memory");
+}
+
+// 16 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+// Keeps the compiler from using registers of a tcgen05.ld before the wait.
+__device__ __forceinline__ void reg_fence16(float* v) {
+  asm volatile(""
+               : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]),
+                 "+f"(v[6]), "+f"(v[7]), "+f"(v[8]), "+f"(v[9]), "+f"(v[10]), "+f"(v[11]),
+                 "+f"(v[12]), "+f"(v[13]), "+f"(v[14]), "+f"(v[15]));
+}
+
+// ------------------------------------------------------------ TMA tiles ----
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar),
+         "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1,
+                                             int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];"
+               :: "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ------------------------------------------------------ waits and votes ----
+// Wait for phase `parity` of `bar`. Gives up when the CTA's abort flag is set
+// or after kWaitLimitNs; the timed-out waiter sets the flag and the fault bit.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
+                                              volatile uint32_t* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1u;
+      atomicOr(&g_compress_mma_fault, kFaultCompressMmaWait);
+      return false;
+    }
+  }
+}
+
+// Barrier over the 128 threads of epilogue group `id`; true in every thread
+// if `pred` held in any of them.
+__device__ __forceinline__ bool group_any(int id, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, 128, p;\n"
+      " selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r) : "r"(static_cast<uint32_t>(pred)), "r"(id) : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void group_sync(int id) {
+  asm volatile("bar.sync %0, 128;" :: "r"(id) : "memory");
+}
+
+// ------------------------------------------------------------- epilogue ----
+// Values of one slice of the thread's block: u[c][i] = column (slice * SL + i)
+// of chunk c. After the butterflies, u[c][i] is element 64 c + slice * SL + i
+// of t = H_n x.
+template <int NC, int SL>
+__device__ __forceinline__ void load_slice(uint32_t tacc, int slice, float (&u)[NC][SL]) {
+#pragma unroll
+  for (int c = 0; c < NC; ++c)
+#pragma unroll
+    for (int q = 0; q < SL / 16; ++q)
+      tmem_ld16(tacc + c * 64 + slice * SL + q * 16, &u[c][q * 16]);
+  tmem_wait_ld();
+#pragma unroll
+  for (int c = 0; c < NC; ++c)
+#pragma unroll
+    for (int q = 0; q < SL / 16; ++q) reg_fence16(&u[c][q * 16]);
+}
+
+// t = (H_NC (x) I) u over the chunk index, in place.
+template <int NC, int SL>
+__device__ __forceinline__ void chunk_butterflies(float (&u)[NC][SL]) {
+#pragma unroll
+  for (int m = 1; m < NC; m <<= 1)
+#pragma unroll
+    for (int c = 0; c < NC; ++c)
+      if ((c & m) == 0) {
+#pragma unroll
+        for (int i = 0; i < SL; i += 2) {
+          const f2 a{u[c][i], u[c][i + 1]}, b{u[c + m][i], u[c + m][i + 1]};
+          const f2 s = add2(a, b), d = sub2(a, b);
+          u[c][i] = s.x;
+          u[c][i + 1] = s.y;
+          u[c + m][i] = d.x;
+          u[c + m][i + 1] = d.y;
+        }
+      }
+}
+
+// Running sum of squares (four packed accumulators) and max / min.
+template <int NC, int SL>
+__device__ __forceinline__ void slice_stats(const float (&u)[NC][SL], f2 (&ea)[4], float (&hi)[4],
+                                            float (&lo)[4]) {
+#pragma unroll
+  for (int c = 0; c < NC; ++c) {
+#pragma unroll
+    for (int i = 0; i < SL; i += 2) {
+      const f2 v{u[c][i], u[c][i + 1]};
+      ea[(i >> 1) & 3] = fma2(v, v, ea[(i >> 1) & 3]);
+    }
+#pragma unroll
+    for (int i = 0; i < SL; i += 4) {
+      const int j = (i >> 2) & 3;
+      hi[j] = max3(hi[j], max3(u[c][i], u[c][i + 1], u[c][i + 2]), u[c][i + 3]);
+      lo[j] = min3(lo[j], min3(u[c][i], u[c][i + 1], u[c][i + 2]), u[c][i + 3]);
+    }
+  }
+}
+
+// Codes of one slice into the group's staging atoms: chunk c of block row
+// `row` is 64 bytes at row * 64 of atom c, its 16-byte pieces permuted by the
+// 64-byte swizzle (piece ^= (row >> 1) & 3) that the tensor store undoes.
+template <int NC, int SL>
+__device__ __forceinline__ void slice_codes(const float (&u)[NC][SL], int slice, float g,
+                                            uint32_t stage_codes, int row) {
+  const f2 g2{g, g};
+  const uint32_t rbase = stage_codes + row * 64;
+  const int sw = (row >> 1) & 3;
+#pragma unroll
+  for (int c = 0; c < NC; ++c)
+#pragma unroll
+    for (int q = 0; q < SL / 16; ++q) {
+      uint32_t w[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int i = q * 16 + 4 * k;
+        const f2 y0 = mul2(f2{u[c][i], u[c][i + 1]}, g2);
+        const f2 y1 = mul2(f2{u[c][i + 2], u[c][i + 3]}, g2);
+        w[k] = e4m3x4_from_f32(y0.x, y0.y, y1.x, y1.y);
+      }
+      const int piece = (slice * SL) / 16 + q;
+      sts128(rbase + c * kCodeAtomBytes + 16 * (piece ^ sw), make_uint4(w[0], w[1], w[2], w[3]));
+    }
+}
+
+template <int NB, int VARIANT>
+__global__ void __launch_bounds__(kThreads, 1)
+compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
+                    const __grid_constant__ CUtensorMap map_codes, CompressArgs a) {
+  constexpr int NC = NB / 64;            // 64-element chunks per block
+  constexpr int SL = 64 / NC;            // columns per slice (64 registers per slice)
+  constexpr uint32_t TMEM_COLS = 2 * NB; // two accumulators
+  using S = Smem<NB>;
+
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  volatile uint32_t* abort_flag =
+      reinterpret_cast<volatile uint32_t*>(smem_raw + (base - smem_u32(smem_raw)) + S::abort_flag);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int shard = blockIdx.y;
+  const int64_t nblocks = a.nblocks;
+  const int64_t ntiles = (nblocks + kRows - 1) / kRows;
+  const int64_t G = gridDim.x;
+  const int count = static_cast<int>(ntiles > blockIdx.x ? (ntiles - blockIdx.x + G - 1) / G : 0);
+
+  // ---- set-up: barriers, H_64, tensor memory ----
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(base + S::full + 8 * s, 1);
+      mbar_init(base + S::empty + 8 * s, 1);
+    }
+    for (int g = 0; g < 2; ++g) {
+      mbar_init(base + S::tfull + 8 * g, 1);
+      mbar_init(base + S::tempty + 8 * g, 4);   // one arrival per epilogue warp
+    }
+    mbar_init(base + S::mma_done, 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  // H_64 (entries (-1)^popcount(r & k)) as B: 64 rows of 128 bytes, K-major,
+  // 16-byte pieces swizzled by (row & 7).
+  for (int p = threadIdx.x; p < 64 * 8; p += kThreads) {
+    const int r = p >> 3, piece = p & 7;
+    uint32_t w[4];
+#pragma unroll
+    for (int k2 = 0; k2 < 4; ++k2) {
+      const int k0 = piece * 8 + 2 * k2;
+      const uint32_t lo = (__popc(r & k0) & 1) ? 0xBF80u : 0x3F80u;
+      const uint32_t hi = (__popc(r & (k0 + 1)) & 1) ? 0xBF80u : 0x3F80u;
+      w[k2] = lo | (hi << 16);
+    }
+    sts128(base + S::hmat + r * 128 + 16 * (piece ^ (r & 7)), make_uint4(w[0], w[1], w[2], w[3]));
+  }
+  fence_proxy_async_smem();   // H is read by the tensor cores (async proxy)
+  if (warp == 1) tmem_alloc(base + S::tmem_slot, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = lds_u32(base + S::tmem_slot);
+
+  grid_launch_dependents();
+  grid_dependency_wait();   // no global access before the preceding grid is done
+
+  float part_smax = 0.0f;
+  uint32_t part_cnt = 0;
+
+  if (warp == 0) {
+    // ---------------------------------------------------- TMA producer ----
+    if (lane == 0) {
+      prefetch_map(&map_x);
+      const uint64_t policy = l2_evict_first_policy();
+      uint32_t i = 0;
+      bool ok = true;
+      for (int k = 0; k < count && ok; ++k) {
+        const int row0 = static_cast<int>((blockIdx.x + k * G) * kRows);
+        for (int c = 0; c < NC; ++c, ++i) {
+          const uint32_t s = i % kStages, ph = (i / kStages) & 1u;
+          if (!wait_or_abort(base + S::empty + 8 * s, ph ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(base + S::full + 8 * s, kAtomBytes);
+          tma_load_3d(base + S::stages + s * kAtomBytes, &map_x, c * 64, row0, shard,
+                      base + S::full + 8 * s, policy);
+        }
+      }
+      if (!ok) {
+        // copies still in flight land in their stages before the CTA exits
+        const uint32_t first = i > static_cast<uint32_t>(kStages) ? i - kStages : 0u;
+        for (uint32_t j = first; j < i; ++j)
+          mbar_wait(base + S::full + 8 * (j % kStages), (j / kStages) & 1u);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------ MMA issuer ----
+    if (lane == 0) {
+      uint32_t i = 0;
+      bool ok = true;
+      for (int k = 0; k < count && ok; ++k) {
+        const int g = k & 1;
+        const uint32_t use = static_cast<uint32_t>(k >> 1);
+        if (!wait_or_abort(base + S::tempty + 8 * g, (use & 1u) ^ 1u, abort_flag)) break;
+        tc_fence_after();
+        for (int c = 0; c < NC; ++c, ++i) {
+          const uint32_t s = i % kStages, ph = (i / kStages) & 1u;
+          if (!wait_or_abort(base + S::full + 8 * s, ph, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem + g * NB + c * 64;
+          const uint32_t atile = base + S::stages + s * kAtomBytes;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16(d, sw128_desc(atile + 32 * kk), sw128_desc(base + S::hmat + 32 * kk),
+                     kk > 0 ? 1u : 0u);
+          mma_commit(base + S::empty + 8 * s);   // the stage is free once these MMAs are done
+        }
+        if (ok) mma_commit(base + S::tfull + 8 * g);
+      }
+      // every MMA of this CTA has completed before the tensor memory is freed
+      mma_commit(base + S::mma_done);
+      mbar_wait(base + S::mma_done, 0);
+    }
+    __syncwarp();
+  } else {
+    // -------------------------------------------------------- epilogue ----
+    const int g = (warp - 2) >> 2;               // group: accumulator and tiles k % 2 == g
+    const int quad = warp & 3;                   // TMEM lanes 32 quad .. 32 quad + 31
+    const int row = quad * 32 + lane;            // block row of the tile
+    const bool leader = (warp == 2 + 4 * g) && lane == 0;
+    const uint32_t tacc = tmem + (static_cast<uint32_t>(quad * 32) << 16) + g * NB;
+    const uint32_t staging = base + S::codes + g * NC * kCodeAtomBytes;
+    uint8_t* shard_base = a.bundle + static_cast<size_t>(shard) * a.shard_bytes;
+    float2* __restrict__ scales_out = reinterpret_cast<float2*>(shard_base + a.scales_off);
+    if (leader) prefetch_map(&map_codes);
+
+    for (int k = g; k < count; k += 2) {
+      const uint32_t use = static_cast<uint32_t>(k >> 1);
+      const bool got = wait_or_abort(base + S::tfull + 8 * g, use & 1u, abort_flag);
+      if (leader) bulk_wait_read<0>();           // the group's last store has read the staging
+      if (group_any(1 + g, !got || *abort_flag != 0u)) break;
+      tc_fence_after();
+
+      const int64_t tile = blockIdx.x + static_cast<int64_t>(k) * G;
+      const int64_t b = tile * kRows + row;
+      const bool valid = b < nblocks;
+
+      // pass 1: sum of squares and extremes of t = H_n x
+      f2 ea[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+      float hi[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      float lo[4] = {INFINITY, INFINITY, INFINITY, INFINITY};
+      float u[NC][SL];
+#pragma unroll 1
+      for (int sl = 0; sl < NC; ++sl) {
+        load_slice<NC, SL>(tacc, sl, u);
+        chunk_butterflies<NC, SL>(u);
+        slice_stats<NC, SL>(u, ea, hi, lo);
+      }
+      const f2 e01 = add2(ea[0], ea[1]), e23 = add2(ea[2], ea[3]);
+      const float e = (e01.x + e01.y) + (e23.x + e23.y);   // = n * sum x^2
+
+      // alpha = sqrt(E* / E), E = e / n^2: n sqrt(E*) / sqrt(e), one Newton step
+      float r = rsqrtf(e);
+      r = fmaf(fmaf(-0.5f * e * r, r, 0.5f), r, r);
+      const float alpha = (e > 0.f) ? a.n_sqrtE * r : 1.0f;
+      const float cscale = alpha * a.inv_sqrt_n;             // y = cscale * t
+      const float thi = max3(hi[0], hi[1], fmaxf(hi[2], hi[3]));
+      const float tlo = min3(lo[0], lo[1], fminf(lo[2], lo[3]));
+      const float amax = cscale * fmaxf(thi, -tlo);
+      const float sc = (VARIANT == 0)   ? fmaxf(1.0f, amax * (1.0f / 448.0f))
+                       : (VARIANT == 1) ? (amax > 0.f ? amax * (1.0f / 448.0f) : 1.0f)
+                                        : a.s_static;
+      const float gsc = __fdividef(cscale, sc);              // code value = gsc * t
+
+      // pass 2: codes (one slice: the values are still in registers)
+      if constexpr (NC == 1) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(base + S::tempty + 8 * g);
+        slice_codes<NC, SL>(u, 0, gsc, staging, row);
+      } else {
+#pragma unroll 1
+        for (int sl = 0; sl < NC; ++sl) {
+          load_slice<NC, SL>(tacc, sl, u);
+          chunk_butterflies<NC, SL>(u);
+          slice_codes<NC, SL>(u, sl, gsc, staging, row);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(base + S::tempty + 8 * g);
+      }
+      fence_proxy_async_smem();   // codes visible to the tensor store
+      group_sync(1 + g);
+      if (leader) {
+#pragma unroll
+        for (int c = 0; c < NC; ++c)
+          tma_store_3d(&map_codes, staging + c * kCodeAtomBytes, c * 64,
+                       static_cast<int>(tile * kRows), shard);
+        bulk_commit();
+      }
+      if (valid) {
+        scales_out[b] = make_float2(alpha, sc);
+        part_smax = fmaxf(part_smax, sc);
+        part_cnt += (sc > 1.0f) ? 1u : 0u;
+      }
+    }
+    if (leader) bulk_wait_all();   // the codes have been written before the CTA exits
+  }
+
+  // ---- tear-down: free the tensor memory, then the per-tensor header ----
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+  finish_header<kThreads>(part_smax, part_cnt, a.workspace + shard * kWorkspaceShardStride,
+                          a.headers + shard, a.N, a.h, NB, VARIANT, a.target_energy);
+}
+
+template <int NB>
+void (*mma_fn(int variant))(CUtensorMap, CUtensorMap, CompressArgs) {
+  return variant == 0   ? compress_mma_kernel<NB, 0>
+         : variant == 1 ? compress_mma_kernel<NB, 1>
+                        : compress_mma_kernel<NB, 2>;
+}
+
+void (*mma_kernel(int block, int variant))(CUtensorMap, CUtensorMap, CompressArgs) {
+  return block == 64 ? mma_fn<64>(variant) : block == 128 ? mma_fn<128>(variant) : mma_fn<256>(variant);
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against the driver library).
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+std::once_flag g_encode_once;
+EncodeTiled g_encode = nullptr;
+
+EncodeTiled encoder() {
+  std::call_once(g_encode_once, []() {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiled>(fn);
+  });
+  return g_encode;
+}
+
+}  // namespace
+
+size_t compress_mma_smem_bytes(int block) {
+  return block == 64 ? Smem<64>::bytes : block == 128 ? Smem<128>::bytes : Smem<256>::bytes;
+}
+
+const void* compress_mma_kernel_ptr(int block, int variant) {
+  return reinterpret_cast<const void*>(mma_kernel(block, variant));
+}
+
+cudaError_t launch_compress_mma(const CompressArgs& a, int block, int variant, int grid_x, int P,
+                                cudaStream_t stream) {
+  EncodeTiled encode = encoder();
+  if (!encode) return cudaErrorNotSupported;
+  // x viewed as [P][nblocks][block] bf16; one box = one chunk of 128 blocks.
+  CUtensorMap map_x, map_codes;
+  const cuuint64_t xdim[3] = {static_cast<cuuint64_t>(block), static_cast<cuuint64_t>(a.nblocks),
+                              static_cast<cuuint64_t>(P)};
+  const cuuint64_t xstride[2] = {static_cast<cuuint64_t>(block) * 2,
+                                 static_cast<cuuint64_t>(a.shard_elems) * 2};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kRows), 1};
+  const cuuint32_t unit[3] = {1, 1, 1};
+  if (encode(&map_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(a.x), xdim, xstride,
+             box, unit, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  // codes viewed as [P][nblocks][block] bytes with the bundle's shard stride.
+  const cuuint64_t cdim[3] = {static_cast<cuuint64_t>(block), static_cast<cuuint64_t>(a.nblocks),
+                              static_cast<cuuint64_t>(P)};
+  const cuuint64_t cstride[2] = {static_cast<cuuint64_t>(block),
+                                 static_cast<cuuint64_t>(a.shard_bytes)};
+  if (encode(&map_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, a.bundle, cdim, cstride, box, unit,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid_x, P);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = compress_mma_smem_bytes(block);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, mma_kernel(block, variant), map_x, map_codes, a);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t compress_mma_fault(unsigned int* bits, bool clear) {
+  cudaError_t e = cudaMemcpyFromSymbol(bits, g_compress_mma_fault, sizeof(unsigned int));
+  if (e == cudaSuccess && clear) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_compress_mma_fault, &zero, sizeof(unsigned int));
+  }
+  return e;
+}
+
+}  // namespace taco

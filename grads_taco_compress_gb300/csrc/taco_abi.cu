@@ -49,6 +49,7 @@ struct DeviceInfo {
   int occ_decompress[3] = {};
   int occ_recompress[3][kVariants] = {};
   int occ_gather[3] = {};
+  int occ_mma[3][kVariants] = {};
 };
 
 std::once_flag g_once[kMaxDevices];
@@ -87,6 +88,14 @@ cudaError_t device_info(const DeviceInfo** out) {
         if (err == cudaSuccess)
           err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ_gather[b], k,
                                                               kDecompressThreads, dsmem);
+      }
+      for (int v = 0; v < kVariants && err == cudaSuccess; ++v) {
+        const void* k = compress_mma_kernel_ptr(blocks[b], v);
+        const int msmem = static_cast<int>(compress_mma_smem_bytes(blocks[b]));
+        err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, msmem);
+        if (err == cudaSuccess)
+          err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ_mma[b][v], k,
+                                                              kCompressMmaThreads, msmem);
       }
       for (int v = 0; v < kVariants && err == cudaSuccess; ++v) {
         const void* k = recompress_kernel_ptr(blocks[b], v);
@@ -246,6 +255,47 @@ taco_status reduce_recompress_common(const uint8_t* const* shards, int P, int64_
   return TACO_OK;
 }
 
+// Argument checks and kernel arguments shared by both compress entries.
+taco_status compress_args(const void* x_bf16, int P, int64_t N, int64_t h, int block,
+                          float target_energy, int variant, void* bundle_out,
+                          taco_header* headers_out, void* workspace, size_t workspace_bytes,
+                          CompressArgs* out) {
+  taco_status st = check_shape(N, h, block);
+  if (st != TACO_OK) return st;
+  if (P < 1 || P > TACO_MAX_SHARDS) return TACO_ERR_ARG;
+  if (!valid_variant(variant)) return TACO_ERR_ARG;
+  if (!(target_energy > 0.0f) || !std::isfinite(target_energy)) return TACO_ERR_ARG;
+  const double sqrt_nE = std::sqrt(static_cast<double>(block) * target_energy);
+  if (!(sqrt_nE < 3.0e38)) return TACO_ERR_ARG;
+  if (!headers_out) return TACO_ERR_NULL;
+  if (!workspace || workspace_bytes < taco_workspace_bytes(P)) return TACO_ERR_WORKSPACE;
+  if (!aligned(headers_out, 8) || !aligned(workspace, 16)) return TACO_ERR_ALIGN;
+  const Layout l = shard_layout(N, h, block);
+  const size_t in_bytes = static_cast<size_t>(P) * N * h * 2;
+  if (N > 0) {
+    if (!x_bf16 || !bundle_out) return TACO_ERR_NULL;
+    if (!aligned(x_bf16, 16) || !aligned(bundle_out, 16)) return TACO_ERR_ALIGN;
+    if (overlap(x_bf16, in_bytes, bundle_out, P * l.bytes)) return TACO_ERR_ARG;
+  }
+
+  CompressArgs& a = *out;
+  a.x = static_cast<const uint16_t*>(x_bf16);
+  a.shard_elems = N * h;
+  a.nblocks = N * h / block;
+  a.bundle = static_cast<uint8_t*>(bundle_out);
+  a.shard_bytes = l.bytes;
+  a.scales_off = l.scales_off;
+  a.headers = headers_out;
+  a.workspace = static_cast<uint8_t*>(workspace);
+  a.N = N;
+  a.h = h;
+  a.target_energy = target_energy;
+  a.sqrt_nE = static_cast<float>(sqrt_nE);
+  a.inv_sqrt_n = static_cast<float>(1.0 / std::sqrt(static_cast<double>(block)));
+  a.s_static = static_scale(block, target_energy);
+  return TACO_OK;
+}
+
 }  // namespace
 }  // namespace taco
 
@@ -268,44 +318,44 @@ size_t taco_workspace_bytes(int P) {
   return static_cast<size_t>(P) * kWorkspaceShardStride;
 }
 
+taco_status taco_compress_shards_mma(const void* x_bf16, int P, int64_t N, int64_t h, int block,
+                                     float target_energy, int variant, void* bundle_out,
+                                     taco_header* headers_out, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
+  CompressArgs a{};
+  taco_status st = compress_args(x_bf16, P, N, h, block, target_energy, variant, bundle_out,
+                                 headers_out, workspace, workspace_bytes, &a);
+  if (st != TACO_OK) return st;
+  if (a.nblocks > kMmaMaxBlocks) return TACO_ERR_SHAPE;
+  const double n_sqrtE = block * std::sqrt(static_cast<double>(target_energy));   // finite
+  if (N == 0)   // nothing to rotate: the headers as the CUDA-core path writes them
+    return taco_compress_shards(x_bf16, P, N, h, block, target_energy, variant, bundle_out,
+                                headers_out, workspace, workspace_bytes, stream);
+  a.n_sqrtE = static_cast<float>(n_sqrtE);
+
+  const DeviceInfo* info = nullptr;
+  if (device_info(&info) != cudaSuccess) return TACO_ERR_CUDA;
+  const int occ = info->occ_mma[block_index(block)][variant];
+  if (occ < 1) return TACO_ERR_CUDA;
+  const int64_t tiles = (a.nblocks + 127) / 128;
+  int64_t gx = static_cast<int64_t>(info->sms) * occ / P;
+  if (gx > tiles) gx = tiles;
+  if (gx > kMaxCtasPerShard) gx = kMaxCtasPerShard;
+  if (gx < 1) gx = 1;
+  if (launch_compress_mma(a, block, variant, static_cast<int>(gx), P,
+                          static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return TACO_ERR_CUDA;
+  return TACO_OK;
+}
+
 taco_status taco_compress_shards(const void* x_bf16, int P, int64_t N, int64_t h, int block,
                                  float target_energy, int variant, void* bundle_out,
                                  taco_header* headers_out, void* workspace,
                                  size_t workspace_bytes, void* stream) {
-  taco_status st = check_shape(N, h, block);
-  if (st != TACO_OK) return st;
-  if (P < 1 || P > TACO_MAX_SHARDS) return TACO_ERR_ARG;
-  if (!valid_variant(variant)) return TACO_ERR_ARG;
-  if (!(target_energy > 0.0f) || !std::isfinite(target_energy)) return TACO_ERR_ARG;
-  const double sqrt_nE = std::sqrt(static_cast<double>(block) * target_energy);
-  if (!(sqrt_nE < 3.0e38)) return TACO_ERR_ARG;
-  if (!headers_out) return TACO_ERR_NULL;
-  if (!workspace || workspace_bytes < taco_workspace_bytes(P)) return TACO_ERR_WORKSPACE;
-  if (!aligned(headers_out, 8) || !aligned(workspace, 16)) return TACO_ERR_ALIGN;
-  const Layout l = shard_layout(N, h, block);
-  const size_t in_bytes = static_cast<size_t>(P) * N * h * 2;
-  if (N > 0) {
-    if (!x_bf16 || !bundle_out) return TACO_ERR_NULL;
-    if (!aligned(x_bf16, 16) || !aligned(bundle_out, 16)) return TACO_ERR_ALIGN;
-    if (overlap(x_bf16, in_bytes, bundle_out, P * l.bytes)) return TACO_ERR_ARG;
-  }
-
   CompressArgs a{};
-  a.x = static_cast<const uint16_t*>(x_bf16);
-  a.shard_elems = N * h;
-  a.nblocks = N * h / block;
-  a.bundle = static_cast<uint8_t*>(bundle_out);
-  a.shard_bytes = l.bytes;
-  a.scales_off = l.scales_off;
-  a.headers = headers_out;
-  a.workspace = static_cast<uint8_t*>(workspace);
-  a.N = N;
-  a.h = h;
-  a.target_energy = target_energy;
-  a.sqrt_nE = static_cast<float>(sqrt_nE);
-  a.inv_sqrt_n = static_cast<float>(1.0 / std::sqrt(static_cast<double>(block)));
-  a.s_static = static_scale(block, target_energy);
-
+  taco_status st = compress_args(x_bf16, P, N, h, block, target_energy, variant, bundle_out,
+                                 headers_out, workspace, workspace_bytes, &a);
+  if (st != TACO_OK) return st;
   const DeviceInfo* info = nullptr;
   if (device_info(&info) != cudaSuccess) return TACO_ERR_CUDA;
   const int tb = compress_tile_blocks(block);
@@ -321,6 +371,7 @@ taco_status taco_compress_shards(const void* x_bf16, int P, int64_t N, int64_t h
     return TACO_ERR_CUDA;
   return TACO_OK;
 }
+
 
 taco_status taco_compress(const void* x_bf16, int64_t N, int64_t h, int block, float target_energy,
                           int variant, void* shard_out, taco_header* header_out, void* workspace,
@@ -430,11 +481,12 @@ taco_status taco_e4m3_decode_f32(const uint8_t* in, float* out, int64_t n, void*
 
 taco_status taco_get_fault(uint32_t* bits, int clear) {
   if (!bits) return TACO_ERR_NULL;
-  unsigned int c = 0, d = 0, t = 0;
+  unsigned int c = 0, d = 0, t = 0, m = 0;
   if (compress_fault(&c, clear != 0) != cudaSuccess) return TACO_ERR_CUDA;
+  if (compress_mma_fault(&m, clear != 0) != cudaSuccess) return TACO_ERR_CUDA;
   if (decompress_fault(&d, clear != 0) != cudaSuccess) return TACO_ERR_CUDA;
   if (selftest_fault(&t, clear != 0) != cudaSuccess) return TACO_ERR_CUDA;
-  *bits = c | d | t;
+  *bits = c | d | t | m;
   return TACO_OK;
 }
 

@@ -35,6 +35,7 @@ constexpr unsigned long long kWaitLimitNs = 1000ull * 1000ull * 1000ull;   // 1 
 constexpr unsigned kFaultCompressWait = 1u;
 constexpr unsigned kFaultDecompressWait = 2u;
 constexpr unsigned kFaultSelftestWait = 4u;
+constexpr unsigned kFaultCompressMmaWait = 8u;
 
 // ------------------------------------------------------------- f32 pairs ----
 // Two fp32 values in one 64-bit register pair, for the packed f32x2 ALU ops.
@@ -124,6 +125,11 @@ __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(addr));
   return r;
 }
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+  uint32_t r;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r) : "r"(addr));
+  return r;
+}
 __device__ __forceinline__ float lds_f32(uint32_t addr) {
   float r;
   asm volatile("ld.shared.f32 %0, [%1];" : "=f"(r) : "r"(addr));
@@ -141,6 +147,9 @@ __device__ __forceinline__ void fence_mbar_init() {
 // later async-proxy (TMA) writes to the same buffer.
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
 }
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes)

@@ -17,6 +17,9 @@ constexpr int kDecompressThreads = 256;
 constexpr int kDecompressMinBlocks = 2;
 constexpr int kDecompressStages = 4;      // (tile, shard) stages in flight per warp
 constexpr int kVariants = 3;              // DUAL, ABSMAX, STATIC
+constexpr int kCompressMmaThreads = 320;  // producer, MMA, 2 x 4 epilogue warps
+// Largest blocks per shard of the tensor-core compress (32-bit TMA coordinates).
+constexpr int64_t kMmaMaxBlocks = (int64_t{1} << 31) - 256;
 
 // Workspace of compress: per shard one arrival counter (16 bytes) followed by
 // one (max s, count) pair per CTA of the shard's grid row.
@@ -38,6 +41,7 @@ struct CompressArgs {
   float sqrt_nE;            // fp32(sqrt(block * E*))
   float inv_sqrt_n;         // fp32(1 / sqrt(block))
   float s_static;           // fp32(sqrt(block * E*) / 448), STATIC variant
+  float n_sqrtE;            // fp32(block * sqrt(E*)), tensor-core compress
 };
 
 struct DecompressArgs {
@@ -65,6 +69,12 @@ const void* compress_kernel_ptr(int block, int variant);
 cudaError_t launch_compress(const CompressArgs& a, int block, int variant, int grid_x, int P,
                             cudaStream_t stream);
 cudaError_t compress_fault(unsigned int* bits, bool clear);
+
+size_t compress_mma_smem_bytes(int block);
+const void* compress_mma_kernel_ptr(int block, int variant);
+cudaError_t launch_compress_mma(const CompressArgs& a, int block, int variant, int grid_x, int P,
+                                cudaStream_t stream);
+cudaError_t compress_mma_fault(unsigned int* bits, bool clear);
 
 int decompress_tile_blocks(int block);
 size_t decompress_smem_bytes();

@@ -126,6 +126,25 @@ taco_status taco_compress_shards(const void* x_bf16, int P, int64_t N, int64_t h
                                  void* workspace, size_t workspace_bytes,
                                  void* stream);
 
+/* ---- taco_compress_shards_mma ----------------------------------------------
+ * taco_compress_shards with the Hadamard rotation on the tensor cores
+ * (tcgen05, sm_100 family): same arguments, layout, headers, workspace and
+ * errors. H_n = H_{n/64} (x) H_64 (Sylvester, TACO pt summary §2.B.1), so
+ * every 64-element chunk of a block is multiplied by H_64 as one row of a
+ * [128 x 64] x [64 x 64] bf16 product accumulated in fp32, and the
+ * log2(n/64) remaining butterfly levels run in registers. The block energy
+ * is taken from the rotated block (sum t^2 = n sum x^2). The outputs meet the
+ * same parity bar as taco_compress_shards; a code can differ from that
+ * path's by one E4M3 step where the fp32 rotated value differs in its last
+ * bits. Extra limit: at most 2^31 - 256 blocks per shard (the tensor
+ * copies address rows with 32-bit coordinates), else TACO_ERR_SHAPE.
+ * N == 0 writes the headers as taco_compress_shards does. */
+taco_status taco_compress_shards_mma(const void* x_bf16, int P, int64_t N, int64_t h,
+                                     int block, float target_energy, int variant,
+                                     void* bundle_out, taco_header* headers_out,
+                                     void* workspace, size_t workspace_bytes,
+                                     void* stream);
+
 /* ---- taco_compress_shards_noalloc -----------------------------------------
  * The paper has no counterpart to this entry point: it exists for callers
  * that cannot allocate device memory when they compress (a communication
@@ -228,12 +247,16 @@ taco_status taco_e4m3_decode_f32(const uint8_t* in, float* out, int64_t n, void*
  * gives up after one second of wall-clock time, sets a bit in a device-side
  * fault word of the library, lets the copies still in flight land (again
  * bounded) and returns, so that a fault never hangs the GPU. Bits:
- *   TACO_FAULT_COMPRESS_WAIT, TACO_FAULT_DECOMPRESS_WAIT, TACO_FAULT_SELFTEST_WAIT.
+ *   TACO_FAULT_COMPRESS_WAIT, TACO_FAULT_DECOMPRESS_WAIT, TACO_FAULT_SELFTEST_WAIT,
+ *   TACO_FAULT_COMPRESS_MMA_WAIT (taco_compress_shards_mma: a wait on a copy,
+ *   an MMA or the epilogue gave up; the CTA drains its MMAs and copies and
+ *   frees its tensor memory before it returns).
  * taco_get_fault reads (and with clear != 0 resets) the word of the current
  * device; it synchronises with the device. */
 #define TACO_FAULT_COMPRESS_WAIT 1u
 #define TACO_FAULT_DECOMPRESS_WAIT 2u
 #define TACO_FAULT_SELFTEST_WAIT 4u
+#define TACO_FAULT_COMPRESS_MMA_WAIT 8u
 taco_status taco_get_fault(uint32_t* bits, int clear);
 
 /* Self-test of that time-out path: one warp waits on a barrier that nothing

@@ -88,6 +88,24 @@ def test_compress_rejects(lib, kwargs, status):
 
 
 @no_gpu_only
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(block=100), BLOCK), (dict(h=130, block=64), SHAPE), (dict(N=-1), SHAPE),
+    (dict(P=0), ARG), (dict(variant=3), ARG), (dict(E=float("nan")), ARG),
+    (dict(N=1 << 26, h=1 << 12, block=64, bundle=1 << 44), SHAPE),   # 2^32 blocks: beyond 32-bit TMA rows
+    (dict(headers=None), NULL), (dict(ws=None), WS), (dict(x=A + 8), ALIGN),
+    (dict(x=A, bundle=A + 64), ARG),
+])
+def test_compress_mma_rejects(lib, kwargs, status):
+    args = dict(x=A, P=1, N=4, h=256, block=128, E=4096.0, variant=0, bundle=A * 64,
+                headers=A * 128, ws=A * 256, wsb=WSB)
+    args.update(kwargs)
+    st = lib.taco_compress_shards_mma(args["x"], args["P"], args["N"], args["h"], args["block"],
+                                      args["E"], args["variant"], args["bundle"], args["headers"],
+                                      args["ws"], args["wsb"], None)
+    assert st == status
+
+
+@no_gpu_only
 def test_single_compress_rejects(lib):
     assert lib.taco_compress(A, 4, 256, 100, 4096.0, 0, A * 64, A * 128, A * 256, WSB, None) == BLOCK
     assert lib.taco_compress(A + 2, 4, 256, 128, 4096.0, 0, A * 64, A * 128, A * 256, WSB, None) == ALIGN

@@ -1,0 +1,153 @@
+"""Tensor-core compress (taco_compress_shards_mma) against the CPU oracle.
+
+Same parity bar as the CUDA-core compress: codes at least 99.99% equal and
+otherwise one E4M3 step apart, alpha and s within 1e-6 relative. The sizes
+leave a ragged last tile of 128 blocks and give some CTAs no tile at all;
+the full-size cases run many tiles per CTA, so every barrier phase wraps.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import parity
+from grads_taco_compress_gb300 import binding as tb
+from grads_taco_compress_gb300 import workloads as W
+from oracle import taco_oracle as O
+import test_gpu_parity as GP
+from test_gpu_parity import E_STAR, _sample_rows, check_compress_against_oracle, dev_bf16, gpu_compress
+
+pytestmark = pytest.mark.gpu
+
+MMA = tb.taco_compress_shards_mma
+
+
+def test_mma_one_tile():
+    """128 blocks of 64: exactly one full tile, one CTA."""
+    rng = np.random.default_rng(40)
+    x = W.f32_to_bf16_bits(rng.normal(0, 0.1, size=(1, 128, 64)).astype(np.float32))
+    check_compress_against_oracle(x, 64, entry=MMA)
+
+
+@pytest.mark.parametrize("block", [64, 128, 256])
+def test_mma_less_than_one_tile(block):
+    rng = np.random.default_rng(41 + block)
+    x = W.f32_to_bf16_bits(rng.laplace(0, 0.05, size=(2, 3, 2 * block)).astype(np.float32))
+    check_compress_against_oracle(x, block, entry=MMA)
+
+
+SMALL = [
+    ("tiny-512x1024", 512),
+    ("gpt2-1.5b-act", 37),
+    ("gpt3-6.7b-act", 29),
+    ("gpt3-6.7b-grad", 23),
+    ("qwen-7b-long", 19),
+]
+
+
+@pytest.mark.parametrize("name,rows", SMALL)
+def test_mma_small(name, rows):
+    w = W.WORKLOADS[name]
+    x = W.make_shards(w, N=rows, P=min(w.P, 3))
+    _, _, _, _, stats = check_compress_against_oracle(x, w.block, entry=MMA)
+    assert all(s["equal_fraction"] >= parity.CODE_EQUAL_FRACTION for s in stats)
+
+
+@pytest.mark.parametrize("block", [64, 128, 256])
+@pytest.mark.parametrize("variant", [tb.VARIANT_DUAL, tb.VARIANT_ABSMAX, tb.VARIANT_STATIC])
+def test_mma_variants_and_targets(block, variant):
+    rng = np.random.default_rng(block + 10 * variant + 1)
+    v = rng.laplace(0, 0.02, size=(2, 41, 3 * block))
+    v[:, :, 5] *= 300.0                              # an outlier channel -> clamped blocks
+    x = W.f32_to_bf16_bits(v.astype(np.float32))
+    for target in (E_STAR, 1.0, 150.0):
+        check_compress_against_oracle(x, block, variant, target, entry=MMA)
+
+
+@pytest.mark.parametrize("block", [64, 128, 256])
+def test_mma_closed_form_blocks(block):
+    GP.test_compress_closed_form_blocks(block, entry=MMA)
+
+
+@pytest.mark.parametrize("block", [64, 128, 256])
+def test_mma_static_hadamard_rows(block):
+    """STATIC: a block equal to a scaled Hadamard row reaches Q_max exactly."""
+    H = O.sylvester_hadamard(block).astype(np.float32)
+    ks = [0, 1, block // 2, block - 1]
+    rows = np.stack([0.25 * H[k] for k in ks] + [-4.0 * H[k] for k in ks])
+    x = W.f32_to_bf16_bits(rows)[None]
+    codes, _, s, _, _ = gpu_compress(x, block, tb.VARIANT_STATIC, entry=MMA)
+    for i, k in enumerate(ks + ks):
+        want = 0x7E if i < len(ks) else 0xFE
+        assert codes[0, i, k] == want
+        assert np.all(np.delete(codes[0, i], k) & 0x7F == 0)
+    assert np.all(s == np.float32(np.sqrt(block * E_STAR) / 448.0))
+
+
+def test_mma_sixteen_shards():
+    rng = np.random.default_rng(44)
+    x = W.f32_to_bf16_bits(rng.normal(0, 1.0, size=(16, 9, 256)).astype(np.float32))
+    check_compress_against_oracle(x, 128, entry=MMA)
+
+
+def test_mma_empty_tensor():
+    x = torch.empty((3, 0, 128), dtype=torch.bfloat16, device="cuda")
+    _, headers = MMA(x, 64)
+    hdr = tb.parse_headers(headers)
+    assert list(hdr["s_max"]) == [0.0] * 3 and list(hdr["N"]) == [0] * 3
+
+
+def test_mma_does_not_write_outside_its_buffers():
+    w = W.WORKLOADS["gpt3-6.7b-grad"]
+    N = 33
+    x = dev_bf16(W.make_shards(w, N=N, P=2))
+    sb = tb.shard_bytes(N, w.h, w.block)
+    guard = 4096
+    big = torch.full((2 * sb + 2 * guard,), 0xA5, dtype=torch.uint8, device="cuda")
+    bundle = big[guard: guard + 2 * sb].view(2, sb)
+    MMA(x, w.block, bundle=bundle)
+    torch.cuda.synchronize()
+    assert bool((big[:guard] == 0xA5).all()) and bool((big[-guard:] == 0xA5).all())
+
+
+def test_mma_deterministic_and_workspace_reset():
+    w = W.WORKLOADS["gpt2-1.5b-act"]
+    x = dev_bf16(W.make_shards(w, N=700, P=2))
+    ws = tb.new_workspace(2)
+    b1, h1 = MMA(x, w.block, workspace=ws)
+    b2, h2 = MMA(x, w.block, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(b1, b2) and torch.equal(h1, h2)
+    assert int(ws.view(torch.uint8).reshape(2, -1)[:, :4].count_nonzero()) == 0
+
+
+FULL = ["tiny-512x1024", "gpt2-1.5b-act", "gpt3-6.7b-act", "gpt3-6.7b-grad", "qwen-7b-long"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_mma_full_size_sampled_and_against_cuda_core_path(name):
+    """Full size: sampled rows against the oracle, every element against the
+    CUDA-core compress (same parity bar), header as the reduction of s."""
+    w = W.WORKLOADS[name]
+    x = W.make_shards(w)
+    codes, alpha, s, hdr, _ = gpu_compress(x, w.block, entry=MMA)
+    rows = _sample_rows(w.N, seed=3)
+    for p in range(w.P):
+        oc, oa, os_, _ = O.compress(x[p][rows], w.block, E_STAR)
+        parity.compare_codes(codes[p][rows], oc, f"{name} codes[{p}]")
+        parity.compare_scales(alpha[p][rows], oa, f"{name} alpha[{p}]")
+        parity.compare_scales(s[p][rows], os_, f"{name} s[{p}]")
+        assert hdr[p]["s_max"] == s[p].max()
+        assert hdr[p]["n_clamped"] == np.count_nonzero(s[p] > 1.0)
+    fc, fa, fs, _, _ = gpu_compress(x, w.block)
+    for p in range(w.P):
+        parity.compare_codes(codes[p], fc[p], f"{name} codes[{p}] vs CUDA-core path")
+        parity.compare_scales(alpha[p], fa[p], f"{name} alpha[{p}] vs CUDA-core path")
+        parity.compare_scales(s[p], fs[p], f"{name} s[{p}] vs CUDA-core path")
+
+
+def test_mma_no_wait_timed_out():
+    """No bounded wait of the tensor-core kernel gave up in the cases above."""
+    assert tb.taco_get_fault() & 8 == 0

@@ -43,18 +43,20 @@ def bundle_from_arrays(codes, alpha, s, block) -> torch.Tensor:
     return torch.from_numpy(buf).cuda()
 
 
-def gpu_compress(x_bits: np.ndarray, block: int, variant=tb.VARIANT_DUAL, target=E_STAR):
-    """x_bits [P,N,h] -> (codes, alpha, s, headers) as numpy, via compress_shards."""
+def gpu_compress(x_bits: np.ndarray, block: int, variant=tb.VARIANT_DUAL, target=E_STAR,
+                 entry=tb.taco_compress_shards):
+    """x_bits [P,N,h] -> (codes, alpha, s, headers) as numpy, via a compress entry."""
     P, N, h = x_bits.shape
-    bundle, headers = tb.taco_compress_shards(dev_bf16(x_bits), block, target, variant)
+    bundle, headers = entry(dev_bf16(x_bits), block, target, variant)
     codes, alpha, s = tb.shard_views(bundle, P, N, h, block)
     torch.cuda.synchronize()
     return (codes.cpu().numpy(), alpha.cpu().numpy(), s.cpu().numpy(),
             tb.parse_headers(headers), bundle)
 
 
-def check_compress_against_oracle(x_bits, block, variant=tb.VARIANT_DUAL, target=E_STAR):
-    codes, alpha, s, hdr, _ = gpu_compress(x_bits, block, variant, target)
+def check_compress_against_oracle(x_bits, block, variant=tb.VARIANT_DUAL, target=E_STAR,
+                                  entry=tb.taco_compress_shards):
+    codes, alpha, s, hdr, _ = gpu_compress(x_bits, block, variant, target, entry)
     stats = []
     for p in range(x_bits.shape[0]):
         oc, oa, os_, oh = O.compress(x_bits[p], block, target, variant)
@@ -130,7 +132,7 @@ def test_compress_variants_and_targets(block, variant):
 
 
 @pytest.mark.parametrize("block", [64, 128, 256])
-def test_compress_closed_form_blocks(block):
+def test_compress_closed_form_blocks(block, entry=tb.taco_compress_shards):
     """Spike, constant and zero blocks: exact codes and exact round trip."""
     H = O.sylvester_hadamard(block)
     rows = []
@@ -141,7 +143,7 @@ def test_compress_closed_form_blocks(block):
     rows.append(np.full(block, 0.0078125, np.float32))
     rows.append(np.zeros(block, np.float32))
     x = W.f32_to_bf16_bits(np.stack(rows))[None]
-    codes, alpha, s, hdr, _ = gpu_compress(x, block)
+    codes, alpha, s, hdr, _ = gpu_compress(x, block, entry=entry)
     for i, j in enumerate((0, 7, block - 1)):
         want = np.where(-H[:, j] > 0, 0x68, 0xE8)
         assert np.array_equal(codes[0, i], want)
