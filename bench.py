@@ -83,14 +83,25 @@ def measured_peaks() -> dict:
     return {}
 
 
-def source_hash() -> str:
-    """Hash of the CUDA sources: ties an ncu traffic figure to the kernel it measured."""
+# The sources each timed kernel is built and launched from (its own file,
+# the shared device header, the launch interface and the C ABI's grid sizing).
+KERNEL_SOURCES = {
+    "compress": "compress_mma.cu",           # the step's compress: tensor-core Hadamard
+    "compress_fwht": "compress.cu",          # CUDA-core FWHT alternative
+    "decompress_reduce": "decompress_reduce.cu",
+    "reduce_recompress": "decompress_reduce.cu",
+}
+COMMON_SOURCES = ("taco_device.cuh", "taco_launch.h", "taco_abi.cu")
+
+
+def source_hash(kernel: str) -> str:
+    """Hash of one kernel's sources: ties an ncu traffic figure to the kernel it measured."""
     h = hashlib.sha256()
     csrc = ROOT / "grads_taco_compress_gb300" / "csrc"
-    for f in sorted(csrc.glob("*")):
-        if f.suffix in (".cu", ".cuh", ".h"):
-            h.update(f.name.encode())
-            h.update(f.read_bytes())
+    for name in (KERNEL_SOURCES[kernel], *COMMON_SOURCES):
+        h.update(name.encode())
+        h.update((csrc / name).read_bytes())
+    h.update((ROOT / "include" / "taco.h").read_bytes())
     return h.hexdigest()[:16]
 
 
@@ -102,7 +113,7 @@ def profiled_traffic(kernel: str, workload: str):
     text = f.read_text()
     mh = re.search(r"source_hash:\s*([0-9a-f]+)", text)
     mt = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not mh or not mt or mh.group(1) != source_hash():
+    if not mh or not mt or mh.group(1) != source_hash(kernel):
         return None
     return float(mt.group(1))
 
@@ -267,9 +278,9 @@ def run_taco(args, w) -> None:
     op = [t.data_ptr() for t in outs]
 
     def compress(k):
-        st = lib.taco_compress_shards(xp[k], P, N, h, n, E, 0, bp[k], hp[k], ws.data_ptr(), wsb, sptr)
+        st = lib.taco_compress_shards_mma(xp[k], P, N, h, n, E, 0, bp[k], hp[k], ws.data_ptr(), wsb, sptr)
         if st:
-            raise taco.TacoError(st, "taco_compress_shards")
+            raise taco.TacoError(st, "taco_compress_shards_mma")
 
     def decompress(k, src):
         st = lib.taco_decompress_reduce(bp[src], P, N, h, n, op[k], sptr)
@@ -329,19 +340,19 @@ def run_taco(args, w) -> None:
 
     t_r = region(lambda i: recompress(i % R, (i + 1) % R))
 
-    # the same compress with the 64-point Hadamard products on the tensor
-    # cores (measured alternative; same outputs within the parity bar)
-    mma_bundles = [torch.empty((P, sb), dtype=torch.uint8, device=dev) for _ in range(R)]
+    # the same compress with the rotation as a CUDA-core FWHT (measured
+    # alternative; same outputs within the parity bar)
+    fwht_bundles = [torch.empty((P, sb), dtype=torch.uint8, device=dev) for _ in range(R)]
 
-    def compress_mma(k):
-        st = lib.taco_compress_shards_mma(xp[k], P, N, h, n, E, 0, mma_bundles[k].data_ptr(), hp[k],
-                                          ws.data_ptr(), wsb, sptr)
+    def compress_fwht(k):
+        st = lib.taco_compress_shards(xp[k], P, N, h, n, E, 0, fwht_bundles[k].data_ptr(), hp[k],
+                                      ws.data_ptr(), wsb, sptr)
         if st:
-            raise taco.TacoError(st, "taco_compress_shards_mma")
+            raise taco.TacoError(st, "taco_compress_shards")
 
     for k in range(3):
-        compress_mma(k % R)
-    t_m = region(lambda i: compress_mma(i % R))
+        compress_fwht(k % R)
+    t_f = region(lambda i: compress_fwht(i % R))
 
     # The whole compressed two-shot AllReduce among P logical ranks (the P
     # input tensors of the step), captured in a CUDA graph and replayed.
@@ -364,8 +375,8 @@ def run_taco(args, w) -> None:
 
     def e2e_step(k):
         xs[k].copy_(x_pin, non_blocking=True)
-        taco.taco_compress_shards(xs[k], n, E, bundle=bundles[k], headers=headers[k], workspace=ws,
-                                  stream=stream)
+        taco.taco_compress_shards_mma(xs[k], n, E, bundle=bundles[k], headers=headers[k], workspace=ws,
+                                      stream=stream)
         taco.taco_decompress_reduce(bundles[k], P, N, h, n, out=outs[k], stream=stream)
         out_pin.copy_(outs[k], non_blocking=True)
 
@@ -393,7 +404,8 @@ def run_taco(args, w) -> None:
             "compress": {"us": round(t_c * 1e6, 3), "alg_bytes": c_bytes,
                          "hbm_gbs": round(c_bytes / t_c / 1e9, 1),
                          "bf16_in_gbs": round(in_bytes / t_c / 1e9, 1),
-                         "frac": round(c_bytes / t_c / 1e9 / hbm, 4)},
+                         "frac": round(c_bytes / t_c / 1e9 / hbm, 4),
+                         "impl": "tcgen05 tensor-core Hadamard (taco_compress_shards_mma)"},
             "decompress_reduce": {"us": round(t_d * 1e6, 3), "alg_bytes": d_bytes,
                                   "hbm_gbs": round(d_bytes / t_d / 1e9, 1),
                                   "bf16_in_gbs": round(in_bytes / t_d / 1e9, 1),
@@ -402,11 +414,11 @@ def run_taco(args, w) -> None:
                                   "hbm_gbs": round(r_bytes / t_r / 1e9, 1),
                                   "bf16_in_gbs": round(in_bytes / t_r / 1e9, 1),
                                   "frac": round(r_bytes / t_r / 1e9 / hbm, 4)},
-            "compress_mma": {"us": round(t_m * 1e6, 3), "alg_bytes": c_bytes,
-                             "hbm_gbs": round(c_bytes / t_m / 1e9, 1),
-                             "bf16_in_gbs": round(in_bytes / t_m / 1e9, 1),
-                             "frac": round(c_bytes / t_m / 1e9 / hbm, 4),
-                             "note": "tcgen05 tensor-core Hadamard, not in the timed step"},
+            "compress_fwht": {"us": round(t_f * 1e6, 3), "alg_bytes": c_bytes,
+                              "hbm_gbs": round(c_bytes / t_f / 1e9, 1),
+                              "bf16_in_gbs": round(in_bytes / t_f / 1e9, 1),
+                              "frac": round(c_bytes / t_f / 1e9 / hbm, 4),
+                              "impl": "CUDA-core FWHT (taco_compress_shards), not in the timed step"},
         }
         kern["emulated_two_shot_allreduce"] = {
             "us": round(t_ar * 1e6, 3), "ranks": P, "tensor": [N, h], "launches": ar.launches(),

@@ -8,7 +8,8 @@ permutations, which is what the receive buffers of a real ReduceScatter and
 AllGather would hand to the same calls.
 
   rank r:  X_r [M, h] = R row chunks of [M/R, h]
-  1. compress      rank r compresses its R chunks         (taco_compress_shards)
+  1. compress      rank r compresses its R chunks         (taco_compress_shards_mma,
+                                                           or taco_compress_shards)
   2. ReduceScatter rank c receives chunk c of every rank  (pointers)
   3. reduce        rank c sums and recompresses them      (taco_reduce_recompress_ptrs)
   4. AllGather     every rank receives the R results      (pointers)
@@ -29,9 +30,13 @@ class EmulatedTwoShotAllReduce:
 
     def __init__(self, R: int, M: int, h: int, block: int,
                  target_energy: float = tb.DEFAULT_TARGET_ENERGY, variant: int = tb.VARIANT_DUAL,
-                 device="cuda"):
+                 device="cuda", compress: str = "mma"):
+        """compress: "mma" (tensor-core Hadamard) or "fwht" (CUDA-core FWHT)."""
         if not 1 <= R <= tb.MAX_SHARDS:
             raise ValueError(f"R must be in 1..{tb.MAX_SHARDS}")
+        if compress not in ("mma", "fwht"):
+            raise ValueError('compress must be "mma" or "fwht"')
+        self._compress = tb.taco_compress_shards_mma if compress == "mma" else tb.taco_compress_shards
         if M % R:
             raise ValueError("M must be a multiple of R")
         self.R, self.M, self.h, self.block = R, M, h, block
@@ -57,9 +62,9 @@ class EmulatedTwoShotAllReduce:
         if xs.shape != (R, self.M, h) or xs.dtype != torch.bfloat16 or not xs.is_contiguous():
             raise ValueError(f"xs must be a contiguous bf16 tensor of shape {(R, self.M, h)}")
         for r in range(R):                                            # 1. compress
-            tb.taco_compress_shards(xs[r].view(R, c, h), n, self.target_energy, self.variant,
-                                    bundle=self.bundles[r], headers=self.headers[r],
-                                    workspace=self.workspace, stream=stream)
+            self._compress(xs[r].view(R, c, h), n, self.target_energy, self.variant,
+                           bundle=self.bundles[r], headers=self.headers[r],
+                           workspace=self.workspace, stream=stream)
         for dst in range(R):                                          # 2.+3. reduce-scatter
             received = [self.bundles[r][dst] for r in range(R)]
             tb.taco_reduce_recompress_ptrs(received, c, h, n, self.target_energy, self.variant,

@@ -16,7 +16,8 @@
 // The energy comes from the rotated block (Parseval: sum t^2 = n sum x^2),
 // so no thread reads x itself: alpha = n sqrt(E*) / sqrt(sum t^2).
 //
-// CTA = 10 warps, one CTA per SM (its shared memory does not fit twice):
+// CTA = 10 warps; two CTAs per SM for n <= 128 (4 stages each), one for
+// n = 256 (6 stages: a tile is 4 atoms), the fastest shapes measured:
 //   warp 0     TMA producer: 3-D tensor loads of [128 blocks x 64 elements]
 //              bf16 atoms (16 KB, 128-byte swizzle) into a ring of stages;
 //   warp 1     owns the tensor memory (2 accumulators x n columns) and one
@@ -47,27 +48,28 @@ namespace {
 
 __device__ unsigned int g_compress_mma_fault;
 
-constexpr int kThreads = kCompressMmaThreads;
-constexpr int kStages = 6;                    // 16 KB input atoms in flight per CTA
 constexpr int kRows = 128;                    // blocks per tile (the MMA's M)
 constexpr uint32_t kAtomBytes = kRows * 64 * 2;       // 16 KB of bf16
 constexpr uint32_t kCodeAtomBytes = kRows * 64;       // 8 KB of codes
 constexpr uint32_t kHBytes = 64 * 64 * 2;             // H_64 in bf16
 
-// Shared memory map (offsets from a 1024-byte aligned base).
+// Shared memory map (offsets from a 1024-byte aligned base) and CTA shape.
 template <int NB>
 struct Smem {
   static constexpr int NC = NB / 64;
+  static constexpr int NG = compress_mma_groups(NB);               // epilogue groups
+  static constexpr int threads = compress_mma_threads(NB);
+  static constexpr int kStages = NB == 256 ? 6 : 4;                 // 16 KB atoms in flight
   static constexpr uint32_t stages = 0;
   static constexpr uint32_t hmat = stages + kStages * kAtomBytes;
   static constexpr uint32_t codes = hmat + kHBytes;                 // [group][chunk] atoms
-  static constexpr uint32_t bars = codes + 2 * NC * kCodeAtomBytes;
-  // barriers: full[kStages], empty[kStages], tfull[2], tempty[2], mma_done
+  static constexpr uint32_t bars = codes + NG * NC * kCodeAtomBytes;
+  // barriers: full[kStages], empty[kStages], tfull[NG], tempty[NG], mma_done
   static constexpr uint32_t full = bars;
   static constexpr uint32_t empty = full + 8 * kStages;
   static constexpr uint32_t tfull = empty + 8 * kStages;
-  static constexpr uint32_t tempty = tfull + 16;
-  static constexpr uint32_t mma_done = tempty + 16;
+  static constexpr uint32_t tempty = tfull + 8 * NG;
+  static constexpr uint32_t mma_done = tempty + 8 * NG;
   static constexpr uint32_t tmem_slot = mma_done + 8;
   static constexpr uint32_t abort_flag = tmem_slot + 4;
   static constexpr uint32_t end = abort_flag + 4;
@@ -284,13 +286,17 @@ __device__ __forceinline__ void slice_codes(const float (&u)[NC][SL], int slice,
 }
 
 template <int NB, int VARIANT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Smem<NB>::threads, 1)
 compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
                     const __grid_constant__ CUtensorMap map_codes, CompressArgs a) {
+  using S = Smem<NB>;
   constexpr int NC = NB / 64;            // 64-element chunks per block
   constexpr int SL = 64 / NC;            // columns per slice (64 registers per slice)
-  constexpr uint32_t TMEM_COLS = 2 * NB; // two accumulators
-  using S = Smem<NB>;
+  constexpr int NG = S::NG;
+  constexpr int kThreads = S::threads;
+  constexpr int kStages = S::kStages;
+  constexpr uint32_t TMEM_COLS = NG * NB;   // one accumulator per epilogue group
+  static_assert(TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "tensor memory columns");
 
   extern __shared__ unsigned char smem_raw[];
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -311,7 +317,7 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
       mbar_init(base + S::full + 8 * s, 1);
       mbar_init(base + S::empty + 8 * s, 1);
     }
-    for (int g = 0; g < 2; ++g) {
+    for (int g = 0; g < NG; ++g) {
       mbar_init(base + S::tfull + 8 * g, 1);
       mbar_init(base + S::tempty + 8 * g, 4);   // one arrival per epilogue warp
     }
@@ -380,8 +386,8 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
       uint32_t i = 0;
       bool ok = true;
       for (int k = 0; k < count && ok; ++k) {
-        const int g = k & 1;
-        const uint32_t use = static_cast<uint32_t>(k >> 1);
+        const int g = k % NG;
+        const uint32_t use = static_cast<uint32_t>(k / NG);
         if (!wait_or_abort(base + S::tempty + 8 * g, (use & 1u) ^ 1u, abort_flag)) break;
         tc_fence_after();
         for (int c = 0; c < NC; ++c, ++i) {
@@ -408,7 +414,7 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
     __syncwarp();
   } else {
     // -------------------------------------------------------- epilogue ----
-    const int g = (warp - 2) >> 2;               // group: accumulator and tiles k % 2 == g
+    const int g = (warp - 2) >> 2;               // group: accumulator and tiles k % NG == g
     const int quad = warp & 3;                   // TMEM lanes 32 quad .. 32 quad + 31
     const int row = quad * 32 + lane;            // block row of the tile
     const bool leader = (warp == 2 + 4 * g) && lane == 0;
@@ -418,8 +424,8 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
     float2* __restrict__ scales_out = reinterpret_cast<float2*>(shard_base + a.scales_off);
     if (leader) prefetch_map(&map_codes);
 
-    for (int k = g; k < count; k += 2) {
-      const uint32_t use = static_cast<uint32_t>(k >> 1);
+    for (int k = g; k < count; k += NG) {
+      const uint32_t use = static_cast<uint32_t>(k / NG);
       const bool got = wait_or_abort(base + S::tfull + 8 * g, use & 1u, abort_flag);
       if (leader) bulk_wait_read<0>();           // the group's last store has read the staging
       if (group_any(1 + g, !got || *abort_flag != 0u)) break;
@@ -502,6 +508,16 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
                           a.headers + shard, a.N, a.h, NB, VARIANT, a.target_energy);
 }
 
+// Every CTA that shared memory lets onto one SM (228 KB, 1 KB reserved per
+// CTA) must find its accumulators in the 512 TMEM columns, or its allocation
+// would wait for another CTA to finish.
+template <int NB>
+constexpr bool fits_sm() {
+  return Smem<NB>::bytes <= 232448 &&
+         (233472 / (Smem<NB>::bytes + 1024)) * compress_mma_groups(NB) * NB <= 512;
+}
+static_assert(fits_sm<64>() && fits_sm<128>() && fits_sm<256>(), "shared or tensor memory per SM");
+
 template <int NB>
 void (*mma_fn(int variant))(CUtensorMap, CUtensorMap, CompressArgs) {
   return variant == 0   ? compress_mma_kernel<NB, 0>
@@ -572,7 +588,7 @@ cudaError_t launch_compress_mma(const CompressArgs& a, int block, int variant, i
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid_x, P);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(compress_mma_threads(block));
   cfg.dynamicSmemBytes = compress_mma_smem_bytes(block);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

@@ -95,7 +95,7 @@ cudaError_t device_info(const DeviceInfo** out) {
         err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, msmem);
         if (err == cudaSuccess)
           err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ_mma[b][v], k,
-                                                              kCompressMmaThreads, msmem);
+                                                              compress_mma_threads(blocks[b]), msmem);
       }
       for (int v = 0; v < kVariants && err == cudaSuccess; ++v) {
         const void* k = recompress_kernel_ptr(blocks[b], v);

@@ -17,7 +17,10 @@ constexpr int kDecompressThreads = 256;
 constexpr int kDecompressMinBlocks = 2;
 constexpr int kDecompressStages = 4;      // (tile, shard) stages in flight per warp
 constexpr int kVariants = 3;              // DUAL, ABSMAX, STATIC
-constexpr int kCompressMmaThreads = 320;  // producer, MMA, 2 x 4 epilogue warps
+// Tensor-core compress: a producer warp, an MMA warp and groups of 4
+// epilogue warps, one accumulator of `block` TMEM columns per group.
+constexpr int compress_mma_groups(int) { return 2; }
+constexpr int compress_mma_threads(int block) { return 64 + 128 * compress_mma_groups(block); }
 // Largest blocks per shard of the tensor-core compress (32-bit TMA coordinates).
 constexpr int64_t kMmaMaxBlocks = (int64_t{1} << 31) - 256;
 

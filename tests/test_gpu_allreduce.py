@@ -35,12 +35,13 @@ def oracle_allreduce(xs, block):
     return np.concatenate(out)
 
 
+@pytest.mark.parametrize("compress", ["mma", "fwht"])
 @pytest.mark.parametrize("name,R,M", [("gpt2-1.5b-act", 4, 64), ("gpt3-6.7b-act", 8, 48),
                                       ("gpt3-6.7b-grad", 2, 30), ("tiny-512x1024", 2, 128)])
-def test_allreduce_matches_oracle_pipeline(name, R, M):
+def test_allreduce_matches_oracle_pipeline(name, R, M, compress):
     w = dataclasses.replace(W.WORKLOADS[name], P=R)
     xs = W.make_shards(w, N=M)                                   # rank r's tensor in xs[r]
-    ar = EmulatedTwoShotAllReduce(R, M, w.h, w.block)
+    ar = EmulatedTwoShotAllReduce(R, M, w.h, w.block, compress=compress)
     got = host_bits(ar(dev_bf16(xs)))
     want = oracle_allreduce(xs, w.block)
     parity.compare_recon(O.bf16_bits_to_f64(got), O.bf16_bits_to_f64(want), "allreduce output")
