@@ -31,6 +31,11 @@ in fp64, inverting each shard on its own and summing: the plain definition.
 Reduce-recompress (the reduced chunk compressed again for the AllGather,
 [PT] §2.B.3): the compress steps applied to the fp64 x_hat above, before
 any rounding to bf16.
+INT8 fallback ([PT] §5 "Agnóstico de Hardware": the framework degrades to
+INT8 on hardware without FP8): every step above with the code format
+replaced, q_i = round-half-even(y_i / s_k) as a signed byte, Q_max = 127 in
+the scale rules, decoded as the integer itself. The pages give no more than
+"INT8"; this symmetric uniform reading is the plainest one.
 
 Readings taken where the pages are silent (each one is a choice):
   * dual scale: alpha_k sets the block energy before rotation (the
@@ -68,6 +73,9 @@ import math
 import numpy as np
 
 Q_MAX = 448.0
+Q_MAX_INT8 = 127.0
+FORMAT_E4M3 = 0
+FORMAT_INT8 = 1
 DEFAULT_TARGET_ENERGY = 4096.0
 VARIANT_DUAL = 0
 VARIANT_ABSMAX = 1
@@ -144,6 +152,41 @@ def e4m3_encode(v) -> np.ndarray:
 
 
 # --------------------------------------------------------------------------
+# INT8 codec of the fallback format ([PT] §5; uniform steps, [PT] §2.A)
+# --------------------------------------------------------------------------
+def int8_encode(v) -> np.ndarray:
+    """fp32 values -> signed bytes (as uint8 bit patterns).
+
+    Round to the nearest integer, ties to even, then clamp to [-127, 127]
+    (symmetric: -128 is never produced). NaN gives 0.
+    """
+    v32 = np.asarray(v, dtype=np.float32).astype(np.float64)
+    q = np.rint(np.where(np.isnan(v32), 0.0, v32))
+    q = np.clip(q, -Q_MAX_INT8, Q_MAX_INT8)
+    return q.astype(np.int64).astype(np.int8).view(np.uint8)
+
+
+def int8_decode(codes: np.ndarray) -> np.ndarray:
+    return np.asarray(codes, dtype=np.uint8).view(np.int8).astype(np.float64)
+
+
+def q_max(fmt: int) -> float:
+    if fmt == FORMAT_E4M3:
+        return Q_MAX
+    if fmt == FORMAT_INT8:
+        return Q_MAX_INT8
+    raise ValueError("unknown code format")
+
+
+def encode(fmt: int, v) -> np.ndarray:
+    return e4m3_encode(v) if fmt == FORMAT_E4M3 else int8_encode(v)
+
+
+def decode(fmt: int, codes) -> np.ndarray:
+    return e4m3_decode(codes) if fmt == FORMAT_E4M3 else int8_decode(codes)
+
+
+# --------------------------------------------------------------------------
 # bfloat16 helpers (inputs are bf16; the reduce writes bf16)
 # --------------------------------------------------------------------------
 def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
@@ -188,7 +231,7 @@ def _check_shape(h: int, block: int) -> None:
 
 def compress_stages(x_bits: np.ndarray, block: int,
                     target_energy: float = DEFAULT_TARGET_ENERGY,
-                    variant: int = VARIANT_DUAL) -> dict:
+                    variant: int = VARIANT_DUAL, fmt: int = FORMAT_E4M3) -> dict:
     """Compress a bf16 [N, h] tensor, returning every intermediate.
 
     ``x_bits`` holds bf16 bit patterns (uint16). Returned arrays, with
@@ -197,12 +240,12 @@ def compress_stages(x_bits: np.ndarray, block: int,
     per-tensor ``header`` dict.
     """
     x_bits = np.asarray(x_bits, dtype=np.uint16)
-    return compress_values_stages(bf16_bits_to_f64(x_bits), block, target_energy, variant)
+    return compress_values_stages(bf16_bits_to_f64(x_bits), block, target_energy, variant, fmt)
 
 
 def compress_values_stages(x_values: np.ndarray, block: int,
                            target_energy: float = DEFAULT_TARGET_ENERGY,
-                           variant: int = VARIANT_DUAL) -> dict:
+                           variant: int = VARIANT_DUAL, fmt: int = FORMAT_E4M3) -> dict:
     """The same steps on real values [N, h] (float64) instead of bf16 inputs.
 
     Used for the compression of a reduced tensor that never went through a
@@ -215,6 +258,7 @@ def compress_values_stages(x_values: np.ndarray, block: int,
     _check_shape(h, n)
     if variant not in VARIANTS:
         raise ValueError("unknown variant")
+    qm = q_max(fmt)
     K = h // n
     x = x_values.reshape(N, K, n)
 
@@ -234,21 +278,21 @@ def compress_values_stages(x_values: np.ndarray, block: int,
     # 4. post-rotation scale s_k: fit the rotated block into Q_max ([PT] §2.B.2)
     amax = np.max(np.abs(y.astype(np.float64)), axis=-1)
     if variant == VARIANT_DUAL:
-        s = np.maximum(1.0, amax / Q_MAX).astype(np.float32)
+        s = np.maximum(1.0, amax / qm).astype(np.float32)
     elif variant == VARIANT_ABSMAX:
-        s = np.where(amax > 0, amax / Q_MAX, 1.0).astype(np.float32)
+        s = np.where(amax > 0, amax / qm, 1.0).astype(np.float32)
     else:
-        # one scale for the whole tensor, fixed by E* and n alone
-        s = np.full((N, K), np.float32(static_scale(n, target_energy)), dtype=np.float32)
+        # one scale for the whole tensor, fixed by E*, n and Q_max alone
+        s = np.full((N, K), np.float32(static_scale(n, target_energy, fmt)), dtype=np.float32)
 
     # 5. FP8 E4M3 codes of y / s_k (the value rounded is an fp32 number)
     ratio = (y.astype(np.float64) / s.astype(np.float64)[..., None]).astype(np.float32)
-    codes = e4m3_encode(ratio).reshape(N, h)
+    codes = encode(fmt, ratio).reshape(N, h)
 
     # 6. per-tensor header
     header = {
         "N": N, "h": h, "block": n, "variant": variant,
-        "target_energy": float(np.float32(target_energy)), "q_max": Q_MAX,
+        "target_energy": float(np.float32(target_energy)), "q_max": qm,
         "s_max": float(s.max()) if s.size else 0.0,
         "n_clamped": int(np.count_nonzero(s > 1.0)),
     }
@@ -256,16 +300,17 @@ def compress_values_stages(x_values: np.ndarray, block: int,
             "codes": codes, "header": header}
 
 
-def static_scale(block: int, target_energy: float = DEFAULT_TARGET_ENERGY) -> float:
+def static_scale(block: int, target_energy: float = DEFAULT_TARGET_ENERGY,
+                 fmt: int = FORMAT_E4M3) -> float:
     """fp32(sqrt(n E*) / Q_max): the STATIC variant's scale of every block."""
-    return float(np.float32(math.sqrt(block * float(target_energy)) / Q_MAX))
+    return float(np.float32(math.sqrt(block * float(target_energy)) / q_max(fmt)))
 
 
 def compress(x_bits: np.ndarray, block: int,
              target_energy: float = DEFAULT_TARGET_ENERGY,
-             variant: int = VARIANT_DUAL):
+             variant: int = VARIANT_DUAL, fmt: int = FORMAT_E4M3):
     """(codes u8 [N,h], alpha f32 [N,K], s f32 [N,K], header dict)."""
-    st = compress_stages(x_bits, block, target_energy, variant)
+    st = compress_stages(x_bits, block, target_energy, variant, fmt)
     return st["codes"], st["alpha"], st["s"], st["header"]
 
 
@@ -273,14 +318,14 @@ def compress(x_bits: np.ndarray, block: int,
 # Decompress-reduce
 # --------------------------------------------------------------------------
 def decompress_one_f64(codes: np.ndarray, alpha: np.ndarray, s: np.ndarray,
-                       block: int) -> np.ndarray:
+                       block: int, fmt: int = FORMAT_E4M3) -> np.ndarray:
     """Reconstruct one shard in fp64: undo s, the rotation, then alpha."""
     codes = np.asarray(codes, dtype=np.uint8)
     N, h = codes.shape
     n = block
     _check_shape(h, n)
     K = h // n
-    q = e4m3_decode(codes).reshape(N, K, n)
+    q = decode(fmt, codes).reshape(N, K, n)
     w = np.asarray(s, dtype=np.float32).astype(np.float64)[..., None] * q
     H = sylvester_hadamard(n).astype(np.float64)
     # inverse of the orthonormal rotation H/sqrt(n) is its transpose
@@ -290,7 +335,7 @@ def decompress_one_f64(codes: np.ndarray, alpha: np.ndarray, s: np.ndarray,
 
 
 def decompress_reduce_f64(codes: np.ndarray, alpha: np.ndarray, s: np.ndarray,
-                          block: int) -> np.ndarray:
+                          block: int, fmt: int = FORMAT_E4M3) -> np.ndarray:
     """Sum over the P shards of the fp64 reconstructions (before rounding).
 
     ``codes`` u8 [P,N,h], ``alpha`` and ``s`` f32 [P,N,K].
@@ -299,14 +344,14 @@ def decompress_reduce_f64(codes: np.ndarray, alpha: np.ndarray, s: np.ndarray,
     P = codes.shape[0]
     total = np.zeros(codes.shape[1:], dtype=np.float64)
     for p in range(P):
-        total += decompress_one_f64(codes[p], alpha[p], s[p], block)
+        total += decompress_one_f64(codes[p], alpha[p], s[p], block, fmt)
     return total
 
 
 def decompress_reduce(codes: np.ndarray, alpha: np.ndarray, s: np.ndarray,
-                      block: int) -> np.ndarray:
+                      block: int, fmt: int = FORMAT_E4M3) -> np.ndarray:
     """bf16 bit patterns [N,h] of the reduced reconstruction (one RNE)."""
-    return f64_to_bf16_bits(decompress_reduce_f64(codes, alpha, s, block))
+    return f64_to_bf16_bits(decompress_reduce_f64(codes, alpha, s, block, fmt))
 
 
 # --------------------------------------------------------------------------

@@ -291,6 +291,72 @@ def check_static_variant(O):
         assert st["header"]["s_max"] == float(s_ref)
 
 
+def _nearest_int_tie_even(v: float) -> int:
+    """Nearest integer by comparing the two neighbours (no library rounding)."""
+    lo = math.floor(v)
+    d_lo, d_hi = v - lo, lo + 1 - v
+    if d_lo < d_hi:
+        return lo
+    if d_hi < d_lo:
+        return lo + 1
+    return lo if lo % 2 == 0 else lo + 1
+
+
+def check_int8_codec(O):
+    """INT8 codes: nearest integer, ties to even, clamp to +-127; two's complement bytes."""
+    ints = np.arange(-127, 128)
+    assert np.array_equal(O.int8_decode(O.int8_encode(ints.astype(np.float32))), ints)
+    assert np.array_equal(O.int8_encode(ints.astype(np.float32)), (ints & 0xFF).astype(np.uint8))
+    assert np.array_equal(O.int8_decode(np.arange(256, dtype=np.uint8)),
+                          np.concatenate([np.arange(0, 128), np.arange(-128, 0)]).astype(np.float64))
+    rng = np.random.default_rng(13)
+    v = np.concatenate([np.arange(-130, 130.5, 0.25), rng.uniform(-140, 140, 2000),
+                        [0.49999997, -0.49999997, 1e-30, -1e-30, 127.5, -127.5, 1e30, -1e30, np.inf, -np.inf]])
+    v = v.astype(np.float32)
+    got = O.int8_decode(O.int8_encode(v))
+    want = [max(-127, min(127, _nearest_int_tie_even(float(x)))) if np.isfinite(x)
+            else (127 if x > 0 else -127) for x in v]
+    assert np.array_equal(got, np.array(want, dtype=np.float64))
+    assert np.all(O.int8_encode(v) != 0x80)                  # -128 is never produced
+
+
+def check_int8_closed_forms(O):
+    """The FP8 closed forms with Q_max = 127: spike -> +-sqrt(E*) = +-64, constant -> one 127."""
+    for n in (64, 128, 256):
+        H = O.sylvester_hadamard(n)
+        for c in (0.0078125, -3.5):
+            j = 5 % n
+            spike = np.zeros(n, np.float32)
+            spike[j] = c
+            x = _bf16_bits(spike)[None, :]
+            codes, alpha, s, hdr = O.compress(x, n, E_STAR, O.VARIANT_DUAL, O.FORMAT_INT8)
+            assert s[0, 0] == 1.0 and hdr["q_max"] == 127.0
+            want = np.where(np.sign(c) * H[:, j] > 0, 64, -64)
+            assert np.array_equal(O.int8_decode(codes[0]), want.astype(np.float64))
+            assert np.array_equal(O.decompress_reduce(codes[None], alpha[None], s[None], n, O.FORMAT_INT8), x)
+            const = _bf16_bits(np.full(n, c, np.float32))[None, :]
+            codes, alpha, s, hdr = O.compress(const, n, E_STAR, O.VARIANT_DUAL, O.FORMAT_INT8)
+            assert math.isclose(float(s[0, 0]), math.sqrt(n * E_STAR) / 127.0, rel_tol=2e-7)
+            q = O.int8_decode(codes[0])
+            assert q[0] == (127 if c > 0 else -127) and np.all(q[1:] == 0)
+            assert np.array_equal(O.decompress_reduce(codes[None], alpha[None], s[None], n, O.FORMAT_INT8), const)
+
+
+def check_int8_error_bound(O):
+    """Uniform steps of s: every rotated value is off by at most s/2, so a block's
+    reconstruction error is at most (s/2) sqrt(n) / alpha (the rotation is orthonormal)."""
+    rng = np.random.default_rng(14)
+    for n, E in ((64, 4096.0), (128, 900.0), (256, 150.0)):
+        x = _random_bf16(rng, (24, 4 * n), 0.01)
+        x[:, 3] = _random_bf16(rng, (24,), 2.0)
+        codes, alpha, s, _ = O.compress(x, n, E, O.VARIANT_DUAL, O.FORMAT_INT8)
+        rec = O.decompress_reduce_f64(codes[None], alpha[None], s[None], n, O.FORMAT_INT8)
+        err = (rec - O.bf16_bits_to_f64(x)).reshape(24, 4, n)
+        bound = s.astype(np.float64) / 2 * math.sqrt(n) / alpha.astype(np.float64)
+        assert np.all(np.linalg.norm(err, axis=-1) <= bound * (1 + 1e-5) + 1e-30)
+        assert np.all(np.abs(O.int8_decode(codes)) <= 127)
+
+
 # --------------------------------------------------------------------------
 # Decompress-reduce: sum in the rotated domain, invert once (linearity)
 # --------------------------------------------------------------------------

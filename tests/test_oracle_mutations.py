@@ -20,7 +20,7 @@ MUTATIONS = {
     "energy_sum_not_mean": ("energy = np.sum(x * x, axis=-1) / n", "energy = np.sum(x * x, axis=-1)"),
     "energy_centred": ("energy = np.sum(x * x, axis=-1) / n",
                        "energy = np.var(x, axis=-1)"),
-    "no_overflow_floor": ("np.maximum(1.0, amax / Q_MAX)", "(amax / Q_MAX)"),
+    "no_overflow_floor": ("np.maximum(1.0, amax / qm)", "(amax / qm)"),
     "qmax_wrong": ("Q_MAX = 448.0", "Q_MAX = 240.0"),
     "hadamard_sign_moved": ("h = np.block([[h, h], [h, -h]])", "h = np.block([[h, -h], [h, h]])"),
     "e4m3_ties_odd": ("(hi % 2 == 0)", "(hi % 2 == 1)"),
@@ -36,10 +36,16 @@ MUTATIONS = {
     "reduce_drops_last_shard": ("for p in range(P):", "for p in range(P - 1):"),
     "recompress_first_shard_only": ("x_hat = decompress_reduce_f64(codes, alpha, s, block)",
                                     "x_hat = decompress_reduce_f64(codes[:1], alpha[:1], s[:1], block)"),
-    "static_scale_drops_n": ("math.sqrt(block * float(target_energy)) / Q_MAX",
-                             "math.sqrt(float(target_energy)) / Q_MAX"),
-    "static_scale_per_block_amax": ("np.full((N, K), np.float32(static_scale(n, target_energy)), dtype=np.float32)",
-                                    "np.maximum(1.0, amax / Q_MAX).astype(np.float32)"),
+    "static_scale_drops_n": ("math.sqrt(block * float(target_energy)) / q_max(fmt)",
+                             "math.sqrt(float(target_energy)) / q_max(fmt)"),
+    "static_scale_per_block_amax": ("np.full((N, K), np.float32(static_scale(n, target_energy, fmt)), dtype=np.float32)",
+                                    "np.maximum(1.0, amax / qm).astype(np.float32)"),
+    "int8_ties_up": ("q = np.rint(np.where(np.isnan(v32), 0.0, v32))",
+                     "q = np.floor(np.where(np.isnan(v32), 0.0, v32) + 0.5)"),
+    "int8_qmax_128": ("Q_MAX_INT8 = 127.0", "Q_MAX_INT8 = 128.0"),
+    "int8_decode_unsigned": ("np.asarray(codes, dtype=np.uint8).view(np.int8).astype(np.float64)",
+                             "np.asarray(codes, dtype=np.uint8).astype(np.float64)"),
+    "int8_scale_uses_fp8_qmax": ("    qm = q_max(fmt)\n", "    qm = Q_MAX\n"),
     "recompress_skips_alpha": ("    st = compress_values_stages(x_hat, block, target_energy, variant)\n    return st[\"codes\"], st[\"alpha\"]",
                                "    st = compress_values_stages(x_hat, block, target_energy, variant)\n    return st[\"codes\"], st[\"alpha\"] * 0 + 1"),
 }
