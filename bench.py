@@ -354,6 +354,24 @@ def run_taco(args, w) -> None:
         compress_fwht(k % R)
     t_f = region(lambda i: compress_fwht(i % R))
 
+    # the INT8 fallback format: compress (tensor cores) and decompress-reduce
+    # of its own bundles (same bytes per element as the FP8 format)
+    def compress_int8(k):
+        st = lib.taco_compress_shards_int8(xp[k], P, N, h, n, E, 0, fwht_bundles[k].data_ptr(), hp[k],
+                                           ws.data_ptr(), wsb, sptr)
+        if st:
+            raise taco.TacoError(st, "taco_compress_shards_int8")
+
+    def decompress_int8(k, src):
+        st = lib.taco_decompress_reduce_int8(fwht_bundles[src].data_ptr(), P, N, h, n, op[k], sptr)
+        if st:
+            raise taco.TacoError(st, "taco_decompress_reduce_int8")
+
+    for k in range(R):
+        compress_int8(k)
+    t_ci = region(lambda i: compress_int8(i % R))
+    t_di = region(lambda i: decompress_int8(i % R, (i + 1) % R))
+
     # The whole compressed two-shot AllReduce among P logical ranks (the P
     # input tensors of the step), captured in a CUDA graph and replayed.
     from grads_taco_compress_gb300.allreduce import EmulatedTwoShotAllReduce
@@ -419,6 +437,14 @@ def run_taco(args, w) -> None:
                               "bf16_in_gbs": round(in_bytes / t_f / 1e9, 1),
                               "frac": round(c_bytes / t_f / 1e9 / hbm, 4),
                               "impl": "CUDA-core FWHT (taco_compress_shards), not in the timed step"},
+            "compress_int8": {"us": round(t_ci * 1e6, 3), "alg_bytes": c_bytes,
+                              "hbm_gbs": round(c_bytes / t_ci / 1e9, 1),
+                              "frac": round(c_bytes / t_ci / 1e9 / hbm, 4),
+                              "impl": "INT8 fallback codes, tensor cores, not in the timed step"},
+            "decompress_reduce_int8": {"us": round(t_di * 1e6, 3), "alg_bytes": d_bytes,
+                                       "hbm_gbs": round(d_bytes / t_di / 1e9, 1),
+                                       "frac": round(d_bytes / t_di / 1e9 / hbm, 4),
+                                       "impl": "INT8 fallback codes, not in the timed step"},
         }
         kern["emulated_two_shot_allreduce"] = {
             "us": round(t_ar * 1e6, 3), "ranks": P, "tensor": [N, h], "launches": ar.launches(),

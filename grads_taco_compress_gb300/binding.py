@@ -38,6 +38,7 @@ EXPORTED_SYMBOLS = (
     "taco_shard_bytes", "taco_shard_scales_offset",
     "taco_workspace_bytes", "taco_compress", "taco_compress_shards",
     "taco_compress_shards_noalloc", "taco_compress_shards_mma",
+    "taco_compress_shards_int8", "taco_decompress_reduce_int8",
     "taco_decompress_reduce", "taco_decompress_reduce_ptrs",
     "taco_reduce_recompress", "taco_reduce_recompress_ptrs",
     "taco_decompress_shards", "taco_decompress_shards_ptrs",
@@ -75,6 +76,8 @@ def _lib() -> ctypes.CDLL:
             "taco_compress_shards": (i32, [vp, i32, i64, i64, i32, f32, i32, vp, vp, vp, sz, vp]),
             "taco_compress_shards_noalloc": (i32, [vp, i32, i64, i64, i32, f32, i32, vp, vp, vp]),
             "taco_compress_shards_mma": (i32, [vp, i32, i64, i64, i32, f32, i32, vp, vp, vp, sz, vp]),
+            "taco_compress_shards_int8": (i32, [vp, i32, i64, i64, i32, f32, i32, vp, vp, vp, sz, vp]),
+            "taco_decompress_reduce_int8": (i32, [vp, i32, i64, i64, i32, vp, vp]),
             "taco_decompress_reduce": (i32, [vp, i32, i64, i64, i32, vp, vp]),
             "taco_decompress_reduce_ptrs": (i32, [ctypes.POINTER(vp), i32, i64, i64, i32, vp, vp]),
             "taco_decompress_shards": (i32, [vp, i32, i64, i64, i32, vp, vp]),
@@ -239,16 +242,36 @@ def taco_compress(x: torch.Tensor, block: int, target_energy: float = DEFAULT_TA
     return shard, header
 
 
-def taco_decompress_reduce(bundle: torch.Tensor, P: int, N: int, h: int, block: int,
-                           out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """Sum of the P reconstructions of a bundle as bf16 [N, h]."""
+def _decompress_reduce(entry: str, bundle: torch.Tensor, P: int, N: int, h: int, block: int,
+                       out, stream) -> torch.Tensor:
     if not bundle.is_cuda:
         raise ValueError("bundle must be a CUDA tensor")
     if out is None:
         out = torch.empty((N, h), dtype=torch.bfloat16, device=bundle.device)
-    st = _lib().taco_decompress_reduce(_ptr(bundle), P, N, h, block, _ptr(out), _stream_ptr(stream))
-    _check(st, "taco_decompress_reduce")
+    st = getattr(_lib(), entry)(_ptr(bundle), P, N, h, block, _ptr(out), _stream_ptr(stream))
+    _check(st, entry)
     return out
+
+
+def taco_decompress_reduce(bundle: torch.Tensor, P: int, N: int, h: int, block: int,
+                           out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Sum of the P reconstructions of a bundle as bf16 [N, h]."""
+    return _decompress_reduce("taco_decompress_reduce", bundle, P, N, h, block, out, stream)
+
+
+def taco_compress_shards_int8(x: torch.Tensor, block: int, target_energy: float = DEFAULT_TARGET_ENERGY,
+                              variant: int = VARIANT_DUAL, bundle: torch.Tensor | None = None,
+                              headers: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                              stream=None):
+    """taco_compress_shards_mma with INT8 fallback codes (Q_max 127)."""
+    return _compress_shards("taco_compress_shards_int8", x, block, target_energy, variant, bundle,
+                            headers, workspace, stream)
+
+
+def taco_decompress_reduce_int8(bundle: torch.Tensor, P: int, N: int, h: int, block: int,
+                                out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """taco_decompress_reduce of a bundle with INT8 fallback codes."""
+    return _decompress_reduce("taco_decompress_reduce_int8", bundle, P, N, h, block, out, stream)
 
 
 def taco_decompress_reduce_ptrs(shards, N: int, h: int, block: int,

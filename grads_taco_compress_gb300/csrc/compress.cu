@@ -220,7 +220,7 @@ compress_kernel(CompressArgs a) {
 
   // ---- per-tensor header: CTA reduction, then the last CTA of the shard ----
   finish_header<kCompressThreads>(part_smax, part_cnt, a.workspace + shard * kWorkspaceShardStride,
-                                  a.headers + shard, a.N, a.h, NB, VARIANT, a.target_energy);
+                                  a.headers + shard, a.N, a.h, NB, VARIANT, a.target_energy, a.q_max);
 }
 
 template <int NB>

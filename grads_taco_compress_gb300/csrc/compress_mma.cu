@@ -30,6 +30,9 @@
 //              rotation, computes alpha, s and the codes, writes the codes
 //              into a 64-byte-swizzled staging buffer that one thread stores
 //              with 3-D TMA tensor stores, and stores its (alpha, s) pair.
+// FMT selects the code format: 0 = FP8 E4M3 (Q_max 448), 1 = the INT8
+// fallback (Q_max 127, round half to even; pt summary §5, hardware without
+// FP8).
 // Every wait is bounded in time; a wait that gives up sets a CTA-wide abort
 // flag that ends every role's loop, records kFaultCompressMmaWait and lets
 // the CTA drain its copies and MMAs before it frees the tensor memory.
@@ -262,7 +265,7 @@ __device__ __forceinline__ void slice_stats(const float (&u)[NC][SL], f2 (&ea)[4
 // Codes of one slice into the group's staging atoms: chunk c of block row
 // `row` is 64 bytes at row * 64 of atom c, its 16-byte pieces permuted by the
 // 64-byte swizzle (piece ^= (row >> 1) & 3) that the tensor store undoes.
-template <int NC, int SL>
+template <int NC, int SL, int FMT>
 __device__ __forceinline__ void slice_codes(const float (&u)[NC][SL], int slice, float g,
                                             uint32_t stage_codes, int row) {
   const f2 g2{g, g};
@@ -278,14 +281,14 @@ __device__ __forceinline__ void slice_codes(const float (&u)[NC][SL], int slice,
         const int i = q * 16 + 4 * k;
         const f2 y0 = mul2(f2{u[c][i], u[c][i + 1]}, g2);
         const f2 y1 = mul2(f2{u[c][i + 2], u[c][i + 3]}, g2);
-        w[k] = e4m3x4_from_f32(y0.x, y0.y, y1.x, y1.y);
+        w[k] = (FMT == 0) ? e4m3x4_from_f32(y0.x, y0.y, y1.x, y1.y) : i8x4_from_f32(y0, y1);
       }
       const int piece = (slice * SL) / 16 + q;
       sts128(rbase + c * kCodeAtomBytes + 16 * (piece ^ sw), make_uint4(w[0], w[1], w[2], w[3]));
     }
 }
 
-template <int NB, int VARIANT>
+template <int NB, int VARIANT, int FMT>
 __global__ void __launch_bounds__(Smem<NB>::threads, 1)
 compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
                     const __grid_constant__ CUtensorMap map_codes, CompressArgs a) {
@@ -297,6 +300,7 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
   constexpr int kStages = S::kStages;
   constexpr uint32_t TMEM_COLS = NG * NB;   // one accumulator per epilogue group
   static_assert(TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "tensor memory columns");
+  constexpr float QMAX = (FMT == 0) ? 448.0f : 127.0f;
 
   extern __shared__ unsigned char smem_raw[];
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -457,8 +461,8 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
       const float thi = max3(hi[0], hi[1], fmaxf(hi[2], hi[3]));
       const float tlo = min3(lo[0], lo[1], fminf(lo[2], lo[3]));
       const float amax = cscale * fmaxf(thi, -tlo);
-      const float sc = (VARIANT == 0)   ? fmaxf(1.0f, amax * (1.0f / 448.0f))
-                       : (VARIANT == 1) ? (amax > 0.f ? amax * (1.0f / 448.0f) : 1.0f)
+      const float sc = (VARIANT == 0)   ? fmaxf(1.0f, amax * (1.0f / QMAX))
+                       : (VARIANT == 1) ? (amax > 0.f ? amax * (1.0f / QMAX) : 1.0f)
                                         : a.s_static;
       const float gsc = __fdividef(cscale, sc);              // code value = gsc * t
 
@@ -467,13 +471,13 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(base + S::tempty + 8 * g);
-        slice_codes<NC, SL>(u, 0, gsc, staging, row);
+        slice_codes<NC, SL, FMT>(u, 0, gsc, staging, row);
       } else {
 #pragma unroll 1
         for (int sl = 0; sl < NC; ++sl) {
           load_slice<NC, SL>(tacc, sl, u);
           chunk_butterflies<NC, SL>(u);
-          slice_codes<NC, SL>(u, sl, gsc, staging, row);
+          slice_codes<NC, SL, FMT>(u, sl, gsc, staging, row);
         }
         tc_fence_before();
         __syncwarp();
@@ -505,7 +509,7 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
     tmem_dealloc(tmem, TMEM_COLS);
   }
   finish_header<kThreads>(part_smax, part_cnt, a.workspace + shard * kWorkspaceShardStride,
-                          a.headers + shard, a.N, a.h, NB, VARIANT, a.target_energy);
+                          a.headers + shard, a.N, a.h, NB, VARIANT, a.target_energy, QMAX);
 }
 
 // Every CTA that shared memory lets onto one SM (228 KB, 1 KB reserved per
@@ -518,15 +522,22 @@ constexpr bool fits_sm() {
 }
 static_assert(fits_sm<64>() && fits_sm<128>() && fits_sm<256>(), "shared or tensor memory per SM");
 
-template <int NB>
+template <int NB, int FMT>
 void (*mma_fn(int variant))(CUtensorMap, CUtensorMap, CompressArgs) {
-  return variant == 0   ? compress_mma_kernel<NB, 0>
-         : variant == 1 ? compress_mma_kernel<NB, 1>
-                        : compress_mma_kernel<NB, 2>;
+  return variant == 0   ? compress_mma_kernel<NB, 0, FMT>
+         : variant == 1 ? compress_mma_kernel<NB, 1, FMT>
+                        : compress_mma_kernel<NB, 2, FMT>;
 }
 
-void (*mma_kernel(int block, int variant))(CUtensorMap, CUtensorMap, CompressArgs) {
-  return block == 64 ? mma_fn<64>(variant) : block == 128 ? mma_fn<128>(variant) : mma_fn<256>(variant);
+template <int FMT>
+void (*mma_kernel_fmt(int block, int variant))(CUtensorMap, CUtensorMap, CompressArgs) {
+  return block == 64    ? mma_fn<64, FMT>(variant)
+         : block == 128 ? mma_fn<128, FMT>(variant)
+                        : mma_fn<256, FMT>(variant);
+}
+
+void (*mma_kernel(int block, int variant, int fmt))(CUtensorMap, CUtensorMap, CompressArgs) {
+  return fmt == 0 ? mma_kernel_fmt<0>(block, variant) : mma_kernel_fmt<1>(block, variant);
 }
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no link
@@ -556,12 +567,12 @@ size_t compress_mma_smem_bytes(int block) {
   return block == 64 ? Smem<64>::bytes : block == 128 ? Smem<128>::bytes : Smem<256>::bytes;
 }
 
-const void* compress_mma_kernel_ptr(int block, int variant) {
-  return reinterpret_cast<const void*>(mma_kernel(block, variant));
+const void* compress_mma_kernel_ptr(int block, int variant, int fmt) {
+  return reinterpret_cast<const void*>(mma_kernel(block, variant, fmt));
 }
 
-cudaError_t launch_compress_mma(const CompressArgs& a, int block, int variant, int grid_x, int P,
-                                cudaStream_t stream) {
+cudaError_t launch_compress_mma(const CompressArgs& a, int block, int variant, int fmt, int grid_x,
+                                int P, cudaStream_t stream) {
   EncodeTiled encode = encoder();
   if (!encode) return cudaErrorNotSupported;
   // x viewed as [P][nblocks][block] bf16; one box = one chunk of 128 blocks.
@@ -596,7 +607,7 @@ cudaError_t launch_compress_mma(const CompressArgs& a, int block, int variant, i
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, mma_kernel(block, variant), map_x, map_codes, a);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, mma_kernel(block, variant, fmt), map_x, map_codes, a);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -13,9 +13,10 @@
 // P stages, one per shard; lane 0 keeps
 // kDecompressStages stages in flight, each a pair of 1-D cp.async.bulk
 // copies (the tile's codes and its (alpha, s) pairs) completed on one mbarrier.
-// Codes are decoded in pairs with cvt.rn.f16x2.e4m3x2 and accumulated with
-// packed f32x2 FMAs; the bf16 output tile is assembled in shared memory and
-// leaves as one TMA bulk store.
+// Codes are decoded in pairs with cvt.rn.f16x2.e4m3x2 (FMT 0) or, for the
+// INT8 fallback format (FMT 1, pt summary §5), by placing the byte under a
+// fixed exponent, and accumulated with packed f32x2 FMAs; the bf16 output
+// tile is assembled in shared memory and leaves as one TMA bulk store.
 
 #include "taco_device.cuh"
 #include "taco_launch.h"
@@ -39,7 +40,12 @@ constexpr uint32_t kOutBytes = kTileElems * 2;        // bf16 output of one tile
 // sum x_hat^2 = n sum z^2 (H symmetric, H H = n I), so alpha' = sqrt(E* /
 // sum z^2), the rotated block is alpha' sqrt(n) z and no transform is
 // needed; the bf16 sum is written too when `out` is not null.
-template <int NB, int MODE, int VARIANT>
+template <int FMT>
+__device__ __forceinline__ f2 decode2(uint32_t two_codes) {
+  return FMT == 0 ? e4m3x2_to_f2(two_codes) : i8x2_to_f2(two_codes);
+}
+
+template <int NB, int MODE, int VARIANT, int FMT = 0>
 __global__ void __launch_bounds__(kDecompressThreads, kDecompressMinBlocks)
 decompress_reduce_kernel(DecompressArgs a) {
   constexpr int LPB = NB / 64;
@@ -149,10 +155,10 @@ decompress_reduce_kernel(DecompressArgs a) {
       const f2 d2{d, d};
 #pragma unroll
       for (int q = 0; q < kCH; ++q) {
-        z[q][0] = fma2(d2, e4m3x2_to_f2(w[q].x & 0xffffu), z[q][0]);
-        z[q][1] = fma2(d2, e4m3x2_to_f2(w[q].x >> 16), z[q][1]);
-        z[q][2] = fma2(d2, e4m3x2_to_f2(w[q].y & 0xffffu), z[q][2]);
-        z[q][3] = fma2(d2, e4m3x2_to_f2(w[q].y >> 16), z[q][3]);
+        z[q][0] = fma2(d2, decode2<FMT>(w[q].x & 0xffffu), z[q][0]);
+        z[q][1] = fma2(d2, decode2<FMT>(w[q].x >> 16), z[q][1]);
+        z[q][2] = fma2(d2, decode2<FMT>(w[q].y & 0xffffu), z[q][2]);
+        z[q][3] = fma2(d2, decode2<FMT>(w[q].y >> 16), z[q][3]);
       }
     }
     if (!ok) break;
@@ -268,12 +274,17 @@ size_t decompress_smem_bytes() {
          (kDecompressStages * (kStageBytes + 8) + kOutBytes);
 }
 
-const void* decompress_kernel_ptr(int block) {
-  switch (block) {
-    case 64: return reinterpret_cast<const void*>(decompress_reduce_kernel<64, 0, 0>);
-    case 128: return reinterpret_cast<const void*>(decompress_reduce_kernel<128, 0, 0>);
-    default: return reinterpret_cast<const void*>(decompress_reduce_kernel<256, 0, 0>);
-  }
+namespace {
+template <int FMT>
+void (*decompress_fn(int block))(DecompressArgs) {
+  return block == 64    ? decompress_reduce_kernel<64, 0, 0, FMT>
+         : block == 128 ? decompress_reduce_kernel<128, 0, 0, FMT>
+                        : decompress_reduce_kernel<256, 0, 0, FMT>;
+}
+}  // namespace
+
+const void* decompress_kernel_ptr(int block, int fmt) {
+  return reinterpret_cast<const void*>(fmt == 0 ? decompress_fn<0>(block) : decompress_fn<1>(block));
 }
 
 namespace {
@@ -293,7 +304,8 @@ const void* recompress_kernel_ptr(int block, int variant) {
   }
 }
 
-cudaError_t launch_decompress(const DecompressArgs& a, int block, int grid, cudaStream_t stream) {
+cudaError_t launch_decompress(const DecompressArgs& a, int block, int fmt, int grid,
+                              cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kDecompressThreads);
@@ -304,9 +316,7 @@ cudaError_t launch_decompress(const DecompressArgs& a, int block, int grid, cuda
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  void (*kern)(DecompressArgs) = block == 64    ? decompress_reduce_kernel<64, 0, 0>
-                                 : block == 128 ? decompress_reduce_kernel<128, 0, 0>
-                                                : decompress_reduce_kernel<256, 0, 0>;
+  void (*kern)(DecompressArgs) = fmt == 0 ? decompress_fn<0>(block) : decompress_fn<1>(block);
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
   return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -22,9 +22,11 @@ inline bool valid_variant(int v) {
   return v == TACO_VARIANT_DUAL || v == TACO_VARIANT_ABSMAX || v == TACO_VARIANT_STATIC;
 }
 
-inline float static_scale(int block, float target_energy) {
-  return static_cast<float>(std::sqrt(static_cast<double>(block) * target_energy) / 448.0);
+inline float static_scale(int block, float target_energy, double q_max = 448.0) {
+  return static_cast<float>(std::sqrt(static_cast<double>(block) * target_energy) / q_max);
 }
+
+constexpr int kFormats = 2;   // 0 = FP8 E4M3, 1 = INT8 fallback
 
 inline int block_index(int block) { return block == 64 ? 0 : (block == 128 ? 1 : 2); }
 
@@ -46,10 +48,10 @@ taco_status check_shape(int64_t N, int64_t h, int block) {
 struct DeviceInfo {
   int sms = 0;
   int occ_compress[3][kVariants] = {};
-  int occ_decompress[3] = {};
+  int occ_decompress[3][kFormats] = {};
   int occ_recompress[3][kVariants] = {};
   int occ_gather[3] = {};
-  int occ_mma[3][kVariants] = {};
+  int occ_mma[3][kVariants][kFormats] = {};
 };
 
 std::once_flag g_once[kMaxDevices];
@@ -75,11 +77,11 @@ cudaError_t device_info(const DeviceInfo** out) {
           err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ_compress[b][v], k,
                                                               kCompressThreads, csmem);
       }
-      if (err == cudaSuccess) {
-        const void* k = decompress_kernel_ptr(blocks[b]);
+      for (int f = 0; f < kFormats && err == cudaSuccess; ++f) {
+        const void* k = decompress_kernel_ptr(blocks[b], f);
         err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dsmem);
         if (err == cudaSuccess)
-          err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ_decompress[b], k,
+          err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ_decompress[b][f], k,
                                                               kDecompressThreads, dsmem);
       }
       if (err == cudaSuccess) {
@@ -90,12 +92,14 @@ cudaError_t device_info(const DeviceInfo** out) {
                                                               kDecompressThreads, dsmem);
       }
       for (int v = 0; v < kVariants && err == cudaSuccess; ++v) {
-        const void* k = compress_mma_kernel_ptr(blocks[b], v);
-        const int msmem = static_cast<int>(compress_mma_smem_bytes(blocks[b]));
-        err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, msmem);
-        if (err == cudaSuccess)
-          err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ_mma[b][v], k,
-                                                              compress_mma_threads(blocks[b]), msmem);
+        for (int f = 0; f < kFormats && err == cudaSuccess; ++f) {
+          const void* k = compress_mma_kernel_ptr(blocks[b], v, f);
+          const int msmem = static_cast<int>(compress_mma_smem_bytes(blocks[b]));
+          err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, msmem);
+          if (err == cudaSuccess)
+            err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                &d.occ_mma[b][v][f], k, compress_mma_threads(blocks[b]), msmem);
+        }
       }
       for (int v = 0; v < kVariants && err == cudaSuccess; ++v) {
         const void* k = recompress_kernel_ptr(blocks[b], v);
@@ -126,7 +130,7 @@ Layout shard_layout(int64_t N, int64_t h, int block) {
 }
 
 taco_status decompress_common(const uint8_t* const* shards, int P, int64_t N, int64_t h,
-                              int block, void* out, void* stream) {
+                              int block, void* out, void* stream, int fmt = 0) {
   taco_status st = check_shape(N, h, block);
   if (st != TACO_OK) return st;
   if (P < 1 || P > TACO_MAX_SHARDS) return TACO_ERR_ARG;
@@ -152,10 +156,10 @@ taco_status decompress_common(const uint8_t* const* shards, int P, int64_t N, in
   if (device_info(&info) != cudaSuccess) return TACO_ERR_CUDA;
   const int64_t tiles = (a.nblocks + decompress_tile_blocks(block) - 1) / decompress_tile_blocks(block);
   const int64_t needed = (tiles + kDecompressThreads / 32 - 1) / (kDecompressThreads / 32);
-  int64_t grid = static_cast<int64_t>(info->sms) * info->occ_decompress[block_index(block)];
+  int64_t grid = static_cast<int64_t>(info->sms) * info->occ_decompress[block_index(block)][fmt];
   if (grid > needed) grid = needed;
   if (grid < 1) grid = 1;
-  if (launch_decompress(a, block, static_cast<int>(grid), static_cast<cudaStream_t>(stream)) !=
+  if (launch_decompress(a, block, fmt, static_cast<int>(grid), static_cast<cudaStream_t>(stream)) !=
       cudaSuccess)
     return TACO_ERR_CUDA;
   return TACO_OK;
@@ -293,6 +297,46 @@ taco_status compress_args(const void* x_bf16, int P, int64_t N, int64_t h, int b
   a.sqrt_nE = static_cast<float>(sqrt_nE);
   a.inv_sqrt_n = static_cast<float>(1.0 / std::sqrt(static_cast<double>(block)));
   a.s_static = static_scale(block, target_energy);
+  a.q_max = 448.0f;
+  return TACO_OK;
+}
+
+// The tensor-core compress for both code formats (0 = E4M3, 1 = INT8).
+taco_status compress_mma_common(const void* x_bf16, int P, int64_t N, int64_t h, int block,
+                                float target_energy, int variant, void* bundle_out,
+                                taco_header* headers_out, void* workspace, size_t workspace_bytes,
+                                void* stream, int fmt) {
+  CompressArgs a{};
+  taco_status st = compress_args(x_bf16, P, N, h, block, target_energy, variant, bundle_out,
+                                 headers_out, workspace, workspace_bytes, &a);
+  if (st != TACO_OK) return st;
+  if (a.nblocks > kMmaMaxBlocks) return TACO_ERR_SHAPE;
+  const double n_sqrtE = block * std::sqrt(static_cast<double>(target_energy));   // finite
+  a.n_sqrtE = static_cast<float>(n_sqrtE);
+  if (fmt == 1) {
+    a.s_static = static_scale(block, target_energy, 127.0);
+    a.q_max = 127.0f;
+  }
+
+  const DeviceInfo* info = nullptr;
+  if (device_info(&info) != cudaSuccess) return TACO_ERR_CUDA;
+  if (N == 0) {
+    // nothing to rotate or encode: one CTA per shard of the CUDA-core kernel
+    // writes the headers (its code loop is empty)
+    return launch_compress(a, block, variant, 1, P, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? TACO_OK
+               : TACO_ERR_CUDA;
+  }
+  const int occ = info->occ_mma[block_index(block)][variant][fmt];
+  if (occ < 1) return TACO_ERR_CUDA;
+  const int64_t tiles = (a.nblocks + 127) / 128;
+  int64_t gx = static_cast<int64_t>(info->sms) * occ / P;
+  if (gx > tiles) gx = tiles;
+  if (gx > kMaxCtasPerShard) gx = kMaxCtasPerShard;
+  if (gx < 1) gx = 1;
+  if (launch_compress_mma(a, block, variant, fmt, static_cast<int>(gx), P,
+                          static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return TACO_ERR_CUDA;
   return TACO_OK;
 }
 
@@ -322,30 +366,16 @@ taco_status taco_compress_shards_mma(const void* x_bf16, int P, int64_t N, int64
                                      float target_energy, int variant, void* bundle_out,
                                      taco_header* headers_out, void* workspace,
                                      size_t workspace_bytes, void* stream) {
-  CompressArgs a{};
-  taco_status st = compress_args(x_bf16, P, N, h, block, target_energy, variant, bundle_out,
-                                 headers_out, workspace, workspace_bytes, &a);
-  if (st != TACO_OK) return st;
-  if (a.nblocks > kMmaMaxBlocks) return TACO_ERR_SHAPE;
-  const double n_sqrtE = block * std::sqrt(static_cast<double>(target_energy));   // finite
-  if (N == 0)   // nothing to rotate: the headers as the CUDA-core path writes them
-    return taco_compress_shards(x_bf16, P, N, h, block, target_energy, variant, bundle_out,
-                                headers_out, workspace, workspace_bytes, stream);
-  a.n_sqrtE = static_cast<float>(n_sqrtE);
+  return compress_mma_common(x_bf16, P, N, h, block, target_energy, variant, bundle_out,
+                             headers_out, workspace, workspace_bytes, stream, 0);
+}
 
-  const DeviceInfo* info = nullptr;
-  if (device_info(&info) != cudaSuccess) return TACO_ERR_CUDA;
-  const int occ = info->occ_mma[block_index(block)][variant];
-  if (occ < 1) return TACO_ERR_CUDA;
-  const int64_t tiles = (a.nblocks + 127) / 128;
-  int64_t gx = static_cast<int64_t>(info->sms) * occ / P;
-  if (gx > tiles) gx = tiles;
-  if (gx > kMaxCtasPerShard) gx = kMaxCtasPerShard;
-  if (gx < 1) gx = 1;
-  if (launch_compress_mma(a, block, variant, static_cast<int>(gx), P,
-                          static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return TACO_ERR_CUDA;
-  return TACO_OK;
+taco_status taco_compress_shards_int8(const void* x_bf16, int P, int64_t N, int64_t h, int block,
+                                      float target_energy, int variant, void* bundle_out,
+                                      taco_header* headers_out, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+  return compress_mma_common(x_bf16, P, N, h, block, target_energy, variant, bundle_out,
+                             headers_out, workspace, workspace_bytes, stream, 1);
 }
 
 taco_status taco_compress_shards(const void* x_bf16, int P, int64_t N, int64_t h, int block,
@@ -391,6 +421,19 @@ taco_status taco_decompress_reduce(const void* bundle, int P, int64_t N, int64_t
   const uint8_t* ptrs[TACO_MAX_SHARDS];
   for (int p = 0; p < P; ++p) ptrs[p] = static_cast<const uint8_t*>(bundle) + p * sb;
   return decompress_common(ptrs, P, N, h, block, out_bf16, stream);
+}
+
+taco_status taco_decompress_reduce_int8(const void* bundle, int P, int64_t N, int64_t h, int block,
+                                        void* out_bf16, void* stream) {
+  taco_status st = check_shape(N, h, block);
+  if (st != TACO_OK) return st;
+  if (P < 1 || P > TACO_MAX_SHARDS) return TACO_ERR_ARG;
+  if (N == 0) return TACO_OK;
+  if (!bundle) return TACO_ERR_NULL;
+  const size_t sb = shard_layout(N, h, block).bytes;
+  const uint8_t* ptrs[TACO_MAX_SHARDS];
+  for (int p = 0; p < P; ++p) ptrs[p] = static_cast<const uint8_t*>(bundle) + p * sb;
+  return decompress_common(ptrs, P, N, h, block, out_bf16, stream, 1);
 }
 
 taco_status taco_decompress_reduce_ptrs(const void* const* shards, int P, int64_t N, int64_t h,

@@ -109,6 +109,23 @@ __device__ __forceinline__ f2 e4m3x2_to_f2(uint32_t two_codes) {
   return f2{f.x, f.y};
 }
 
+// ------------------------------------------------------ INT8 fallback ----
+// Signed-byte codes of the INT8 fallback format: q = round-half-even(y) for
+// |y| <= 127 (the scales keep every y in that range). Adding 1.5 * 2^23 to a
+// float of magnitude below 2^22 rounds it to an integer k (round to nearest
+// even, one fp32 add) and leaves k in the low mantissa bits in two's
+// complement, so the low byte is the code.
+constexpr float kI8Round = 12582912.0f;   // 1.5 * 2^23
+
+// Four scaled values -> four codes in one word, element 0 in the low byte.
+__device__ __forceinline__ uint32_t i8x4_from_f32(f2 y01, f2 y23);
+
+// Two codes (low byte first, in the low 16 bits) -> two exact fp32 values:
+// the byte with its sign bit flipped is k + 128 in 0..255; placed under the
+// exponent of 1.5 * 2^23 it reads 1.5 * 2^23 + k + 128, and one packed
+// subtraction leaves k.
+__device__ __forceinline__ f2 i8x2_to_f2(uint32_t two_codes);
+
 // ------------------------------------------------- shared memory / TMA ----
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -363,7 +380,7 @@ __device__ __forceinline__ float block_max(float v) {
 template <int THREADS>
 __device__ void finish_header(float part_smax, uint32_t part_cnt, uint8_t* ws_shard,
                               taco_header* hd, int64_t N, int64_t h, int block, int variant,
-                              float target_energy) {
+                              float target_energy, float q_max = 448.0f) {
   constexpr int WARPS = THREADS / 32;
   __shared__ float sh_max[WARPS];
   __shared__ uint32_t sh_cnt[WARPS];
@@ -425,11 +442,26 @@ __device__ void finish_header(float part_smax, uint32_t part_cnt, uint8_t* ws_sh
     hd->block = block;
     hd->variant = variant;
     hd->target_energy = target_energy;
-    hd->q_max = 448.0f;
+    hd->q_max = q_max;
     hd->s_max = m;
     hd->n_clamped = n;
     *counter = 0u;   // leave the workspace zero-filled for the next call
   }
+}
+
+__device__ __forceinline__ uint32_t i8x4_from_f32(f2 y01, f2 y23) {
+  const f2 m{kI8Round, kI8Round};
+  const f2 r01 = add2(y01, m), r23 = add2(y23, m);
+  const uint32_t lo = __byte_perm(__float_as_uint(r01.x), __float_as_uint(r01.y), 0x0040);
+  const uint32_t hi = __byte_perm(__float_as_uint(r23.x), __float_as_uint(r23.y), 0x0040);
+  return __byte_perm(lo, hi, 0x5410);
+}
+
+__device__ __forceinline__ f2 i8x2_to_f2(uint32_t two_codes) {
+  const uint32_t t = two_codes ^ 0x8080u;
+  const f2 v{__uint_as_float(__byte_perm(t, 0x4B400000u, 0x7650)),
+             __uint_as_float(__byte_perm(t, 0x4B400000u, 0x7651))};
+  return sub2(v, f2{kI8Round + 128.0f, kI8Round + 128.0f});
 }
 
 __device__ __forceinline__ float max3(float a, float b, float c) {

@@ -45,6 +45,7 @@ struct CompressArgs {
   float inv_sqrt_n;         // fp32(1 / sqrt(block))
   float s_static;           // fp32(sqrt(block * E*) / 448), STATIC variant
   float n_sqrtE;            // fp32(block * sqrt(E*)), tensor-core compress
+  float q_max;              // largest code magnitude written to the headers (448 or 127)
 };
 
 struct DecompressArgs {
@@ -74,15 +75,17 @@ cudaError_t launch_compress(const CompressArgs& a, int block, int variant, int g
 cudaError_t compress_fault(unsigned int* bits, bool clear);
 
 size_t compress_mma_smem_bytes(int block);
-const void* compress_mma_kernel_ptr(int block, int variant);
-cudaError_t launch_compress_mma(const CompressArgs& a, int block, int variant, int grid_x, int P,
-                                cudaStream_t stream);
+// fmt: 0 = FP8 E4M3 codes, 1 = INT8 fallback codes
+const void* compress_mma_kernel_ptr(int block, int variant, int fmt);
+cudaError_t launch_compress_mma(const CompressArgs& a, int block, int variant, int fmt, int grid_x,
+                                int P, cudaStream_t stream);
 cudaError_t compress_mma_fault(unsigned int* bits, bool clear);
 
 int decompress_tile_blocks(int block);
 size_t decompress_smem_bytes();
-const void* decompress_kernel_ptr(int block);
-cudaError_t launch_decompress(const DecompressArgs& a, int block, int grid, cudaStream_t stream);
+const void* decompress_kernel_ptr(int block, int fmt);
+cudaError_t launch_decompress(const DecompressArgs& a, int block, int fmt, int grid,
+                              cudaStream_t stream);
 const void* recompress_kernel_ptr(int block, int variant);
 const void* gather_kernel_ptr(int block);
 cudaError_t launch_decompress_shards(const DecompressArgs& a, int block, int grid, int P,

@@ -183,6 +183,26 @@ taco_status taco_compress_shards_noalloc(const void* x_bf16, int P, int64_t N, i
 taco_status taco_decompress_reduce(const void* bundle, int P, int64_t N, int64_t h,
                                    int block, void* out_bf16, void* stream);
 
+/* ---- INT8 fallback format -------------------------------------------------
+ * TACO pt summary §5 ("Agnóstico de Hardware"): the framework degrades to
+ * INT8 on hardware without FP8 support. The pages define no INT8 format
+ * beyond the uniform steps of §2.A; these entries take the plainest reading:
+ * every step of the operator as above, with the code of a rotated value y
+ * being q = round-half-to-even(y / s) as a signed byte (two's complement,
+ * never -128) and Q_max = 127 in place of 448 in the scale rules (DUAL:
+ * s = max(1, max|y| / 127); ABSMAX: s = max|y| / 127; STATIC:
+ * s = sqrt(block * E*) / 127). The headers report q_max = 127. Same shard
+ * layout, arguments, workspace and errors as taco_compress_shards_mma /
+ * taco_decompress_reduce; the rotation runs on the tensor cores. A bundle
+ * must be decompressed with the entry of its format. */
+taco_status taco_compress_shards_int8(const void* x_bf16, int P, int64_t N, int64_t h,
+                                      int block, float target_energy, int variant,
+                                      void* bundle_out, taco_header* headers_out,
+                                      void* workspace, size_t workspace_bytes,
+                                      void* stream);
+taco_status taco_decompress_reduce_int8(const void* bundle, int P, int64_t N, int64_t h,
+                                        int block, void* out_bf16, void* stream);
+
 /* ---- taco_decompress_reduce_ptrs ----------------------------------------
  * As taco_decompress_reduce, with the P shards in P separate buffers
  * (`shards[p]` a device pointer to one shard, 16-byte aligned; `shards` itself

@@ -37,6 +37,19 @@ def compare_codes(got: np.ndarray, want: np.ndarray, what: str = "codes") -> dic
     return {"equal_fraction": frac, "max_steps": worst}
 
 
+def compare_int8_codes(got: np.ndarray, want: np.ndarray, what: str = "int8 codes") -> dict:
+    """INT8 fallback codes: the same bar, steps of one integer."""
+    og = np.asarray(got, dtype=np.uint8).view(np.int8).astype(np.int64)
+    ow = np.asarray(want, dtype=np.uint8).view(np.int8).astype(np.int64)
+    assert og.shape == ow.shape, (what, og.shape, ow.shape)
+    diff = np.abs(og - ow)
+    frac = float(np.mean(diff == 0)) if diff.size else 1.0
+    worst = int(diff.max()) if diff.size else 0
+    assert frac >= CODE_EQUAL_FRACTION, f"{what}: only {frac:.6%} equal"
+    assert worst <= 1, f"{what}: codes differ by {worst}"
+    return {"equal_fraction": frac, "max_steps": worst}
+
+
 def compare_scales(got: np.ndarray, want: np.ndarray, what: str) -> float:
     got = np.asarray(got, dtype=np.float64)
     want = np.asarray(want, dtype=np.float64)
