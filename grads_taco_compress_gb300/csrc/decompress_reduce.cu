@@ -40,9 +40,15 @@ constexpr uint32_t kOutBytes = kTileElems * 2;        // bf16 output of one tile
 // sum x_hat^2 = n sum z^2 (H symmetric, H H = n I), so alpha' = sqrt(E* /
 // sum z^2), the rotated block is alpha' sqrt(n) z and no transform is
 // needed; the bf16 sum is written too when `out` is not null.
+// Four codes of one 32-bit word -> (elements 0, 1), (elements 2, 3).
 template <int FMT>
-__device__ __forceinline__ f2 decode2(uint32_t two_codes) {
-  return FMT == 0 ? e4m3x2_to_f2(two_codes) : i8x2_to_f2(two_codes);
+__device__ __forceinline__ void decode4(uint32_t w, f2& v01, f2& v23) {
+  if constexpr (FMT == 0) {
+    v01 = e4m3x2_to_f2(w & 0xffffu);
+    v23 = e4m3x2_to_f2(w >> 16);
+  } else {
+    i8x4_to_f32(w, v01, v23);
+  }
 }
 
 template <int NB, int MODE, int VARIANT, int FMT = 0>
@@ -155,10 +161,13 @@ decompress_reduce_kernel(DecompressArgs a) {
       const f2 d2{d, d};
 #pragma unroll
       for (int q = 0; q < kCH; ++q) {
-        z[q][0] = fma2(d2, decode2<FMT>(w[q].x & 0xffffu), z[q][0]);
-        z[q][1] = fma2(d2, decode2<FMT>(w[q].x >> 16), z[q][1]);
-        z[q][2] = fma2(d2, decode2<FMT>(w[q].y & 0xffffu), z[q][2]);
-        z[q][3] = fma2(d2, decode2<FMT>(w[q].y >> 16), z[q][3]);
+        f2 c0, c1, c2, c3;
+        decode4<FMT>(w[q].x, c0, c1);
+        decode4<FMT>(w[q].y, c2, c3);
+        z[q][0] = fma2(d2, c0, z[q][0]);
+        z[q][1] = fma2(d2, c1, z[q][1]);
+        z[q][2] = fma2(d2, c2, z[q][2]);
+        z[q][3] = fma2(d2, c3, z[q][3]);
       }
     }
     if (!ok) break;

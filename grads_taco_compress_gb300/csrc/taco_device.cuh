@@ -120,11 +120,11 @@ constexpr float kI8Round = 12582912.0f;   // 1.5 * 2^23
 // Four scaled values -> four codes in one word, element 0 in the low byte.
 __device__ __forceinline__ uint32_t i8x4_from_f32(f2 y01, f2 y23);
 
-// Two codes (low byte first, in the low 16 bits) -> two exact fp32 values:
-// the byte with its sign bit flipped is k + 128 in 0..255; placed under the
+// Four codes (element 0 in the low byte) -> four exact fp32 values: the
+// byte with its sign bit flipped is k + 128 in 0..255; placed under the
 // exponent of 1.5 * 2^23 it reads 1.5 * 2^23 + k + 128, and one packed
-// subtraction leaves k.
-__device__ __forceinline__ f2 i8x2_to_f2(uint32_t two_codes);
+// subtraction per pair leaves k.
+__device__ __forceinline__ void i8x4_to_f32(uint32_t four_codes, f2& v01, f2& v23);
 
 // ------------------------------------------------- shared memory / TMA ----
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -457,11 +457,13 @@ __device__ __forceinline__ uint32_t i8x4_from_f32(f2 y01, f2 y23) {
   return __byte_perm(lo, hi, 0x5410);
 }
 
-__device__ __forceinline__ f2 i8x2_to_f2(uint32_t two_codes) {
-  const uint32_t t = two_codes ^ 0x8080u;
-  const f2 v{__uint_as_float(__byte_perm(t, 0x4B400000u, 0x7650)),
-             __uint_as_float(__byte_perm(t, 0x4B400000u, 0x7651))};
-  return sub2(v, f2{kI8Round + 128.0f, kI8Round + 128.0f});
+__device__ __forceinline__ void i8x4_to_f32(uint32_t four_codes, f2& v01, f2& v23) {
+  const uint32_t t = four_codes ^ 0x80808080u;
+  const f2 off{kI8Round + 128.0f, kI8Round + 128.0f};
+  v01 = sub2(f2{__uint_as_float(__byte_perm(t, 0x4B400000u, 0x7650)),
+                __uint_as_float(__byte_perm(t, 0x4B400000u, 0x7651))}, off);
+  v23 = sub2(f2{__uint_as_float(__byte_perm(t, 0x4B400000u, 0x7652)),
+                __uint_as_float(__byte_perm(t, 0x4B400000u, 0x7653))}, off);
 }
 
 __device__ __forceinline__ float max3(float a, float b, float c) {
