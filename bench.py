@@ -372,6 +372,19 @@ def run_taco(args, w) -> None:
     t_ci = region(lambda i: compress_int8(i % R))
     t_di = region(lambda i: decompress_int8(i % R, (i + 1) % R))
 
+    # decompress-reduce with the inverse rotation on the tensor cores
+    # (block 64 and 128), on the step's own bundles
+    t_dm = None
+    if n in (64, 128):
+        def decompress_mma(k, src):
+            st = lib.taco_decompress_reduce_mma(bp[src], P, N, h, n, op[k], sptr)
+            if st:
+                raise taco.TacoError(st, "taco_decompress_reduce_mma")
+
+        for k in range(3):
+            decompress_mma(k % R, (k + 1) % R)
+        t_dm = region(lambda i: decompress_mma(i % R, (i + 1) % R))
+
     # The whole compressed two-shot AllReduce among P logical ranks (the P
     # input tensors of the step), captured in a CUDA graph and replayed.
     from grads_taco_compress_gb300.allreduce import EmulatedTwoShotAllReduce
@@ -446,6 +459,12 @@ def run_taco(args, w) -> None:
                                        "frac": round(d_bytes / t_di / 1e9 / hbm, 4),
                                        "impl": "INT8 fallback codes, not in the timed step"},
         }
+        if t_dm is not None:
+            kern["decompress_reduce_mma"] = {
+                "us": round(t_dm * 1e6, 3), "alg_bytes": d_bytes,
+                "hbm_gbs": round(d_bytes / t_dm / 1e9, 1),
+                "frac": round(d_bytes / t_dm / 1e9 / hbm, 4),
+                "impl": "tcgen05 E4M3 tensor-core inverse rotation, not in the timed step"}
         kern["emulated_two_shot_allreduce"] = {
             "us": round(t_ar * 1e6, 3), "ranks": P, "tensor": [N, h], "launches": ar.launches(),
             "algbw_gbs": round(N * h * 2 / t_ar / 1e9, 1),

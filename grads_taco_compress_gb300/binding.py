@@ -39,6 +39,7 @@ EXPORTED_SYMBOLS = (
     "taco_workspace_bytes", "taco_compress", "taco_compress_shards",
     "taco_compress_shards_noalloc", "taco_compress_shards_mma",
     "taco_compress_shards_int8", "taco_decompress_reduce_int8",
+    "taco_decompress_reduce_mma", "taco_decompress_reduce_mma_ptrs",
     "taco_decompress_reduce", "taco_decompress_reduce_ptrs",
     "taco_reduce_recompress", "taco_reduce_recompress_ptrs",
     "taco_decompress_shards", "taco_decompress_shards_ptrs",
@@ -78,6 +79,8 @@ def _lib() -> ctypes.CDLL:
             "taco_compress_shards_mma": (i32, [vp, i32, i64, i64, i32, f32, i32, vp, vp, vp, sz, vp]),
             "taco_compress_shards_int8": (i32, [vp, i32, i64, i64, i32, f32, i32, vp, vp, vp, sz, vp]),
             "taco_decompress_reduce_int8": (i32, [vp, i32, i64, i64, i32, vp, vp]),
+            "taco_decompress_reduce_mma": (i32, [vp, i32, i64, i64, i32, vp, vp]),
+            "taco_decompress_reduce_mma_ptrs": (i32, [ctypes.POINTER(vp), i32, i64, i64, i32, vp, vp]),
             "taco_decompress_reduce": (i32, [vp, i32, i64, i64, i32, vp, vp]),
             "taco_decompress_reduce_ptrs": (i32, [ctypes.POINTER(vp), i32, i64, i64, i32, vp, vp]),
             "taco_decompress_shards": (i32, [vp, i32, i64, i64, i32, vp, vp]),
@@ -266,6 +269,24 @@ def taco_compress_shards_int8(x: torch.Tensor, block: int, target_energy: float 
     """taco_compress_shards_mma with INT8 fallback codes (Q_max 127)."""
     return _compress_shards("taco_compress_shards_int8", x, block, target_energy, variant, bundle,
                             headers, workspace, stream)
+
+
+def taco_decompress_reduce_mma(bundle: torch.Tensor, P: int, N: int, h: int, block: int,
+                               out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """taco_decompress_reduce with the inverse rotation on the tensor cores (block 64, 128)."""
+    return _decompress_reduce("taco_decompress_reduce_mma", bundle, P, N, h, block, out, stream)
+
+
+def taco_decompress_reduce_mma_ptrs(shards, N: int, h: int, block: int,
+                                    out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """taco_decompress_reduce_mma with P separate shard tensors."""
+    P = len(shards)
+    if out is None:
+        out = torch.empty((N, h), dtype=torch.bfloat16, device=shards[0].device)
+    arr = (ctypes.c_void_p * max(P, 1))(*[_ptr(s) for s in shards])
+    st = _lib().taco_decompress_reduce_mma_ptrs(arr, P, N, h, block, _ptr(out), _stream_ptr(stream))
+    _check(st, "taco_decompress_reduce_mma_ptrs")
+    return out
 
 
 def taco_decompress_reduce_int8(bundle: torch.Tensor, P: int, N: int, h: int, block: int,

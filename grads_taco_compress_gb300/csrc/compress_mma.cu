@@ -40,10 +40,8 @@
 #include <cmath>
 #include <mutex>
 
-#include <cuda.h>
-
-#include "taco_device.cuh"
 #include "taco_launch.h"
+#include "tcgen05.cuh"
 
 namespace taco {
 
@@ -79,129 +77,16 @@ struct Smem {
   static constexpr uint32_t bytes = end + 1024;                     // + alignment slack
 };
 
-// ------------------------------------------------------------- tcgen05 ----
-__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-               :: "r"(slot), "r"(ncols) : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(ncols)
-               : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
+// Instruction descriptor: bf16 A and B, fp32 D, M = 128, N = 64.
+constexpr uint32_t kIdesc = instr_desc(1, kRows, 64);
 
-// Shared-memory matrix descriptor of a K-major operand stored in the
-// 128-byte swizzle layout: 8-row groups of 128-byte rows, 1024 bytes apart.
-//   bits  0-13 start address >> 4      bits 16-29 leading offset >> 4 (unused)
-//   bits 32-45 stride offset >> 4      bits 46-48 0b001 (descriptor version)
-//   bits 49-51 base offset (0: atoms 1024-byte aligned)
-//   bits 61-63 swizzle mode, 2 = 128-byte swizzle
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (uint64_t{1} << 16) |
-         (uint64_t{1024 >> 4} << 32) | (uint64_t{1} << 46) | (uint64_t{2} << 61);
+  return umma_desc(saddr, kSwizzle128, 1024);
 }
 
-// Instruction descriptor of kind::f16: D f32 (bits 4-5 = 1), A and B bf16
-// (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits
-// 17-22, M >> 4 at bits 24-28.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((64u >> 3) << 17) |
-                            ((static_cast<uint32_t>(kRows) >> 4) << 24);
-
-// D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
-      :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate) : "memory");
-}
-// The barrier at `bar` completes one arrival once every MMA this thread has
-// issued so far has completed.
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-               :: "r"(bar) : "memory");
-}
-
-// 16 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-__device__ __forceinline__ void tmem_wait_ld() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-// Keeps the compiler from using registers of a tcgen05.ld before the wait.
-__device__ __forceinline__ void reg_fence16(float* v) {
-  asm volatile(""
-               : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]),
-                 "+f"(v[6]), "+f"(v[7]), "+f"(v[8]), "+f"(v[9]), "+f"(v[10]), "+f"(v[11]),
-                 "+f"(v[12]), "+f"(v[13]), "+f"(v[14]), "+f"(v[15]));
-}
-
-// ------------------------------------------------------------ TMA tiles ----
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
-                                            int c2, uint32_t bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;"
-      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar),
-         "l"(policy)
-      : "memory");
-}
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1,
-                                             int c2) {
-  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];"
-               :: "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(src)
-               : "memory");
-}
-__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
-  asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-
-// ------------------------------------------------------ waits and votes ----
-// Wait for phase `parity` of `bar`. Gives up when the CTA's abort flag is set
-// or after kWaitLimitNs; the timed-out waiter sets the flag and the fault bit.
-__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
-                                              volatile uint32_t* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer_ns();
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
-      *abort_flag = 1u;
-      atomicOr(&g_compress_mma_fault, kFaultCompressMmaWait);
-      return false;
-    }
-  }
-}
-
-// Barrier over the 128 threads of epilogue group `id`; true in every thread
-// if `pred` held in any of them.
-__device__ __forceinline__ bool group_any(int id, bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, 128, p;\n"
-      " selp.u32 %0, 1, 0, q;\n}"
-      : "=r"(r) : "r"(static_cast<uint32_t>(pred)), "r"(id) : "memory");
-  return r != 0;
-}
-__device__ __forceinline__ void group_sync(int id) {
-  asm volatile("bar.sync %0, 128;" :: "r"(id) : "memory");
+__device__ __forceinline__ bool wait_here(uint32_t bar, uint32_t parity,
+                                          volatile uint32_t* abort_flag) {
+  return wait_or_abort(bar, parity, abort_flag, &g_compress_mma_fault, kFaultCompressMmaWait);
 }
 
 // ------------------------------------------------------------- epilogue ----
@@ -367,7 +252,7 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
         const int row0 = static_cast<int>((blockIdx.x + k * G) * kRows);
         for (int c = 0; c < NC; ++c, ++i) {
           const uint32_t s = i % kStages, ph = (i / kStages) & 1u;
-          if (!wait_or_abort(base + S::empty + 8 * s, ph ^ 1u, abort_flag)) {
+          if (!wait_here(base + S::empty + 8 * s, ph ^ 1u, abort_flag)) {
             ok = false;
             break;
           }
@@ -392,11 +277,11 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
       for (int k = 0; k < count && ok; ++k) {
         const int g = k % NG;
         const uint32_t use = static_cast<uint32_t>(k / NG);
-        if (!wait_or_abort(base + S::tempty + 8 * g, (use & 1u) ^ 1u, abort_flag)) break;
+        if (!wait_here(base + S::tempty + 8 * g, (use & 1u) ^ 1u, abort_flag)) break;
         tc_fence_after();
         for (int c = 0; c < NC; ++c, ++i) {
           const uint32_t s = i % kStages, ph = (i / kStages) & 1u;
-          if (!wait_or_abort(base + S::full + 8 * s, ph, abort_flag)) {
+          if (!wait_here(base + S::full + 8 * s, ph, abort_flag)) {
             ok = false;
             break;
           }
@@ -405,8 +290,8 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
           const uint32_t atile = base + S::stages + s * kAtomBytes;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_bf16(d, sw128_desc(atile + 32 * kk), sw128_desc(base + S::hmat + 32 * kk),
-                     kk > 0 ? 1u : 0u);
+            mma_f16(d, sw128_desc(atile + 32 * kk), sw128_desc(base + S::hmat + 32 * kk), kIdesc,
+                    kk > 0 ? 1u : 0u);
           mma_commit(base + S::empty + 8 * s);   // the stage is free once these MMAs are done
         }
         if (ok) mma_commit(base + S::tfull + 8 * g);
@@ -430,7 +315,7 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
 
     for (int k = g; k < count; k += NG) {
       const uint32_t use = static_cast<uint32_t>(k / NG);
-      const bool got = wait_or_abort(base + S::tfull + 8 * g, use & 1u, abort_flag);
+      const bool got = wait_here(base + S::tfull + 8 * g, use & 1u, abort_flag);
       if (leader) bulk_wait_read<0>();           // the group's last store has read the staging
       if (group_any(1 + g, !got || *abort_flag != 0u)) break;
       tc_fence_after();
@@ -540,28 +425,21 @@ void (*mma_kernel(int block, int variant, int fmt))(CUtensorMap, CUtensorMap, Co
   return fmt == 0 ? mma_kernel_fmt<0>(block, variant) : mma_kernel_fmt<1>(block, variant);
 }
 
-// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
-// against the driver library).
-using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-std::once_flag g_encode_once;
-EncodeTiled g_encode = nullptr;
+}  // namespace
 
-EncodeTiled encoder() {
-  std::call_once(g_encode_once, []() {
-    void* fn = nullptr;
+EncodeTiled tensor_map_encoder() {
+  static std::once_flag once;
+  static EncodeTiled fn = nullptr;
+  std::call_once(once, []() {
+    void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      g_encode = reinterpret_cast<EncodeTiled>(fn);
+      fn = reinterpret_cast<EncodeTiled>(p);
   });
-  return g_encode;
+  return fn;
 }
-
-}  // namespace
 
 size_t compress_mma_smem_bytes(int block) {
   return block == 64 ? Smem<64>::bytes : block == 128 ? Smem<128>::bytes : Smem<256>::bytes;
@@ -573,7 +451,7 @@ const void* compress_mma_kernel_ptr(int block, int variant, int fmt) {
 
 cudaError_t launch_compress_mma(const CompressArgs& a, int block, int variant, int fmt, int grid_x,
                                 int P, cudaStream_t stream) {
-  EncodeTiled encode = encoder();
+  EncodeTiled encode = tensor_map_encoder();
   if (!encode) return cudaErrorNotSupported;
   // x viewed as [P][nblocks][block] bf16; one box = one chunk of 128 blocks.
   CUtensorMap map_x, map_codes;

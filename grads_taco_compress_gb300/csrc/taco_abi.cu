@@ -52,6 +52,7 @@ struct DeviceInfo {
   int occ_recompress[3][kVariants] = {};
   int occ_gather[3] = {};
   int occ_mma[3][kVariants][kFormats] = {};
+  int occ_dmma[2] = {};   // tensor-core decompress, block 64 and 128
 };
 
 std::once_flag g_once[kMaxDevices];
@@ -101,6 +102,13 @@ cudaError_t device_info(const DeviceInfo** out) {
                 &d.occ_mma[b][v][f], k, compress_mma_threads(blocks[b]), msmem);
         }
       }
+      if (err == cudaSuccess && b < 2) {
+        const void* k = decompress_mma_kernel_ptr(blocks[b]);
+        const int msmem = static_cast<int>(decompress_mma_smem_bytes(blocks[b]));
+        err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, msmem);
+        if (err == cudaSuccess)
+          err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ_dmma[b], k, 320, msmem);
+      }
       for (int v = 0; v < kVariants && err == cudaSuccess; ++v) {
         const void* k = recompress_kernel_ptr(blocks[b], v);
         err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dsmem);
@@ -130,7 +138,7 @@ Layout shard_layout(int64_t N, int64_t h, int block) {
 }
 
 taco_status decompress_common(const uint8_t* const* shards, int P, int64_t N, int64_t h,
-                              int block, void* out, void* stream, int fmt = 0) {
+                              int block, void* out, void* stream, int fmt = 0, bool mma = false) {
   taco_status st = check_shape(N, h, block);
   if (st != TACO_OK) return st;
   if (P < 1 || P > TACO_MAX_SHARDS) return TACO_ERR_ARG;
@@ -154,6 +162,19 @@ taco_status decompress_common(const uint8_t* const* shards, int P, int64_t N, in
 
   const DeviceInfo* info = nullptr;
   if (device_info(&info) != cudaSuccess) return TACO_ERR_CUDA;
+  if (mma) {
+    if (a.nblocks > kMmaMaxBlocks) return TACO_ERR_SHAPE;
+    const int occ = info->occ_dmma[block_index(block)];
+    if (occ < 1) return TACO_ERR_CUDA;
+    int64_t grid = static_cast<int64_t>(info->sms) * occ;
+    const int64_t tiles = (a.nblocks + 127) / 128;
+    if (grid > tiles) grid = tiles;
+    if (grid < 1) grid = 1;
+    return launch_decompress_mma(a, block, static_cast<int>(grid), static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? TACO_OK
+               : TACO_ERR_CUDA;
+  }
   const int64_t tiles = (a.nblocks + decompress_tile_blocks(block) - 1) / decompress_tile_blocks(block);
   const int64_t needed = (tiles + kDecompressThreads / 32 - 1) / (kDecompressThreads / 32);
   int64_t grid = static_cast<int64_t>(info->sms) * info->occ_decompress[block_index(block)][fmt];
@@ -436,6 +457,33 @@ taco_status taco_decompress_reduce_int8(const void* bundle, int P, int64_t N, in
   return decompress_common(ptrs, P, N, h, block, out_bf16, stream, 1);
 }
 
+taco_status taco_decompress_reduce_mma(const void* bundle, int P, int64_t N, int64_t h, int block,
+                                       void* out_bf16, void* stream) {
+  taco_status st = check_shape(N, h, block);
+  if (st != TACO_OK) return st;
+  if (block == 256) return TACO_ERR_BLOCK;
+  if (P < 1 || P > TACO_MAX_SHARDS) return TACO_ERR_ARG;
+  if (N == 0) return TACO_OK;
+  if (!bundle) return TACO_ERR_NULL;
+  const size_t sb = shard_layout(N, h, block).bytes;
+  const uint8_t* ptrs[TACO_MAX_SHARDS];
+  for (int p = 0; p < P; ++p) ptrs[p] = static_cast<const uint8_t*>(bundle) + p * sb;
+  return decompress_common(ptrs, P, N, h, block, out_bf16, stream, 0, true);
+}
+
+taco_status taco_decompress_reduce_mma_ptrs(const void* const* shards, int P, int64_t N, int64_t h,
+                                            int block, void* out_bf16, void* stream) {
+  taco_status st = check_shape(N, h, block);
+  if (st != TACO_OK) return st;
+  if (block == 256) return TACO_ERR_BLOCK;
+  if (P < 1 || P > TACO_MAX_SHARDS) return TACO_ERR_ARG;
+  if (N == 0) return TACO_OK;
+  if (!shards) return TACO_ERR_NULL;
+  const uint8_t* ptrs[TACO_MAX_SHARDS];
+  for (int p = 0; p < P; ++p) ptrs[p] = static_cast<const uint8_t*>(shards[p]);
+  return decompress_common(ptrs, P, N, h, block, out_bf16, stream, 0, true);
+}
+
 taco_status taco_decompress_reduce_ptrs(const void* const* shards, int P, int64_t N, int64_t h,
                                         int block, void* out_bf16, void* stream) {
   taco_status st = check_shape(N, h, block);
@@ -524,12 +572,13 @@ taco_status taco_e4m3_decode_f32(const uint8_t* in, float* out, int64_t n, void*
 
 taco_status taco_get_fault(uint32_t* bits, int clear) {
   if (!bits) return TACO_ERR_NULL;
-  unsigned int c = 0, d = 0, t = 0, m = 0;
+  unsigned int c = 0, d = 0, t = 0, m = 0, dm = 0;
   if (compress_fault(&c, clear != 0) != cudaSuccess) return TACO_ERR_CUDA;
   if (compress_mma_fault(&m, clear != 0) != cudaSuccess) return TACO_ERR_CUDA;
+  if (decompress_mma_fault(&dm, clear != 0) != cudaSuccess) return TACO_ERR_CUDA;
   if (decompress_fault(&d, clear != 0) != cudaSuccess) return TACO_ERR_CUDA;
   if (selftest_fault(&t, clear != 0) != cudaSuccess) return TACO_ERR_CUDA;
-  *bits = c | d | t | m;
+  *bits = c | d | t | m | dm;
   return TACO_OK;
 }
 

@@ -36,6 +36,7 @@ constexpr unsigned kFaultCompressWait = 1u;
 constexpr unsigned kFaultDecompressWait = 2u;
 constexpr unsigned kFaultSelftestWait = 4u;
 constexpr unsigned kFaultCompressMmaWait = 8u;
+constexpr unsigned kFaultDecompressMmaWait = 16u;
 
 // ------------------------------------------------------------- f32 pairs ----
 // Two fp32 values in one 64-bit register pair, for the packed f32x2 ALU ops.

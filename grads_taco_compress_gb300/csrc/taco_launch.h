@@ -94,6 +94,12 @@ cudaError_t launch_reduce_recompress(const DecompressArgs& a, int block, int var
                                      cudaStream_t stream);
 cudaError_t decompress_fault(unsigned int* bits, bool clear);
 
+// Tensor-core decompress-reduce (block 64 or 128).
+size_t decompress_mma_smem_bytes(int block);
+const void* decompress_mma_kernel_ptr(int block);
+cudaError_t launch_decompress_mma(const DecompressArgs& a, int block, int grid, cudaStream_t stream);
+cudaError_t decompress_mma_fault(unsigned int* bits, bool clear);
+
 cudaError_t launch_e4m3_encode(const float* in, uint8_t* out, int64_t n, cudaStream_t st);
 cudaError_t launch_e4m3_decode(const uint8_t* in, float* out, int64_t n, cudaStream_t st);
 cudaError_t launch_selftest_wait(unsigned long long limit_ns, uint32_t* status, cudaStream_t st);

@@ -183,6 +183,22 @@ taco_status taco_compress_shards_noalloc(const void* x_bf16, int P, int64_t N, i
 taco_status taco_decompress_reduce(const void* bundle, int P, int64_t N, int64_t h,
                                    int block, void* out_bf16, void* stream);
 
+/* ---- taco_decompress_reduce_mma[_ptrs] ------------------------------------
+ * taco_decompress_reduce[_ptrs] with the inverse rotation on the tensor
+ * cores (tcgen05, E4M3 operands): same arguments, layout and errors, for
+ * block 64 or 128 (block 256 returns TACO_ERR_BLOCK). By linearity
+ * x_hat = sum_p (s_p / (alpha_p sqrt(n))) H_n q_p (TACO pt summary §2.B.2,
+ * reduce of §2.B.3); each 64-code chunk of each shard is multiplied by H_64
+ * as it arrives, exactly in fp32, the scaled sum over shards and the
+ * remaining butterfly levels run in registers, one bf16 rounding at the end.
+ * The output meets the reconstruction bar of taco_decompress_reduce; the two
+ * entries sum in different orders, so single bf16 results may differ by one
+ * unit in the last place. At most 2^31 - 256 blocks per shard. */
+taco_status taco_decompress_reduce_mma(const void* bundle, int P, int64_t N, int64_t h,
+                                       int block, void* out_bf16, void* stream);
+taco_status taco_decompress_reduce_mma_ptrs(const void* const* shards, int P, int64_t N,
+                                            int64_t h, int block, void* out_bf16, void* stream);
+
 /* ---- INT8 fallback format -------------------------------------------------
  * TACO pt summary §5 ("Agnóstico de Hardware"): the framework degrades to
  * INT8 on hardware without FP8 support. The pages define no INT8 format
@@ -270,13 +286,15 @@ taco_status taco_e4m3_decode_f32(const uint8_t* in, float* out, int64_t n, void*
  *   TACO_FAULT_COMPRESS_WAIT, TACO_FAULT_DECOMPRESS_WAIT, TACO_FAULT_SELFTEST_WAIT,
  *   TACO_FAULT_COMPRESS_MMA_WAIT (taco_compress_shards_mma: a wait on a copy,
  *   an MMA or the epilogue gave up; the CTA drains its MMAs and copies and
- *   frees its tensor memory before it returns).
+ *   frees its tensor memory before it returns), TACO_FAULT_DECOMPRESS_MMA_WAIT
+ *   (the same for taco_decompress_reduce_mma).
  * taco_get_fault reads (and with clear != 0 resets) the word of the current
  * device; it synchronises with the device. */
 #define TACO_FAULT_COMPRESS_WAIT 1u
 #define TACO_FAULT_DECOMPRESS_WAIT 2u
 #define TACO_FAULT_SELFTEST_WAIT 4u
 #define TACO_FAULT_COMPRESS_MMA_WAIT 8u
+#define TACO_FAULT_DECOMPRESS_MMA_WAIT 16u
 taco_status taco_get_fault(uint32_t* bits, int clear);
 
 /* Self-test of that time-out path: one warp waits on a barrier that nothing

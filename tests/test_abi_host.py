@@ -106,6 +106,19 @@ def test_compress_mma_rejects(lib, kwargs, status):
 
 
 @no_gpu_only
+def test_decompress_mma_rejects(lib):
+    assert lib.taco_decompress_reduce_mma(A, 2, 4, 256, 256, A * 1024, None) == BLOCK
+    assert lib.taco_decompress_reduce_mma(A, 2, 4, 200, 64, A * 1024, None) == SHAPE
+    assert lib.taco_decompress_reduce_mma(A, 17, 4, 256, 128, A * 1024, None) == ARG
+    assert lib.taco_decompress_reduce_mma(None, 2, 4, 256, 128, A * 1024, None) == NULL
+    assert lib.taco_decompress_reduce_mma(A, 2, 4, 256, 128, A * 1024 + 2, None) == ALIGN
+    assert lib.taco_decompress_reduce_mma(A, 2, 4, 256, 128, A + 512, None) == ARG
+    assert lib.taco_decompress_reduce_int8(A, 2, 4, 256, 128, A * 1024 + 2, None) == ALIGN
+    assert lib.taco_compress_shards_int8(A, 1, 4, 256, 128, 4096.0, 3, A * 64, A * 128, A * 256,
+                                         WSB, None) == ARG
+
+
+@no_gpu_only
 def test_single_compress_rejects(lib):
     assert lib.taco_compress(A, 4, 256, 100, 4096.0, 0, A * 64, A * 128, A * 256, WSB, None) == BLOCK
     assert lib.taco_compress(A + 2, 4, 256, 128, 4096.0, 0, A * 64, A * 128, A * 256, WSB, None) == ALIGN
