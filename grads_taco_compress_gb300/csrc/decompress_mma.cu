@@ -55,6 +55,7 @@ constexpr uint32_t kOutAtomBytes = kRows * 64 * 2;    // 16 KB of bf16
 constexpr uint32_t kHBytes = 64 * 64;                 // H_64 in E4M3
 constexpr uint32_t kTmemCols = 512;                   // two halves of 256
 constexpr uint32_t kHalfCols = 256;
+constexpr int kLoadCols = 32;                         // accumulator columns per tensor-memory wait
 
 template <int NB>
 struct DSmem {
@@ -241,10 +242,23 @@ decompress_mma_kernel(const __grid_constant__ DmmaMaps maps, DecompressArgs a) {
     if (leader) prefetch_map(&maps.out);
     bool stop = false;
 
+    // (alpha, s) pairs of one shard group of one tile, read one group ahead of
+    // their use so that the global-memory latency overlaps a group's work
+    float2 nxt[GS];
+    auto fetch = [&](int kk, int gg) {
+      const int64_t bb = (blockIdx.x + static_cast<int64_t>(kk) * G) * kRows + row;
+#pragma unroll
+      for (int pl = 0; pl < GS; ++pl) {
+        const int p = gg * GS + pl;
+        nxt[pl] = make_float2(1.0f, 0.0f);   // d = 0 for absent shards and rows
+        if (kk < count && p < P && bb < nblocks)
+          nxt[pl] = __ldg(reinterpret_cast<const float2*>(a.shard[p] + a.scales_off) + bb);
+      }
+    };
+    fetch(g, 0);
+
     for (int k = g; k < count && !stop; k += 2) {
       const int64_t tile = blockIdx.x + static_cast<int64_t>(k) * G;
-      const int64_t b = tile * kRows + row;
-      const bool valid = b < nblocks;
 
       float z[NC][64];
 #pragma unroll
@@ -253,18 +267,18 @@ decompress_mma_kernel(const __grid_constant__ DmmaMaps maps, DecompressArgs a) {
         for (int i = 0; i < 64; ++i) z[c][i] = 0.0f;
 
       for (int grp = 0; grp < ngroups; ++grp) {
-        // scales of this group's shards: d = s / alpha / sqrt(n), read
-        // before the wait so that their latency overlaps it
+        // scales of this group's shards: d = s / alpha / sqrt(n)
+        float2 cur[GS];
+#pragma unroll
+        for (int pl = 0; pl < GS; ++pl) cur[pl] = nxt[pl];
+        if (grp + 1 < ngroups) {
+          fetch(k, grp + 1);
+        } else {
+          fetch(k + 2, 0);
+        }
         float d[GS];
 #pragma unroll
-        for (int pl = 0; pl < GS; ++pl) {
-          const int p = grp * GS + pl;
-          d[pl] = 0.0f;
-          if (p < P && valid) {
-            const float2 as = __ldg(reinterpret_cast<const float2*>(a.shard[p] + a.scales_off) + b);
-            d[pl] = __fdividef(as.y, as.x) * a.inv_sqrt_n;
-          }
-        }
+        for (int pl = 0; pl < GS; ++pl) d[pl] = __fdividef(cur[pl].y, cur[pl].x) * a.inv_sqrt_n;
         const uint32_t use = static_cast<uint32_t>((k >> 1) * ngroups + grp);
         const bool got = wait_here(base + S::tfull + 8 * g, use & 1u, abort_flag);
         if (leader && grp == 0) bulk_wait_read<0>();   // the group's last store has read the staging
@@ -280,18 +294,20 @@ decompress_mma_kernel(const __grid_constant__ DmmaMaps maps, DecompressArgs a) {
 #pragma unroll
           for (int c = 0; c < NC; ++c)
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              float v[32];
-              tmem_ld16(thalf + pl * NB + c * 64 + h * 32, v);
-              tmem_ld16(thalf + pl * NB + c * 64 + h * 32 + 16, v + 16);
-              tmem_wait_ld();
-              reg_fence16(v);
-              reg_fence16(v + 16);
+            for (int h = 0; h < 64 / kLoadCols; ++h) {
+              float v[kLoadCols];
 #pragma unroll
-              for (int i = 0; i < 32; i += 2) {
-                const f2 r = fma2(d2, f2{v[i], v[i + 1]}, f2{z[c][h * 32 + i], z[c][h * 32 + i + 1]});
-                z[c][h * 32 + i] = r.x;
-                z[c][h * 32 + i + 1] = r.y;
+              for (int q = 0; q < kLoadCols / 16; ++q)
+                tmem_ld16(thalf + pl * NB + c * 64 + h * kLoadCols + q * 16, v + q * 16);
+              tmem_wait_ld();
+#pragma unroll
+              for (int q = 0; q < kLoadCols / 16; ++q) reg_fence16(v + q * 16);
+#pragma unroll
+              for (int i = 0; i < kLoadCols; i += 2) {
+                const int e = h * kLoadCols + i;
+                const f2 r = fma2(d2, f2{v[i], v[i + 1]}, f2{z[c][e], z[c][e + 1]});
+                z[c][e] = r.x;
+                z[c][e + 1] = r.y;
               }
             }
         }
