@@ -12,6 +12,7 @@ from .binding import (  # noqa: F401
     taco_compress_shards_noalloc, taco_decompress_reduce, taco_decompress_reduce_int8,
     taco_decompress_reduce_mma, taco_decompress_reduce_mma_ptrs, taco_decompress_reduce_ptrs,
     taco_decompress_shards, taco_decompress_shards_ptrs, taco_e4m3_decode_f32, taco_e4m3_encode_f32,
-    taco_reduce_recompress, taco_reduce_recompress_ptrs,
+    taco_reduce_recompress, taco_reduce_recompress_ptrs, taco_reduce_recompress_int8_ptrs,
+    taco_decompress_shards_int8_ptrs,
     workspace_bytes,
 )

@@ -30,13 +30,25 @@ class EmulatedTwoShotAllReduce:
 
     def __init__(self, R: int, M: int, h: int, block: int,
                  target_energy: float = tb.DEFAULT_TARGET_ENERGY, variant: int = tb.VARIANT_DUAL,
-                 device="cuda", compress: str = "mma"):
-        """compress: "mma" (tensor-core Hadamard) or "fwht" (CUDA-core FWHT)."""
+                 device="cuda", compress: str = "mma", fmt: str = "e4m3"):
+        """compress: "mma" (tensor-core Hadamard) or "fwht" (CUDA-core FWHT);
+        fmt: "e4m3" (FP8 codes) or "int8" (the INT8 fallback format; its
+        compress runs on the tensor cores)."""
         if not 1 <= R <= tb.MAX_SHARDS:
             raise ValueError(f"R must be in 1..{tb.MAX_SHARDS}")
         if compress not in ("mma", "fwht"):
             raise ValueError('compress must be "mma" or "fwht"')
-        self._compress = tb.taco_compress_shards_mma if compress == "mma" else tb.taco_compress_shards
+        if fmt not in ("e4m3", "int8"):
+            raise ValueError('fmt must be "e4m3" or "int8"')
+        self.fmt = fmt
+        if fmt == "int8":
+            self._compress = tb.taco_compress_shards_int8
+            self._recompress = tb.taco_reduce_recompress_int8_ptrs
+            self._expand = tb.taco_decompress_shards_int8_ptrs
+        else:
+            self._compress = tb.taco_compress_shards_mma if compress == "mma" else tb.taco_compress_shards
+            self._recompress = tb.taco_reduce_recompress_ptrs
+            self._expand = tb.taco_decompress_shards_ptrs
         if M % R:
             raise ValueError("M must be a multiple of R")
         self.R, self.M, self.h, self.block = R, M, h, block
@@ -67,11 +79,11 @@ class EmulatedTwoShotAllReduce:
                            workspace=self.workspace, stream=stream)
         for dst in range(R):                                          # 2.+3. reduce-scatter
             received = [self.bundles[r][dst] for r in range(R)]
-            tb.taco_reduce_recompress_ptrs(received, c, h, n, self.target_energy, self.variant,
-                                           shard=self.reduced[dst], header=self.reduced_headers[dst],
-                                           workspace=self.workspace, stream=stream)
-        tb.taco_decompress_shards_ptrs(self.reduced, c, h, n,          # 4.+5. all-gather
-                                       out=self.out.view(R, c, h), stream=stream)
+            self._recompress(received, c, h, n, self.target_energy, self.variant,
+                             shard=self.reduced[dst], header=self.reduced_headers[dst],
+                             workspace=self.workspace, stream=stream)
+        self._expand(self.reduced, c, h, n,                           # 4.+5. all-gather
+                     out=self.out.view(R, c, h), stream=stream)
         return self.out
 
     def capture(self, xs: torch.Tensor) -> torch.cuda.CUDAGraph:

@@ -40,6 +40,7 @@ EXPORTED_SYMBOLS = (
     "taco_compress_shards_noalloc", "taco_compress_shards_mma",
     "taco_compress_shards_int8", "taco_decompress_reduce_int8",
     "taco_decompress_reduce_mma", "taco_decompress_reduce_mma_ptrs",
+    "taco_reduce_recompress_int8_ptrs", "taco_decompress_shards_int8_ptrs",
     "taco_decompress_reduce", "taco_decompress_reduce_ptrs",
     "taco_reduce_recompress", "taco_reduce_recompress_ptrs",
     "taco_decompress_shards", "taco_decompress_shards_ptrs",
@@ -81,6 +82,9 @@ def _lib() -> ctypes.CDLL:
             "taco_decompress_reduce_int8": (i32, [vp, i32, i64, i64, i32, vp, vp]),
             "taco_decompress_reduce_mma": (i32, [vp, i32, i64, i64, i32, vp, vp]),
             "taco_decompress_reduce_mma_ptrs": (i32, [ctypes.POINTER(vp), i32, i64, i64, i32, vp, vp]),
+            "taco_reduce_recompress_int8_ptrs": (i32, [ctypes.POINTER(vp), i32, i64, i64, i32, f32, i32,
+                                                       vp, vp, vp, vp, sz, vp]),
+            "taco_decompress_shards_int8_ptrs": (i32, [ctypes.POINTER(vp), i32, i64, i64, i32, vp, vp]),
             "taco_decompress_reduce": (i32, [vp, i32, i64, i64, i32, vp, vp]),
             "taco_decompress_reduce_ptrs": (i32, [ctypes.POINTER(vp), i32, i64, i64, i32, vp, vp]),
             "taco_decompress_shards": (i32, [vp, i32, i64, i64, i32, vp, vp]),
@@ -320,15 +324,23 @@ def taco_decompress_shards(bundle: torch.Tensor, P: int, N: int, h: int, block: 
 
 
 def taco_decompress_shards_ptrs(shards, N: int, h: int, block: int,
-                                out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+                                out: torch.Tensor | None = None, stream=None,
+                                entry: str = "taco_decompress_shards_ptrs") -> torch.Tensor:
     """As taco_decompress_shards with P separate shard tensors."""
     P = len(shards)
     if out is None:
         out = torch.empty((P, N, h), dtype=torch.bfloat16, device=shards[0].device)
     arr = (ctypes.c_void_p * max(P, 1))(*[_ptr(s) for s in shards])
-    st = _lib().taco_decompress_shards_ptrs(arr, P, N, h, block, _ptr(out), _stream_ptr(stream))
-    _check(st, "taco_decompress_shards_ptrs")
+    st = getattr(_lib(), entry)(arr, P, N, h, block, _ptr(out), _stream_ptr(stream))
+    _check(st, entry)
     return out
+
+
+def taco_decompress_shards_int8_ptrs(shards, N: int, h: int, block: int,
+                                     out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """taco_decompress_shards_ptrs for shards with INT8 fallback codes."""
+    return taco_decompress_shards_ptrs(shards, N, h, block, out, stream,
+                                       entry="taco_decompress_shards_int8_ptrs")
 
 
 def taco_reduce_recompress(bundle: torch.Tensor, P: int, N: int, h: int, block: int,
@@ -362,7 +374,8 @@ def taco_reduce_recompress_ptrs(shards, N: int, h: int, block: int,
                                 target_energy: float = DEFAULT_TARGET_ENERGY,
                                 variant: int = VARIANT_DUAL, shard: torch.Tensor | None = None,
                                 header: torch.Tensor | None = None, out: torch.Tensor | None = None,
-                                workspace: torch.Tensor | None = None, stream=None):
+                                workspace: torch.Tensor | None = None, stream=None,
+                                entry: str = "taco_reduce_recompress_ptrs"):
     """As taco_reduce_recompress with P separate shard tensors."""
     P = len(shards)
     dev = shards[0].device
@@ -373,11 +386,21 @@ def taco_reduce_recompress_ptrs(shards, N: int, h: int, block: int,
     if workspace is None:
         workspace = new_workspace(1, dev)
     arr = (ctypes.c_void_p * max(P, 1))(*[_ptr(s) for s in shards])
-    st = _lib().taco_reduce_recompress_ptrs(arr, P, N, h, block, float(target_energy), variant,
-                                            _ptr(shard), _ptr(header), _ptr(out), _ptr(workspace),
-                                            workspace.numel(), _stream_ptr(stream))
-    _check(st, "taco_reduce_recompress_ptrs")
+    st = getattr(_lib(), entry)(arr, P, N, h, block, float(target_energy), variant,
+                                _ptr(shard), _ptr(header), _ptr(out), _ptr(workspace),
+                                workspace.numel(), _stream_ptr(stream))
+    _check(st, entry)
     return shard, header, out
+
+
+def taco_reduce_recompress_int8_ptrs(shards, N: int, h: int, block: int,
+                                     target_energy: float = DEFAULT_TARGET_ENERGY,
+                                     variant: int = VARIANT_DUAL, shard: torch.Tensor | None = None,
+                                     header: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                                     workspace: torch.Tensor | None = None, stream=None):
+    """taco_reduce_recompress_ptrs with INT8 fallback codes in and out."""
+    return taco_reduce_recompress_ptrs(shards, N, h, block, target_energy, variant, shard, header,
+                                       out, workspace, stream, entry="taco_reduce_recompress_int8_ptrs")
 
 
 def taco_e4m3_encode_f32(x: torch.Tensor, stream=None) -> torch.Tensor:

@@ -196,8 +196,9 @@ decompress_reduce_kernel(DecompressArgs a) {
       const float zhi = max3(max3(hq[0], hq[1], hq[2]), max3(hq[3], hq[4], hq[5]), fmaxf(hq[6], hq[7]));
       const float zlo = min3(min3(lq[0], lq[1], lq[2]), min3(lq[3], lq[4], lq[5]), fminf(lq[6], lq[7]));
       const float amax = cscale * block_max<LPB>(fmaxf(zhi, -zlo));
-      const float sc = (VARIANT == 0)   ? fmaxf(1.0f, amax * (1.0f / 448.0f))
-                       : (VARIANT == 1) ? (amax > 0.f ? amax * (1.0f / 448.0f) : 1.0f)
+      constexpr float QMAX = (FMT == 0) ? 448.0f : 127.0f;
+      const float sc = (VARIANT == 0)   ? fmaxf(1.0f, amax * (1.0f / QMAX))
+                       : (VARIANT == 1) ? (amax > 0.f ? amax * (1.0f / QMAX) : 1.0f)
                                         : a.s_static;
       const float g = __fdividef(cscale, sc);
       const f2 g2{g, g};
@@ -210,8 +211,13 @@ decompress_reduce_kernel(DecompressArgs a) {
           const f2 y0 = mul2(z[q][0], g2), y1 = mul2(z[q][1], g2);
           const f2 y2 = mul2(z[q][2], g2), y3 = mul2(z[q][3], g2);
           uint2 w;
-          w.x = e4m3x4_from_f32(y0.x, y0.y, y1.x, y1.y);
-          w.y = e4m3x4_from_f32(y2.x, y2.y, y3.x, y3.y);
+          if constexpr (FMT == 0) {
+            w.x = e4m3x4_from_f32(y0.x, y0.y, y1.x, y1.y);
+            w.y = e4m3x4_from_f32(y2.x, y2.y, y3.x, y3.y);
+          } else {
+            w.x = i8x4_from_f32(y0, y1);
+            w.y = i8x4_from_f32(y2, y3);
+          }
           sts64(base + 8 * (j + LPB * (q ^ cx)), w);
         }
       }
@@ -270,7 +276,7 @@ decompress_reduce_kernel(DecompressArgs a) {
   if (lane == 0) bulk_wait_all();   // the output has been written before the CTA exits
   if constexpr (MODE == 1) {
     finish_header<kDecompressThreads>(part_smax, part_cnt, a.workspace, a.rc_header, a.N, a.h, NB,
-                                      VARIANT, a.target_energy);
+                                      VARIANT, a.target_energy, FMT == 0 ? 448.0f : 127.0f);
   }
 }
 
@@ -297,19 +303,27 @@ const void* decompress_kernel_ptr(int block, int fmt) {
 }
 
 namespace {
+template <int NB, int FMT>
+void (*recompress_fn_fmt(int variant))(DecompressArgs) {
+  return variant == 0   ? decompress_reduce_kernel<NB, 1, 0, FMT>
+         : variant == 1 ? decompress_reduce_kernel<NB, 1, 1, FMT>
+                        : decompress_reduce_kernel<NB, 1, 2, FMT>;
+}
 template <int NB>
-void (*recompress_fn(int variant))(DecompressArgs) {
-  return variant == 0   ? decompress_reduce_kernel<NB, 1, 0>
-         : variant == 1 ? decompress_reduce_kernel<NB, 1, 1>
-                        : decompress_reduce_kernel<NB, 1, 2>;
+void (*recompress_fn(int variant, int fmt))(DecompressArgs) {
+  return fmt == 0 ? recompress_fn_fmt<NB, 0>(variant) : recompress_fn_fmt<NB, 1>(variant);
+}
+template <int NB>
+void (*gather_fn(int fmt))(DecompressArgs) {
+  return fmt == 0 ? decompress_reduce_kernel<NB, 2, 0, 0> : decompress_reduce_kernel<NB, 2, 0, 1>;
 }
 }  // namespace
 
-const void* recompress_kernel_ptr(int block, int variant) {
+const void* recompress_kernel_ptr(int block, int variant, int fmt) {
   switch (block) {
-    case 64: return reinterpret_cast<const void*>(recompress_fn<64>(variant));
-    case 128: return reinterpret_cast<const void*>(recompress_fn<128>(variant));
-    default: return reinterpret_cast<const void*>(recompress_fn<256>(variant));
+    case 64: return reinterpret_cast<const void*>(recompress_fn<64>(variant, fmt));
+    case 128: return reinterpret_cast<const void*>(recompress_fn<128>(variant, fmt));
+    default: return reinterpret_cast<const void*>(recompress_fn<256>(variant, fmt));
   }
 }
 
@@ -330,7 +344,7 @@ cudaError_t launch_decompress(const DecompressArgs& a, int block, int fmt, int g
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-cudaError_t launch_decompress_shards(const DecompressArgs& a, int block, int grid, int P,
+cudaError_t launch_decompress_shards(const DecompressArgs& a, int block, int fmt, int grid, int P,
                                      cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, P);
@@ -342,23 +356,23 @@ cudaError_t launch_decompress_shards(const DecompressArgs& a, int block, int gri
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  void (*kern)(DecompressArgs) = block == 64    ? decompress_reduce_kernel<64, 2, 0>
-                                 : block == 128 ? decompress_reduce_kernel<128, 2, 0>
-                                                : decompress_reduce_kernel<256, 2, 0>;
+  void (*kern)(DecompressArgs) = block == 64    ? gather_fn<64>(fmt)
+                                 : block == 128 ? gather_fn<128>(fmt)
+                                                : gather_fn<256>(fmt);
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-const void* gather_kernel_ptr(int block) {
+const void* gather_kernel_ptr(int block, int fmt) {
   switch (block) {
-    case 64: return reinterpret_cast<const void*>(decompress_reduce_kernel<64, 2, 0>);
-    case 128: return reinterpret_cast<const void*>(decompress_reduce_kernel<128, 2, 0>);
-    default: return reinterpret_cast<const void*>(decompress_reduce_kernel<256, 2, 0>);
+    case 64: return reinterpret_cast<const void*>(gather_fn<64>(fmt));
+    case 128: return reinterpret_cast<const void*>(gather_fn<128>(fmt));
+    default: return reinterpret_cast<const void*>(gather_fn<256>(fmt));
   }
 }
 
-cudaError_t launch_reduce_recompress(const DecompressArgs& a, int block, int variant, int grid,
-                                     cudaStream_t stream) {
+cudaError_t launch_reduce_recompress(const DecompressArgs& a, int block, int variant, int fmt,
+                                     int grid, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kDecompressThreads);
@@ -369,9 +383,9 @@ cudaError_t launch_reduce_recompress(const DecompressArgs& a, int block, int var
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  void (*kern)(DecompressArgs) = block == 64    ? recompress_fn<64>(variant)
-                                 : block == 128 ? recompress_fn<128>(variant)
-                                                : recompress_fn<256>(variant);
+  void (*kern)(DecompressArgs) = block == 64    ? recompress_fn<64>(variant, fmt)
+                                 : block == 128 ? recompress_fn<128>(variant, fmt)
+                                                : recompress_fn<256>(variant, fmt);
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
   return e != cudaSuccess ? e : cudaGetLastError();
 }

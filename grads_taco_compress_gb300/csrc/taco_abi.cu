@@ -49,8 +49,8 @@ struct DeviceInfo {
   int sms = 0;
   int occ_compress[3][kVariants] = {};
   int occ_decompress[3][kFormats] = {};
-  int occ_recompress[3][kVariants] = {};
-  int occ_gather[3] = {};
+  int occ_recompress[3][kVariants][kFormats] = {};
+  int occ_gather[3][kFormats] = {};
   int occ_mma[3][kVariants][kFormats] = {};
   int occ_dmma[2] = {};   // tensor-core decompress, block 64 and 128
 };
@@ -85,11 +85,11 @@ cudaError_t device_info(const DeviceInfo** out) {
           err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ_decompress[b][f], k,
                                                               kDecompressThreads, dsmem);
       }
-      if (err == cudaSuccess) {
-        const void* k = gather_kernel_ptr(blocks[b]);
+      for (int f = 0; f < kFormats && err == cudaSuccess; ++f) {
+        const void* k = gather_kernel_ptr(blocks[b], f);
         err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dsmem);
         if (err == cudaSuccess)
-          err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ_gather[b], k,
+          err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ_gather[b][f], k,
                                                               kDecompressThreads, dsmem);
       }
       for (int v = 0; v < kVariants && err == cudaSuccess; ++v) {
@@ -110,11 +110,13 @@ cudaError_t device_info(const DeviceInfo** out) {
           err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ_dmma[b], k, 320, msmem);
       }
       for (int v = 0; v < kVariants && err == cudaSuccess; ++v) {
-        const void* k = recompress_kernel_ptr(blocks[b], v);
-        err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dsmem);
-        if (err == cudaSuccess)
-          err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ_recompress[b][v], k,
-                                                              kDecompressThreads, dsmem);
+        for (int f = 0; f < kFormats && err == cudaSuccess; ++f) {
+          const void* k = recompress_kernel_ptr(blocks[b], v, f);
+          err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dsmem);
+          if (err == cudaSuccess)
+            err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ_recompress[b][v][f], k,
+                                                                kDecompressThreads, dsmem);
+        }
       }
     }
     g_info_err[dev] = err;
@@ -187,7 +189,7 @@ taco_status decompress_common(const uint8_t* const* shards, int P, int64_t N, in
 }
 
 taco_status decompress_shards_common(const uint8_t* const* shards, int P, int64_t N, int64_t h,
-                                     int block, void* out, void* stream) {
+                                     int block, void* out, void* stream, int fmt = 0) {
   taco_status st = check_shape(N, h, block);
   if (st != TACO_OK) return st;
   if (P < 1 || P > TACO_MAX_SHARDS) return TACO_ERR_ARG;
@@ -213,12 +215,12 @@ taco_status decompress_shards_common(const uint8_t* const* shards, int P, int64_
   const int tb = decompress_tile_blocks(block);
   const int64_t tiles = (a.nblocks + tb - 1) / tb;
   const int64_t needed = (tiles + kDecompressThreads / 32 - 1) / (kDecompressThreads / 32);
-  const int64_t total = static_cast<int64_t>(info->sms) * info->occ_gather[block_index(block)];
+  const int64_t total = static_cast<int64_t>(info->sms) * info->occ_gather[block_index(block)][fmt];
   int64_t gx = (total + P - 1) / P;
   if (gx > needed) gx = needed;
   if (gx < 1) gx = 1;
-  if (launch_decompress_shards(a, block, static_cast<int>(gx), P, static_cast<cudaStream_t>(stream)) !=
-      cudaSuccess)
+  if (launch_decompress_shards(a, block, fmt, static_cast<int>(gx), P,
+                               static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return TACO_ERR_CUDA;
   return TACO_OK;
 }
@@ -226,7 +228,7 @@ taco_status decompress_shards_common(const uint8_t* const* shards, int P, int64_
 taco_status reduce_recompress_common(const uint8_t* const* shards, int P, int64_t N, int64_t h,
                                      int block, float target_energy, int variant, void* shard_out,
                                      taco_header* header_out, void* out, void* workspace,
-                                     size_t workspace_bytes, void* stream) {
+                                     size_t workspace_bytes, void* stream, int fmt = 0) {
   taco_status st = check_shape(N, h, block);
   if (st != TACO_OK) return st;
   if (P < 1 || P > TACO_MAX_SHARDS) return TACO_ERR_ARG;
@@ -263,18 +265,19 @@ taco_status reduce_recompress_common(const uint8_t* const* shards, int P, int64_
   a.target_energy = target_energy;
   a.sqrt_E = static_cast<float>(std::sqrt(static_cast<double>(target_energy)));
   a.sqrt_n = static_cast<float>(std::sqrt(static_cast<double>(block)));
-  a.s_static = static_scale(block, target_energy);
+  a.s_static = static_scale(block, target_energy, fmt == 0 ? 448.0 : 127.0);
 
   const DeviceInfo* info = nullptr;
   if (device_info(&info) != cudaSuccess) return TACO_ERR_CUDA;
   const int tb = decompress_tile_blocks(block);
   const int64_t tiles = (a.nblocks + tb - 1) / tb;
   const int64_t needed = (tiles + kDecompressThreads / 32 - 1) / (kDecompressThreads / 32);
-  int64_t grid = static_cast<int64_t>(info->sms) * info->occ_recompress[block_index(block)][variant];
+  int64_t grid =
+      static_cast<int64_t>(info->sms) * info->occ_recompress[block_index(block)][variant][fmt];
   if (grid > needed) grid = needed;
   if (grid > kMaxCtasPerShard) grid = kMaxCtasPerShard;
   if (grid < 1) grid = 1;
-  if (launch_reduce_recompress(a, block, variant, static_cast<int>(grid),
+  if (launch_reduce_recompress(a, block, variant, fmt, static_cast<int>(grid),
                                static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return TACO_ERR_CUDA;
   return TACO_OK;
@@ -548,6 +551,34 @@ taco_status taco_reduce_recompress_ptrs(const void* const* shards, int P, int64_
   for (int p = 0; p < P; ++p) ptrs[p] = static_cast<const uint8_t*>(shards[p]);
   return reduce_recompress_common(ptrs, P, N, h, block, target_energy, variant, shard_out,
                                   header_out, out_bf16, workspace, workspace_bytes, stream);
+}
+
+taco_status taco_reduce_recompress_int8_ptrs(const void* const* shards, int P, int64_t N,
+                                             int64_t h, int block, float target_energy,
+                                             int variant, void* shard_out,
+                                             taco_header* header_out, void* out_bf16,
+                                             void* workspace, size_t workspace_bytes,
+                                             void* stream) {
+  taco_status st = check_shape(N, h, block);
+  if (st != TACO_OK) return st;
+  if (P < 1 || P > TACO_MAX_SHARDS) return TACO_ERR_ARG;
+  if (!shards) return TACO_ERR_NULL;
+  const uint8_t* ptrs[TACO_MAX_SHARDS];
+  for (int p = 0; p < P; ++p) ptrs[p] = static_cast<const uint8_t*>(shards[p]);
+  return reduce_recompress_common(ptrs, P, N, h, block, target_energy, variant, shard_out,
+                                  header_out, out_bf16, workspace, workspace_bytes, stream, 1);
+}
+
+taco_status taco_decompress_shards_int8_ptrs(const void* const* shards, int P, int64_t N,
+                                             int64_t h, int block, void* out_bf16, void* stream) {
+  taco_status st = check_shape(N, h, block);
+  if (st != TACO_OK) return st;
+  if (P < 1 || P > TACO_MAX_SHARDS) return TACO_ERR_ARG;
+  if (N == 0) return TACO_OK;
+  if (!shards) return TACO_ERR_NULL;
+  const uint8_t* ptrs[TACO_MAX_SHARDS];
+  for (int p = 0; p < P; ++p) ptrs[p] = static_cast<const uint8_t*>(shards[p]);
+  return decompress_shards_common(ptrs, P, N, h, block, out_bf16, stream, 1);
 }
 
 taco_status taco_e4m3_encode_f32(const float* in, uint8_t* out, int64_t n, void* stream) {

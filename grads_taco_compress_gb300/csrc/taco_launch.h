@@ -86,12 +86,12 @@ size_t decompress_smem_bytes();
 const void* decompress_kernel_ptr(int block, int fmt);
 cudaError_t launch_decompress(const DecompressArgs& a, int block, int fmt, int grid,
                               cudaStream_t stream);
-const void* recompress_kernel_ptr(int block, int variant);
-const void* gather_kernel_ptr(int block);
-cudaError_t launch_decompress_shards(const DecompressArgs& a, int block, int grid, int P,
+const void* recompress_kernel_ptr(int block, int variant, int fmt);
+const void* gather_kernel_ptr(int block, int fmt);
+cudaError_t launch_decompress_shards(const DecompressArgs& a, int block, int fmt, int grid, int P,
                                      cudaStream_t stream);
-cudaError_t launch_reduce_recompress(const DecompressArgs& a, int block, int variant, int grid,
-                                     cudaStream_t stream);
+cudaError_t launch_reduce_recompress(const DecompressArgs& a, int block, int variant, int fmt,
+                                     int grid, cudaStream_t stream);
 cudaError_t decompress_fault(unsigned int* bits, bool clear);
 
 // Tensor-core decompress-reduce (block 64 or 128).

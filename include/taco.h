@@ -218,6 +218,18 @@ taco_status taco_compress_shards_int8(const void* x_bf16, int P, int64_t N, int6
                                       void* stream);
 taco_status taco_decompress_reduce_int8(const void* bundle, int P, int64_t N, int64_t h,
                                         int block, void* out_bf16, void* stream);
+/* The AllGather side and the step between the two halves of the two-shot
+ * AllReduce in the INT8 format: taco_reduce_recompress_ptrs and
+ * taco_decompress_shards_ptrs with INT8 codes in and out (q_max 127 in the
+ * written header). */
+taco_status taco_reduce_recompress_int8_ptrs(const void* const* shards, int P, int64_t N,
+                                             int64_t h, int block, float target_energy,
+                                             int variant, void* shard_out,
+                                             taco_header* header_out, void* out_bf16,
+                                             void* workspace, size_t workspace_bytes,
+                                             void* stream);
+taco_status taco_decompress_shards_int8_ptrs(const void* const* shards, int P, int64_t N,
+                                             int64_t h, int block, void* out_bf16, void* stream);
 
 /* ---- taco_decompress_reduce_ptrs ----------------------------------------
  * As taco_decompress_reduce, with the P shards in P separate buffers

@@ -359,7 +359,7 @@ def decompress_reduce(codes: np.ndarray, alpha: np.ndarray, s: np.ndarray,
 # --------------------------------------------------------------------------
 def reduce_recompress(codes: np.ndarray, alpha: np.ndarray, s: np.ndarray, block: int,
                       target_energy: float = DEFAULT_TARGET_ENERGY,
-                      variant: int = VARIANT_DUAL):
+                      variant: int = VARIANT_DUAL, fmt: int = FORMAT_E4M3):
     """Compress the sum of the P reconstructions without rounding it to bf16.
 
     In the two-shot AllReduce ([PT] §2.B.3) each rank reduces the P chunks
@@ -367,8 +367,8 @@ def reduce_recompress(codes: np.ndarray, alpha: np.ndarray, s: np.ndarray, block
     The plain definition: x_hat = decompress_reduce_f64(...) in fp64, then
     the compress steps on those values. Returns (codes, alpha, s, header).
     """
-    x_hat = decompress_reduce_f64(codes, alpha, s, block)
-    st = compress_values_stages(x_hat, block, target_energy, variant)
+    x_hat = decompress_reduce_f64(codes, alpha, s, block, fmt)
+    st = compress_values_stages(x_hat, block, target_energy, variant, fmt)
     return st["codes"], st["alpha"], st["s"], st["header"]
 
 

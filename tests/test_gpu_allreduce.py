@@ -21,17 +21,18 @@ pytestmark = pytest.mark.gpu
 E_STAR = 4096.0
 
 
-def oracle_allreduce(xs, block):
+def oracle_allreduce(xs, block, fmt=O.FORMAT_E4M3, target=E_STAR):
     R, M, h = xs.shape
     c = M // R
-    parts = [[O.compress(xs[r, k * c:(k + 1) * c], block, E_STAR) for k in range(R)] for r in range(R)]
+    parts = [[O.compress(xs[r, k * c:(k + 1) * c], block, target, O.VARIANT_DUAL, fmt) for k in range(R)]
+             for r in range(R)]
     out = []
     for k in range(R):
         codes = np.stack([parts[r][k][0] for r in range(R)])
         alpha = np.stack([parts[r][k][1] for r in range(R)])
         s = np.stack([parts[r][k][2] for r in range(R)])
-        rc, ra, rs, _ = O.reduce_recompress(codes, alpha, s, block, E_STAR)
-        out.append(O.decompress_reduce(rc[None], ra[None], rs[None], block))
+        rc, ra, rs, _ = O.reduce_recompress(codes, alpha, s, block, target, O.VARIANT_DUAL, fmt)
+        out.append(O.decompress_reduce(rc[None], ra[None], rs[None], block, fmt))
     return np.concatenate(out)
 
 
@@ -47,6 +48,23 @@ def test_allreduce_matches_oracle_pipeline(name, R, M, compress):
     parity.compare_recon(O.bf16_bits_to_f64(got), O.bf16_bits_to_f64(want), "allreduce output")
     exact = O.bf16_bits_to_f64(xs).sum(axis=0)
     assert parity.rel_rms(O.bf16_bits_to_f64(got), exact) < 0.06
+
+
+@pytest.mark.parametrize("name,R,M", [("gpt2-1.5b-act", 4, 64), ("gpt3-6.7b-act", 8, 48),
+                                      ("gpt3-6.7b-grad", 2, 30)])
+def test_allreduce_int8_matches_oracle_pipeline(name, R, M):
+    """The INT8 fallback format through all five steps (E* = 900: RMS 30 levels of 127)."""
+    w = dataclasses.replace(W.WORKLOADS[name], P=R)
+    xs = W.make_shards(w, N=M)
+    ar = EmulatedTwoShotAllReduce(R, M, w.h, w.block, target_energy=900.0, fmt="int8")
+    got = host_bits(ar(dev_bf16(xs)))
+    want = oracle_allreduce(xs, w.block, O.FORMAT_INT8, 900.0)
+    parity.compare_recon(O.bf16_bits_to_f64(got), O.bf16_bits_to_f64(want), "int8 allreduce output")
+    exact = O.bf16_bits_to_f64(xs).sum(axis=0)
+    assert parity.rel_rms(O.bf16_bits_to_f64(got), exact) < 0.12
+    from grads_taco_compress_gb300 import binding as tb
+    for hd in ar.reduced_headers:
+        assert tb.parse_headers(hd.view(1, -1))[0]["q_max"] == 127.0
 
 
 def test_allreduce_graph_replay_equals_eager():

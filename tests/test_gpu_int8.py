@@ -125,5 +125,42 @@ def test_int8_full_size_sampled(name):
     parity.compare_recon(O.bf16_bits_to_f64(out[rows]), O.bf16_bits_to_f64(want))
 
 
+def _random_int8_bundle(N, h, block, P, seed):
+    rng = np.random.default_rng(seed)
+    K = h // block
+    codes = np.clip(np.rint(rng.normal(0, 30, size=(P, N, h))), -127, 127).astype(np.int8).view(np.uint8)
+    alpha = np.exp(rng.normal(np.log(3000.0), 0.5, size=(P, N, K))).astype(np.float32)
+    s = np.where(rng.random((P, N, K)) < 0.9, 1.0, rng.uniform(1, 4, (P, N, K))).astype(np.float32)
+    return codes, alpha, s
+
+
+@pytest.mark.parametrize("block,P", [(64, 4), (128, 3), (256, 2)])
+@pytest.mark.parametrize("variant", [tb.VARIANT_DUAL, tb.VARIANT_STATIC])
+def test_int8_reduce_recompress(block, P, variant):
+    N, h = 21, 3 * block
+    codes, alpha, s = _random_int8_bundle(N, h, block, P, seed=block * P + variant)
+    bundle = bundle_from_arrays(codes, alpha, s, block)
+    shard, header, _ = tb.taco_reduce_recompress_int8_ptrs([bundle[p] for p in range(P)], N, h, block,
+                                                           900.0, variant)
+    rc, ra, rs = tb.shard_views(shard.view(1, -1), 1, N, h, block)
+    torch.cuda.synchronize()
+    oc, oa, os_, oh = O.reduce_recompress(codes, alpha, s, block, 900.0, variant, I8)
+    parity.compare_int8_codes(rc.cpu().numpy()[0], oc)
+    parity.compare_scales(ra.cpu().numpy()[0], oa, "alpha")
+    parity.compare_scales(rs.cpu().numpy()[0], os_, "s")
+    assert tb.parse_headers(header.view(1, -1))[0]["q_max"] == 127.0
+
+
+@pytest.mark.parametrize("block,P", [(64, 5), (128, 3), (256, 2)])
+def test_int8_decompress_shards(block, P):
+    N, h = 19, 3 * block
+    codes, alpha, s = _random_int8_bundle(N, h, block, P, seed=block + P)
+    bundle = bundle_from_arrays(codes, alpha, s, block)
+    out = tb.taco_decompress_shards_int8_ptrs([bundle[p] for p in range(P)], N, h, block)
+    for p in range(P):
+        want = O.decompress_reduce(codes[p:p + 1], alpha[p:p + 1], s[p:p + 1], block, I8)
+        parity.compare_recon(O.bf16_bits_to_f64(host_bits(out[p])), O.bf16_bits_to_f64(want))
+
+
 def test_int8_no_wait_timed_out():
     assert tb.taco_get_fault() == 0

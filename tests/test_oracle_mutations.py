@@ -34,8 +34,8 @@ MUTATIONS = {
     "decode_not_normalised": ("u = (w @ H) / math.sqrt(n)", "u = (w @ H) / n"),
     "bf16_truncates": ("np.rint(np.ldexp(v[finite], -q))", "np.trunc(np.ldexp(v[finite], -q))"),
     "reduce_drops_last_shard": ("for p in range(P):", "for p in range(P - 1):"),
-    "recompress_first_shard_only": ("x_hat = decompress_reduce_f64(codes, alpha, s, block)",
-                                    "x_hat = decompress_reduce_f64(codes[:1], alpha[:1], s[:1], block)"),
+    "recompress_first_shard_only": ("x_hat = decompress_reduce_f64(codes, alpha, s, block, fmt)",
+                                    "x_hat = decompress_reduce_f64(codes[:1], alpha[:1], s[:1], block, fmt)"),
     "static_scale_drops_n": ("math.sqrt(block * float(target_energy)) / q_max(fmt)",
                              "math.sqrt(float(target_energy)) / q_max(fmt)"),
     "static_scale_per_block_amax": ("np.full((N, K), np.float32(static_scale(n, target_energy, fmt)), dtype=np.float32)",
@@ -46,8 +46,8 @@ MUTATIONS = {
     "int8_decode_unsigned": ("np.asarray(codes, dtype=np.uint8).view(np.int8).astype(np.float64)",
                              "np.asarray(codes, dtype=np.uint8).astype(np.float64)"),
     "int8_scale_uses_fp8_qmax": ("    qm = q_max(fmt)\n", "    qm = Q_MAX\n"),
-    "recompress_skips_alpha": ("    st = compress_values_stages(x_hat, block, target_energy, variant)\n    return st[\"codes\"], st[\"alpha\"]",
-                               "    st = compress_values_stages(x_hat, block, target_energy, variant)\n    return st[\"codes\"], st[\"alpha\"] * 0 + 1"),
+    "recompress_skips_alpha": ("    st = compress_values_stages(x_hat, block, target_energy, variant, fmt)\n    return st[\"codes\"], st[\"alpha\"]",
+                               "    st = compress_values_stages(x_hat, block, target_energy, variant, fmt)\n    return st[\"codes\"], st[\"alpha\"] * 0 + 1"),
 }
 
 
