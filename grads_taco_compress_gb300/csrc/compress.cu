@@ -216,11 +216,12 @@ compress_kernel(CompressArgs a) {
       }
     }
   }
-  if (lane == 0) bulk_wait_all();   // the codes have been written before the CTA exits
-
   // ---- per-tensor header: CTA reduction, then the last CTA of the shard ----
   finish_header<kCompressThreads>(part_smax, part_cnt, a.workspace + shard * kWorkspaceShardStride,
                                   a.headers + shard, a.N, a.h, NB, VARIANT, a.target_energy, a.q_max);
+  // the stages may be released once every store has read them (the kernel's
+  // end makes the stored codes visible)
+  if (lane == 0) bulk_wait_read<0>();
 }
 
 template <int NB>

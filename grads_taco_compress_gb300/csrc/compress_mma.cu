@@ -383,18 +383,20 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
         part_cnt += (sc > 1.0f) ? 1u : 0u;
       }
     }
-    if (leader) bulk_wait_all();   // the codes have been written before the CTA exits
   }
 
-  // ---- tear-down: free the tensor memory, then the per-tensor header ----
+  // ---- tear-down: the per-tensor header (its arrival count overlaps the
+  // last stores), then free the tensor memory once every store has read
+  // the staging buffer (the kernel's end makes the stored codes visible) ----
   tc_fence_before();
+  finish_header<kThreads>(part_smax, part_cnt, a.workspace + shard * kWorkspaceShardStride,
+                          a.headers + shard, a.N, a.h, NB, VARIANT, a.target_energy, QMAX);
+  if (warp >= 2 && (warp - 2) % 4 == 0 && lane == 0) bulk_wait_read<0>();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }
-  finish_header<kThreads>(part_smax, part_cnt, a.workspace + shard * kWorkspaceShardStride,
-                          a.headers + shard, a.N, a.h, NB, VARIANT, a.target_energy, QMAX);
 }
 
 // Every CTA that shared memory lets onto one SM (228 KB, 1 KB reserved per

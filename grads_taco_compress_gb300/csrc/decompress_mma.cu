@@ -354,7 +354,8 @@ decompress_mma_kernel(const __grid_constant__ DmmaMaps maps, DecompressArgs a) {
         bulk_commit();
       }
     }
-    if (leader) bulk_wait_all();   // the output has been written before the CTA exits
+    if (leader) bulk_wait_read<0>();   // every store has read the staging (the kernel's end
+                                       // makes the stored output visible)
   }
 
   // ---- tear-down: free the tensor memory ----

@@ -273,11 +273,13 @@ decompress_reduce_kernel(DecompressArgs a) {
       }
     }
   }
-  if (lane == 0) bulk_wait_all();   // the output has been written before the CTA exits
   if constexpr (MODE == 1) {
     finish_header<kDecompressThreads>(part_smax, part_cnt, a.workspace, a.rc_header, a.N, a.h, NB,
                                       VARIANT, a.target_energy, FMT == 0 ? 448.0f : 127.0f);
   }
+  // the buffers may be released once every store has read them (the
+  // kernel's end makes the stored output visible)
+  if (lane == 0) bulk_wait_read<0>();
 }
 
 }  // namespace

@@ -211,10 +211,6 @@ template <int N>
 __device__ __forceinline__ void bulk_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read %0;" :: "n"(N) : "memory");
 }
-// All bulk groups of this thread have completed.
-__device__ __forceinline__ void bulk_wait_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
 
 // Programmatic dependent launch: wait until the preceding grid in the stream
 // has completed and its memory is visible (before any global access), and
