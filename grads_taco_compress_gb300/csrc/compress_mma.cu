@@ -16,8 +16,9 @@
 // The energy comes from the rotated block (Parseval: sum t^2 = n sum x^2),
 // so no thread reads x itself: alpha = n sqrt(E*) / sqrt(sum t^2).
 //
-// CTA = 10 warps; two CTAs per SM for n <= 128 (4 stages each), one for
-// n = 256 (6 stages: a tile is 4 atoms), the fastest shapes measured:
+// CTA = 10 warps, one per SM (its registers do not fit twice), with a ring of
+// 4 input stages for n <= 128 and 6 for n = 256 (a tile is 4 atoms), the
+// fastest shapes measured:
 //   warp 0     TMA producer: 3-D tensor loads of [128 blocks x 64 elements]
 //              bf16 atoms (16 KB, 128-byte swizzle) into a ring of stages;
 //   warp 1     owns the tensor memory (2 accumulators x n columns) and one
