@@ -13,6 +13,6 @@ from .binding import (  # noqa: F401
     taco_decompress_reduce_mma, taco_decompress_reduce_mma_ptrs, taco_decompress_reduce_ptrs,
     taco_decompress_shards, taco_decompress_shards_ptrs, taco_e4m3_decode_f32, taco_e4m3_encode_f32,
     taco_reduce_recompress, taco_reduce_recompress_ptrs, taco_reduce_recompress_int8_ptrs,
-    taco_decompress_shards_int8_ptrs,
+    taco_decompress_shards_int8_ptrs, taco_reduce_recompress_batched_ptrs, FORMAT_E4M3, FORMAT_INT8,
     workspace_bytes,
 )

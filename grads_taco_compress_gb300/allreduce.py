@@ -15,7 +15,10 @@ AllGather would hand to the same calls.
   4. AllGather     every rank receives the R results      (pointers)
   5. expand        the R chunks to the full [M, h] result (taco_decompress_shards_ptrs)
 
-All ranks end with the same tensor, so step 5 runs once.
+All ranks end with the same tensor, so step 5 runs once. When R * R <= 16
+(the shard limit of one launch) step 1 is a single compress launch over the
+R * R chunks of all ranks and steps 2-3 a single batched reduce-recompress
+launch (one grid row per destination rank): 3 launches in all, else 2 R + 1.
 """
 
 from __future__ import annotations
@@ -45,10 +48,12 @@ class EmulatedTwoShotAllReduce:
             self._compress = tb.taco_compress_shards_int8
             self._recompress = tb.taco_reduce_recompress_int8_ptrs
             self._expand = tb.taco_decompress_shards_int8_ptrs
+            self._format = tb.FORMAT_INT8
         else:
             self._compress = tb.taco_compress_shards_mma if compress == "mma" else tb.taco_compress_shards
             self._recompress = tb.taco_reduce_recompress_ptrs
             self._expand = tb.taco_decompress_shards_ptrs
+            self._format = tb.FORMAT_E4M3
         if M % R:
             raise ValueError("M must be a multiple of R")
         self.R, self.M, self.h, self.block = R, M, h, block
@@ -56,32 +61,50 @@ class EmulatedTwoShotAllReduce:
         self.target_energy, self.variant = float(target_energy), variant
         dev = torch.device(device)
         sb = tb.shard_bytes(self.chunk, h, block)
-        self.bundles = [torch.empty((R, sb), dtype=torch.uint8, device=dev) for _ in range(R)]
-        self.headers = [torch.empty((R, tb.HEADER_BYTES), dtype=torch.uint8, device=dev) for _ in range(R)]
-        self.reduced = [torch.empty(sb, dtype=torch.uint8, device=dev) for _ in range(R)]
-        self.reduced_headers = [torch.empty(tb.HEADER_BYTES, dtype=torch.uint8, device=dev) for _ in range(R)]
+        self.batched = R * R <= tb.MAX_SHARDS
+        # rank r's compressed chunks are rows r*R .. r*R+R-1 of one bundle
+        self.bundle_all = torch.empty((R * R, sb), dtype=torch.uint8, device=dev)
+        self.headers_all = torch.empty((R * R, tb.HEADER_BYTES), dtype=torch.uint8, device=dev)
+        self.bundles = [self.bundle_all[r * R:(r + 1) * R] for r in range(R)]
+        self.headers = [self.headers_all[r * R:(r + 1) * R] for r in range(R)]
+        self.reduced_all = torch.empty((R, sb), dtype=torch.uint8, device=dev)
+        self.reduced_headers_all = torch.empty((R, tb.HEADER_BYTES), dtype=torch.uint8, device=dev)
+        self.reduced = [self.reduced_all[d] for d in range(R)]
+        self.reduced_headers = [self.reduced_headers_all[d] for d in range(R)]
         self.out = torch.empty((M, h), dtype=torch.bfloat16, device=dev)
-        self.workspace = tb.new_workspace(R, dev)
+        self.workspace = tb.new_workspace(R * R if self.batched else R, dev)
         self._graph = None
 
     def launches(self) -> int:
         """Kernel launches of one AllReduce."""
-        return 2 * self.R + 1
+        return 3 if self.batched else 2 * self.R + 1
 
     def __call__(self, xs: torch.Tensor, stream=None) -> torch.Tensor:
         """xs: bf16 [R, M, h], rank r's tensor in xs[r]. Returns the reduced [M, h]."""
         R, c, h, n = self.R, self.chunk, self.h, self.block
         if xs.shape != (R, self.M, h) or xs.dtype != torch.bfloat16 or not xs.is_contiguous():
             raise ValueError(f"xs must be a contiguous bf16 tensor of shape {(R, self.M, h)}")
-        for r in range(R):                                            # 1. compress
-            self._compress(xs[r].view(R, c, h), n, self.target_energy, self.variant,
-                           bundle=self.bundles[r], headers=self.headers[r],
+        if self.batched:                                              # 1. compress
+            self._compress(xs.view(R * R, c, h), n, self.target_energy, self.variant,
+                           bundle=self.bundle_all, headers=self.headers_all,
                            workspace=self.workspace, stream=stream)
-        for dst in range(R):                                          # 2.+3. reduce-scatter
-            received = [self.bundles[r][dst] for r in range(R)]
-            self._recompress(received, c, h, n, self.target_energy, self.variant,
-                             shard=self.reduced[dst], header=self.reduced_headers[dst],
-                             workspace=self.workspace, stream=stream)
+        else:
+            for r in range(R):
+                self._compress(xs[r].view(R, c, h), n, self.target_energy, self.variant,
+                               bundle=self.bundles[r], headers=self.headers[r],
+                               workspace=self.workspace, stream=stream)
+        if self.batched:                                              # 2.+3. reduce-scatter
+            received = [self.bundles[r][dst] for dst in range(R) for r in range(R)]
+            tb.taco_reduce_recompress_batched_ptrs(received, R, c, h, n, self.target_energy, self.variant,
+                                                   self._format, shards_out=self.reduced_all,
+                                                   headers=self.reduced_headers_all,
+                                                   workspace=self.workspace, stream=stream)
+        else:
+            for dst in range(R):
+                received = [self.bundles[r][dst] for r in range(R)]
+                self._recompress(received, c, h, n, self.target_energy, self.variant,
+                                 shard=self.reduced[dst], header=self.reduced_headers[dst],
+                                 workspace=self.workspace, stream=stream)
         self._expand(self.reduced, c, h, n,                           # 4.+5. all-gather
                      out=self.out.view(R, c, h), stream=stream)
         return self.out

@@ -23,6 +23,8 @@ STATUS_NAMES = {0: "TACO_OK", 1: "TACO_ERR_NULL", 2: "TACO_ERR_SHAPE", 3: "TACO_
 VARIANT_DUAL = 0
 VARIANT_ABSMAX = 1
 VARIANT_STATIC = 2
+FORMAT_E4M3 = 0
+FORMAT_INT8 = 1
 MAX_SHARDS = 16
 HEADER_BYTES = 40
 DEFAULT_TARGET_ENERGY = 4096.0
@@ -41,6 +43,7 @@ EXPORTED_SYMBOLS = (
     "taco_compress_shards_int8", "taco_decompress_reduce_int8",
     "taco_decompress_reduce_mma", "taco_decompress_reduce_mma_ptrs",
     "taco_reduce_recompress_int8_ptrs", "taco_decompress_shards_int8_ptrs",
+    "taco_reduce_recompress_batched_ptrs",
     "taco_decompress_reduce", "taco_decompress_reduce_ptrs",
     "taco_reduce_recompress", "taco_reduce_recompress_ptrs",
     "taco_decompress_shards", "taco_decompress_shards_ptrs",
@@ -85,6 +88,8 @@ def _lib() -> ctypes.CDLL:
             "taco_reduce_recompress_int8_ptrs": (i32, [ctypes.POINTER(vp), i32, i64, i64, i32, f32, i32,
                                                        vp, vp, vp, vp, sz, vp]),
             "taco_decompress_shards_int8_ptrs": (i32, [ctypes.POINTER(vp), i32, i64, i64, i32, vp, vp]),
+            "taco_reduce_recompress_batched_ptrs": (i32, [ctypes.POINTER(vp), i32, i32, i64, i64, i32, f32,
+                                                          i32, i32, vp, vp, vp, sz, vp]),
             "taco_decompress_reduce": (i32, [vp, i32, i64, i64, i32, vp, vp]),
             "taco_decompress_reduce_ptrs": (i32, [ctypes.POINTER(vp), i32, i64, i64, i32, vp, vp]),
             "taco_decompress_shards": (i32, [vp, i32, i64, i64, i32, vp, vp]),
@@ -391,6 +396,33 @@ def taco_reduce_recompress_ptrs(shards, N: int, h: int, block: int,
                                 workspace.numel(), _stream_ptr(stream))
     _check(st, entry)
     return shard, header, out
+
+
+def taco_reduce_recompress_batched_ptrs(shards, Y: int, N: int, h: int, block: int,
+                                        target_energy: float = DEFAULT_TARGET_ENERGY,
+                                        variant: int = VARIANT_DUAL, code_format: int = FORMAT_E4M3,
+                                        shards_out: torch.Tensor | None = None,
+                                        headers: torch.Tensor | None = None,
+                                        workspace: torch.Tensor | None = None, stream=None):
+    """Y reduce-recompress operations in one launch; shards holds Y*P tensors,
+    reduction y takes shards[y*P:(y+1)*P]. Returns (shards_out u8 [Y, shard_bytes],
+    headers u8 [Y, 40])."""
+    if len(shards) % Y:
+        raise ValueError("len(shards) must be a multiple of Y")
+    P = len(shards) // Y
+    dev = shards[0].device
+    if shards_out is None:
+        shards_out = torch.empty((Y, max(shard_bytes(N, h, block), 1)), dtype=torch.uint8, device=dev)
+    if headers is None:
+        headers = torch.empty((Y, HEADER_BYTES), dtype=torch.uint8, device=dev)
+    if workspace is None:
+        workspace = new_workspace(Y, dev)
+    arr = (ctypes.c_void_p * max(len(shards), 1))(*[_ptr(s) for s in shards])
+    st = _lib().taco_reduce_recompress_batched_ptrs(arr, Y, P, N, h, block, float(target_energy), variant,
+                                                     code_format, _ptr(shards_out), _ptr(headers),
+                                                     _ptr(workspace), workspace.numel(), _stream_ptr(stream))
+    _check(st, "taco_reduce_recompress_batched_ptrs")
+    return shards_out, headers
 
 
 def taco_reduce_recompress_int8_ptrs(shards, N: int, h: int, block: int,

@@ -39,7 +39,9 @@ constexpr uint32_t kOutBytes = kTileElems * 2;        // bf16 output of one tile
 // compressed again without leaving the rotated domain: H x_hat = n z and
 // sum x_hat^2 = n sum z^2 (H symmetric, H H = n I), so alpha' = sqrt(E* /
 // sum z^2), the rotated block is alpha' sqrt(n) z and no transform is
-// needed; the bf16 sum is written too when `out` is not null.
+// needed; the bf16 sum is written too when `out` is not null. gridDim.y
+// independent reductions run in one launch: reduction y takes shards
+// y*P .. y*P+P-1 and writes shard y, header y and workspace y.
 // Four codes of one 32-bit word -> (elements 0, 1), (elements 2, 3).
 template <int FMT>
 __device__ __forceinline__ void decode4(uint32_t w, f2& v01, f2& v23) {
@@ -69,8 +71,11 @@ decompress_reduce_kernel(DecompressArgs a) {
   const int sub = lane / LPB;
   const int cx = sub & (kCH - 1);
   const int P = (MODE == 2) ? 1 : a.P;
-  const uint8_t* const* shard_of = (MODE == 2) ? a.shard + blockIdx.y : a.shard;
+  const uint8_t* const* shard_of = (MODE == 2)   ? a.shard + blockIdx.y
+                                  : (MODE == 1) ? a.shard + blockIdx.y * a.P
+                                                : a.shard;
   uint16_t* const out_base = (MODE == 2) ? a.out + static_cast<int64_t>(blockIdx.y) * a.nblocks * NB : a.out;
+  uint8_t* const rc_shard = (MODE == 1) ? a.rc_shard + blockIdx.y * a.rc_stride : nullptr;
 
   const uint32_t stage0 = smem_u32(smem) + warp * (D * kStageBytes);
   const uint32_t bar0 = smem_u32(smem) + WARPS * D * kStageBytes + warp * (D * 8);
@@ -222,14 +227,14 @@ decompress_reduce_kernel(DecompressArgs a) {
         }
       }
       if (sub < vb && j == 0) {
-        reinterpret_cast<float2*>(a.rc_shard + a.scales_off)[b0 + sub] = make_float2(alpha, sc);
+        reinterpret_cast<float2*>(rc_shard + a.scales_off)[b0 + sub] = make_float2(alpha, sc);
         part_smax = fmaxf(part_smax, sc);
         part_cnt += (sc > 1.0f) ? 1u : 0u;
       }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        tma_store_1d(a.rc_shard + b0 * NB, out0, static_cast<uint32_t>(vb) * NB);
+        tma_store_1d(rc_shard + b0 * NB, out0, static_cast<uint32_t>(vb) * NB);
         bulk_commit();
       }
       if (a.out == nullptr) continue;
@@ -274,7 +279,8 @@ decompress_reduce_kernel(DecompressArgs a) {
     }
   }
   if constexpr (MODE == 1) {
-    finish_header<kDecompressThreads>(part_smax, part_cnt, a.workspace, a.rc_header, a.N, a.h, NB,
+    finish_header<kDecompressThreads>(part_smax, part_cnt, a.workspace + blockIdx.y * kWorkspaceShardStride,
+                                      a.rc_header + blockIdx.y, a.N, a.h, NB,
                                       VARIANT, a.target_energy, FMT == 0 ? 448.0f : 127.0f);
   }
   // the buffers may be released once every store has read them (the
@@ -374,9 +380,9 @@ const void* gather_kernel_ptr(int block, int fmt) {
 }
 
 cudaError_t launch_reduce_recompress(const DecompressArgs& a, int block, int variant, int fmt,
-                                     int grid, cudaStream_t stream) {
+                                     int grid, int batch, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
+  cfg.gridDim = dim3(grid, batch);
   cfg.blockDim = dim3(kDecompressThreads);
   cfg.dynamicSmemBytes = decompress_smem_bytes();
   cfg.stream = stream;

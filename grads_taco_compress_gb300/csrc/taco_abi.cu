@@ -225,33 +225,39 @@ taco_status decompress_shards_common(const uint8_t* const* shards, int P, int64_
   return TACO_OK;
 }
 
+// Y reductions of P shards each in one launch (Y = 1: the single form).
+// shards: Y*P pointers, reduction y takes shards[y*P .. y*P+P-1]; the Y
+// outputs are consecutive shards from shard_out, headers header_out[0..Y-1].
 taco_status reduce_recompress_common(const uint8_t* const* shards, int P, int64_t N, int64_t h,
                                      int block, float target_energy, int variant, void* shard_out,
                                      taco_header* header_out, void* out, void* workspace,
-                                     size_t workspace_bytes, void* stream, int fmt = 0) {
+                                     size_t workspace_bytes, void* stream, int fmt = 0, int Y = 1) {
   taco_status st = check_shape(N, h, block);
   if (st != TACO_OK) return st;
-  if (P < 1 || P > TACO_MAX_SHARDS) return TACO_ERR_ARG;
+  if (P < 1 || Y < 1 || P * Y > TACO_MAX_SHARDS) return TACO_ERR_ARG;
+  if (Y > 1 && out) return TACO_ERR_ARG;
   if (!valid_variant(variant)) return TACO_ERR_ARG;
   if (!(target_energy > 0.0f) || !std::isfinite(target_energy)) return TACO_ERR_ARG;
   if (!header_out) return TACO_ERR_NULL;
-  if (!workspace || workspace_bytes < kWorkspaceShardStride) return TACO_ERR_WORKSPACE;
+  if (!workspace || workspace_bytes < Y * kWorkspaceShardStride) return TACO_ERR_WORKSPACE;
   if (!aligned(header_out, 8) || !aligned(workspace, 16)) return TACO_ERR_ALIGN;
   const Layout l = shard_layout(N, h, block);
   const size_t out_bytes = static_cast<size_t>(N) * static_cast<size_t>(h) * 2;
+  const size_t rc_bytes = static_cast<size_t>(Y) * l.bytes;
   DecompressArgs a{};
   if (N > 0) {
     if (!shard_out) return TACO_ERR_NULL;
     if (!aligned(shard_out, 16) || (out && !aligned(out, 16))) return TACO_ERR_ALIGN;
-    if (out && overlap(out, out_bytes, shard_out, l.bytes)) return TACO_ERR_ARG;
-    for (int p = 0; p < P; ++p) {
+    if (out && overlap(out, out_bytes, shard_out, rc_bytes)) return TACO_ERR_ARG;
+    for (int p = 0; p < P * Y; ++p) {
       if (!shards[p]) return TACO_ERR_NULL;
       if (!aligned(shards[p], 16)) return TACO_ERR_ALIGN;
-      if (overlap(shards[p], l.bytes, shard_out, l.bytes)) return TACO_ERR_ARG;
+      if (overlap(shards[p], l.bytes, shard_out, rc_bytes)) return TACO_ERR_ARG;
       if (out && overlap(shards[p], l.bytes, out, out_bytes)) return TACO_ERR_ARG;
       a.shard[p] = shards[p];
     }
   }
+  a.rc_stride = l.bytes;
   a.scales_off = l.scales_off;
   a.P = P;
   a.nblocks = N * h / block;
@@ -272,12 +278,13 @@ taco_status reduce_recompress_common(const uint8_t* const* shards, int P, int64_
   const int tb = decompress_tile_blocks(block);
   const int64_t tiles = (a.nblocks + tb - 1) / tb;
   const int64_t needed = (tiles + kDecompressThreads / 32 - 1) / (kDecompressThreads / 32);
-  int64_t grid =
+  const int64_t total =
       static_cast<int64_t>(info->sms) * info->occ_recompress[block_index(block)][variant][fmt];
+  int64_t grid = (total + Y - 1) / Y;
   if (grid > needed) grid = needed;
   if (grid > kMaxCtasPerShard) grid = kMaxCtasPerShard;
   if (grid < 1) grid = 1;
-  if (launch_reduce_recompress(a, block, variant, fmt, static_cast<int>(grid),
+  if (launch_reduce_recompress(a, block, variant, fmt, static_cast<int>(grid), Y,
                                static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return TACO_ERR_CUDA;
   return TACO_OK;
@@ -567,6 +574,23 @@ taco_status taco_reduce_recompress_int8_ptrs(const void* const* shards, int P, i
   for (int p = 0; p < P; ++p) ptrs[p] = static_cast<const uint8_t*>(shards[p]);
   return reduce_recompress_common(ptrs, P, N, h, block, target_energy, variant, shard_out,
                                   header_out, out_bf16, workspace, workspace_bytes, stream, 1);
+}
+
+taco_status taco_reduce_recompress_batched_ptrs(const void* const* shards, int Y, int P, int64_t N,
+                                                int64_t h, int block, float target_energy,
+                                                int variant, int code_format, void* shards_out,
+                                                taco_header* headers_out, void* workspace,
+                                                size_t workspace_bytes, void* stream) {
+  taco_status st = check_shape(N, h, block);
+  if (st != TACO_OK) return st;
+  if (Y < 1 || P < 1 || static_cast<int64_t>(Y) * P > TACO_MAX_SHARDS) return TACO_ERR_ARG;
+  if (code_format != TACO_FORMAT_E4M3 && code_format != TACO_FORMAT_INT8) return TACO_ERR_ARG;
+  if (!shards) return TACO_ERR_NULL;
+  const uint8_t* ptrs[TACO_MAX_SHARDS];
+  for (int p = 0; p < Y * P; ++p) ptrs[p] = static_cast<const uint8_t*>(shards[p]);
+  return reduce_recompress_common(ptrs, P, N, h, block, target_energy, variant, shards_out,
+                                  headers_out, nullptr, workspace, workspace_bytes, stream,
+                                  code_format, Y);
 }
 
 taco_status taco_decompress_shards_int8_ptrs(const void* const* shards, int P, int64_t N,

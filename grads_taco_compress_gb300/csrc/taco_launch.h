@@ -58,7 +58,9 @@ struct DecompressArgs {
   // reduce-recompress only: the compressed sum and its header
   uint8_t* rc_shard;        // codes | (alpha, s) pairs, same layout as the inputs
   taco_header* rc_header;
-  uint8_t* workspace;       // one shard's header workspace
+  uint8_t* workspace;       // one header workspace per reduced shard
+  size_t rc_stride;         // bytes between the reduced shards of a batched launch
+                            // (gridDim.y reductions of P shards each)
   int64_t N;
   int64_t h;
   float target_energy;
@@ -91,7 +93,7 @@ const void* gather_kernel_ptr(int block, int fmt);
 cudaError_t launch_decompress_shards(const DecompressArgs& a, int block, int fmt, int grid, int P,
                                      cudaStream_t stream);
 cudaError_t launch_reduce_recompress(const DecompressArgs& a, int block, int variant, int fmt,
-                                     int grid, cudaStream_t stream);
+                                     int grid, int batch, cudaStream_t stream);
 cudaError_t decompress_fault(unsigned int* bits, bool clear);
 
 // Tensor-core decompress-reduce (block 64 or 128).

@@ -231,6 +231,23 @@ taco_status taco_reduce_recompress_int8_ptrs(const void* const* shards, int P, i
 taco_status taco_decompress_shards_int8_ptrs(const void* const* shards, int P, int64_t N,
                                              int64_t h, int block, void* out_bf16, void* stream);
 
+/* ---- taco_reduce_recompress_batched_ptrs --------------------------------
+ * Y independent reduce-recompress operations in one launch: the step between
+ * the ReduceScatter and the AllGather (TACO pt summary §2.B.3) for Y
+ * destinations at once. Reduction y sums shards[y*P .. y*P+P-1] (host array
+ * of Y*P device pointers, 1 <= Y*P <= TACO_MAX_SHARDS) and writes shard y of
+ * `shards_out` (Y consecutive shards of taco_shard_bytes, device, 16-byte
+ * aligned) and headers_out[y]; the workspace holds Y shard workspaces
+ * (taco_workspace_bytes(Y)). code_format: TACO_FORMAT_E4M3 or
+ * TACO_FORMAT_INT8 (codes in and out). No bf16 side output. Otherwise as
+ * taco_reduce_recompress_ptrs. */
+enum { TACO_FORMAT_E4M3 = 0, TACO_FORMAT_INT8 = 1 };
+taco_status taco_reduce_recompress_batched_ptrs(const void* const* shards, int Y, int P, int64_t N,
+                                                int64_t h, int block, float target_energy,
+                                                int variant, int code_format, void* shards_out,
+                                                taco_header* headers_out, void* workspace,
+                                                size_t workspace_bytes, void* stream);
+
 /* ---- taco_decompress_reduce_ptrs ----------------------------------------
  * As taco_decompress_reduce, with the P shards in P separate buffers
  * (`shards[p]` a device pointer to one shard, 16-byte aligned; `shards` itself

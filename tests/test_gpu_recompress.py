@@ -111,3 +111,25 @@ def test_recompress_full_size_sampled(name):
     parity.compare_scales(ra[rows], oa, f"{name} alpha")
     parity.compare_scales(rs[rows], os_, f"{name} s")
     assert hdr["s_max"] == rs.max() and hdr["n_clamped"] == np.count_nonzero(rs > 1.0)
+
+
+@pytest.mark.parametrize("Y,P,block,fmt", [(4, 4, 64, tb.FORMAT_E4M3), (2, 8, 128, tb.FORMAT_E4M3),
+                                           (3, 5, 256, tb.FORMAT_E4M3), (4, 4, 128, tb.FORMAT_INT8),
+                                           (1, 16, 64, tb.FORMAT_E4M3)])
+def test_batched_recompress_equals_single_calls(Y, P, block, fmt):
+    """Y reductions in one launch: each output equals the single-call result."""
+    from test_gpu_parity import bundle_from_arrays
+    N, h = 23, 3 * block
+    shards = []
+    for y in range(Y):
+        codes, alpha, s = W.make_random_bundle(N, h, block, P, seed=100 * y + block + P)
+        if fmt == tb.FORMAT_INT8:
+            codes = (codes.astype(np.int64) % 201 - 100).astype(np.int8).view(np.uint8)
+        b = bundle_from_arrays(codes, alpha, s, block)
+        shards += [b[p] for p in range(P)]
+    out, headers = tb.taco_reduce_recompress_batched_ptrs(shards, Y, N, h, block, 900.0, tb.VARIANT_DUAL, fmt)
+    single = tb.taco_reduce_recompress_ptrs if fmt == tb.FORMAT_E4M3 else tb.taco_reduce_recompress_int8_ptrs
+    for y in range(Y):
+        sh, hd, _ = single(shards[y * P:(y + 1) * P], N, h, block, 900.0, tb.VARIANT_DUAL)
+        torch.cuda.synchronize()
+        assert torch.equal(out[y], sh) and torch.equal(headers[y], hd)
