@@ -513,7 +513,9 @@ def run_taco(args, w) -> None:
         kern["emulated_two_shot_allreduce"] = {
             "us": round(t_ar * 1e6, 3), "ranks": P, "tensor": [N, h], "launches": ar.launches(),
             "algbw_gbs": round(N * h * 2 / t_ar / 1e9, 1),
-            "note": "one CUDA graph: compress per rank, reduce-recompress per rank, one expand"}
+            "note": ("one CUDA graph: " + ("one compress launch for all ranks, one batched reduce-recompress, "
+                                            "one expand" if ar.batched else
+                                            "compress per rank, reduce-recompress per rank, one expand"))}
         dom = "compress" if t_c >= t_d else "decompress_reduce"
         achieved = kern[dom]["hbm_gbs"]
         line = {
