@@ -385,6 +385,24 @@ def run_taco(args, w) -> None:
             decompress_mma(k % R, (k + 1) % R)
         t_dm = region(lambda i: decompress_mma(i % R, (i + 1) % R))
 
+    # Context for the roofline fractions: a plain device copy (torch copy_)
+    # that reads and writes the same number of bytes as one launch of each
+    # step kernel, timed the same way. The measured peak is a 4 GB copy; at
+    # these sizes launch ramp-up and drain cost a copy a visible share too.
+    def copy_same_bytes(total_bytes: int) -> float:
+        nel = max(8, total_bytes // 4)
+        reps = max(3, math.ceil(3 * l2 / (4 * nel)) + 1)
+        src = [torch.empty(nel, dtype=torch.bfloat16, device=dev) for _ in range(reps)]
+        dst = [torch.empty(nel, dtype=torch.bfloat16, device=dev) for _ in range(reps)]
+        for i in range(5):
+            dst[i % reps].copy_(src[i % reps])
+        t = region(lambda i: dst[i % reps].copy_(src[i % reps]))
+        del src, dst
+        return t
+
+    t_copy_c = copy_same_bytes(P * N * h * 3 + P * N * K * 8)
+    t_copy_d = copy_same_bytes(P * N * h + P * N * K * 8 + N * h * 2)
+
     # The whole compressed two-shot AllReduce among P logical ranks (the P
     # input tensors of the step), captured in a CUDA graph and replayed.
     from grads_taco_compress_gb300.allreduce import EmulatedTwoShotAllReduce
@@ -481,11 +499,13 @@ def run_taco(args, w) -> None:
                          "hbm_gbs": round(c_bytes / t_c / 1e9, 1),
                          "bf16_in_gbs": round(in_bytes / t_c / 1e9, 1),
                          "frac": round(c_bytes / t_c / 1e9 / hbm, 4),
+                         "copy_same_bytes_frac": round(c_bytes / t_copy_c / 1e9 / hbm, 4),
                          "impl": "tcgen05 tensor-core Hadamard (taco_compress_shards_mma)"},
             "decompress_reduce": {"us": round(t_d * 1e6, 3), "alg_bytes": d_bytes,
                                   "hbm_gbs": round(d_bytes / t_d / 1e9, 1),
                                   "bf16_in_gbs": round(in_bytes / t_d / 1e9, 1),
-                                  "frac": round(d_bytes / t_d / 1e9 / hbm, 4)},
+                                  "frac": round(d_bytes / t_d / 1e9 / hbm, 4),
+                                  "copy_same_bytes_frac": round(d_bytes / t_copy_d / 1e9 / hbm, 4)},
             "reduce_recompress": {"us": round(t_r * 1e6, 3), "alg_bytes": r_bytes,
                                   "hbm_gbs": round(r_bytes / t_r / 1e9, 1),
                                   "bf16_in_gbs": round(in_bytes / t_r / 1e9, 1),
