@@ -1,4 +1,6 @@
-// TACO fused compress kernel for sm_103a.
+// TACO fused compress kernel for sm_103a with the rotation as a CUDA-core
+// FWHT (taco_compress_shards, taco_compress, taco_compress_shards_noalloc;
+// compress_mma.cu holds the tensor-core kernel).
 //
 // One launch does every step of the operator ("TACO: Efficient Communication
 // Compression of Intermediate Tensors ...", gist.science pt summary, §2.B.3:
