@@ -53,7 +53,6 @@ namespace {
 __device__ unsigned int g_compress_mma_fault;
 
 constexpr int kRows = 128;                    // blocks per tile (the MMA's M)
-constexpr int kRing = 16;                     // tile indices in flight from producer to MMA
 constexpr uint32_t kAtomBytes = kRows * 64 * 2;       // 16 KB of bf16
 constexpr uint32_t kCodeAtomBytes = kRows * 64;       // 8 KB of codes
 constexpr uint32_t kHBytes = 64 * 64 * 2;             // H_64 in bf16
@@ -69,18 +68,15 @@ struct Smem {
   static constexpr uint32_t hmat = stages + kStages * kAtomBytes;
   static constexpr uint32_t codes = hmat + kHBytes;                 // [group][chunk] atoms
   static constexpr uint32_t bars = codes + NG * NC * kCodeAtomBytes;
-  // barriers: full[kStages], empty[kStages], tfull[NG], tempty[NG], info[NG], mma_done
+  // barriers: full[kStages], empty[kStages], tfull[NG], tempty[NG], mma_done
   static constexpr uint32_t full = bars;
   static constexpr uint32_t empty = full + 8 * kStages;
   static constexpr uint32_t tfull = empty + 8 * kStages;
   static constexpr uint32_t tempty = tfull + 8 * NG;
-  static constexpr uint32_t info = tempty + 8 * NG;
-  static constexpr uint32_t mma_done = info + 8 * NG;
+  static constexpr uint32_t mma_done = tempty + 8 * NG;
   static constexpr uint32_t tmem_slot = mma_done + 8;
   static constexpr uint32_t abort_flag = tmem_slot + 4;
-  static constexpr uint32_t ring = abort_flag + 4;               // int32[kRing]: tile of local tile k
-  static constexpr uint32_t tile_of = ring + 4 * kRing;          // int32[NG]: tile of each accumulator
-  static constexpr uint32_t end = tile_of + 4 * NG;
+  static constexpr uint32_t end = abort_flag + 4;
   static constexpr uint32_t bytes = end + 1024;                     // + alignment slack
 };
 
@@ -204,6 +200,8 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
   const int shard = blockIdx.y;
   const int64_t nblocks = a.nblocks;
   const int64_t ntiles = (nblocks + kRows - 1) / kRows;
+  const int64_t G = gridDim.x;
+  const int count = static_cast<int>(ntiles > blockIdx.x ? (ntiles - blockIdx.x + G - 1) / G : 0);
 
   // ---- set-up: barriers, H_64, tensor memory ----
   if (threadIdx.x == 0) {
@@ -214,7 +212,6 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
     for (int g = 0; g < NG; ++g) {
       mbar_init(base + S::tfull + 8 * g, 1);
       mbar_init(base + S::tempty + 8 * g, 4);   // one arrival per epilogue warp
-      mbar_init(base + S::info + 8 * g, 1);
     }
     mbar_init(base + S::mma_done, 1);
     *abort_flag = 0u;
@@ -247,44 +244,25 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
   float part_smax = 0.0f;
   uint32_t part_cnt = 0;
 
-  volatile int* ring = reinterpret_cast<volatile int*>(smem_raw + (base - smem_u32(smem_raw)) + S::ring);
-  volatile int* tile_of =
-      reinterpret_cast<volatile int*>(smem_raw + (base - smem_u32(smem_raw)) + S::tile_of);
-
   if (warp == 0) {
     // ---------------------------------------------------- TMA producer ----
-    // Tiles are handed out by the shard's counter in the workspace, so that
-    // faster CTAs take more of them and the CTAs of a launch finish together.
-    // The tile index goes to the MMA lane through `ring`, published by the
-    // barrier arrival of the tile's first atom; past the last tile a -1 goes
-    // out with a plain arrival.
     if (lane == 0) {
       prefetch_map(&map_x);
       const uint64_t policy = l2_evict_first_policy();
-      unsigned int* next_tile =
-          reinterpret_cast<unsigned int*>(a.workspace + shard * kWorkspaceShardStride) + 1;
       uint32_t i = 0;
       bool ok = true;
-      for (int k = 0; ok; ++k) {
-        const int64_t tile = atomicAdd(next_tile, 1u);
-        const bool done = tile >= ntiles;
-        ring[k % kRing] = done ? -1 : static_cast<int>(tile);
-        const int row0 = static_cast<int>(tile * kRows);
-        for (int c = 0; c < (done ? 1 : NC); ++c, ++i) {
+      for (int k = 0; k < count && ok; ++k) {
+        const int row0 = static_cast<int>((blockIdx.x + k * G) * kRows);
+        for (int c = 0; c < NC; ++c, ++i) {
           const uint32_t s = i % kStages, ph = (i / kStages) & 1u;
           if (!wait_here(base + S::empty + 8 * s, ph ^ 1u, abort_flag)) {
             ok = false;
             break;
           }
-          if (done) {
-            mbar_arrive(base + S::full + 8 * s);
-          } else {
-            mbar_arrive_expect_tx(base + S::full + 8 * s, kAtomBytes);
-            tma_load_3d(base + S::stages + s * kAtomBytes, &map_x, c * 64, row0, shard,
-                        base + S::full + 8 * s, policy);
-          }
+          mbar_arrive_expect_tx(base + S::full + 8 * s, kAtomBytes);
+          tma_load_3d(base + S::stages + s * kAtomBytes, &map_x, c * 64, row0, shard,
+                      base + S::full + 8 * s, policy);
         }
-        if (done) break;
       }
       if (!ok) {
         // copies still in flight land in their stages before the CTA exits
@@ -296,38 +274,17 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer ----
-    // The tile of local tile k (or -1 at the end) goes on to the epilogue
-    // group of accumulator k % NG through tile_of, published by that
-    // accumulator's `info` barrier once the accumulator is free.
     if (lane == 0) {
       uint32_t i = 0;
       bool ok = true;
-      for (int k = 0; ok; ++k) {
+      for (int k = 0; k < count && ok; ++k) {
         const int g = k % NG;
         const uint32_t use = static_cast<uint32_t>(k / NG);
         if (!wait_here(base + S::tempty + 8 * g, (use & 1u) ^ 1u, abort_flag)) break;
         tc_fence_after();
-        {
-          const uint32_t s = i % kStages, ph = (i / kStages) & 1u;
-          if (!wait_here(base + S::full + 8 * s, ph, abort_flag)) break;
-        }
-        const int tile = ring[k % kRing];
-        tile_of[g] = tile;
-        mbar_arrive(base + S::info + 8 * g);
-        if (tile < 0) {
-          // the end: the other accumulators' groups learn it once they are free
-          for (int j = 1; j < NG && ok; ++j) {
-            const int g2 = (k + j) % NG;
-            const uint32_t use2 = static_cast<uint32_t>((k + j) / NG);
-            if (!wait_here(base + S::tempty + 8 * g2, (use2 & 1u) ^ 1u, abort_flag)) break;
-            tile_of[g2] = -1;
-            mbar_arrive(base + S::info + 8 * g2);
-          }
-          break;
-        }
         for (int c = 0; c < NC; ++c, ++i) {
           const uint32_t s = i % kStages, ph = (i / kStages) & 1u;
-          if (c > 0 && !wait_here(base + S::full + 8 * s, ph, abort_flag)) {
+          if (!wait_here(base + S::full + 8 * s, ph, abort_flag)) {
             ok = false;
             break;
           }
@@ -359,17 +316,14 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
     float2* __restrict__ scales_out = reinterpret_cast<float2*>(shard_base + a.scales_off);
     if (leader) prefetch_map(&map_codes);
 
-    for (int k = g;; k += NG) {
+    for (int k = g; k < count; k += NG) {
       const uint32_t use = static_cast<uint32_t>(k / NG);
-      const bool got_info = wait_here(base + S::info + 8 * g, use & 1u, abort_flag);
-      const int tile_k = tile_of[g];
-      if (group_any(1 + g, !got_info || tile_k < 0 || *abort_flag != 0u)) break;
       const bool got = wait_here(base + S::tfull + 8 * g, use & 1u, abort_flag);
       if (leader) bulk_wait_read<0>();           // the group's last store has read the staging
       if (group_any(1 + g, !got || *abort_flag != 0u)) break;
       tc_fence_after();
 
-      const int64_t tile = tile_k;
+      const int64_t tile = blockIdx.x + static_cast<int64_t>(k) * G;
       const int64_t b = tile * kRows + row;
       const bool valid = b < nblocks;
 

@@ -368,9 +368,7 @@ __device__ __forceinline__ float block_max(float v) {
 // brings its (max s, count of s > 1); the CTA reduces them, writes one
 // partial into the shard's workspace and counts its arrival; the last CTA to
 // arrive reduces all partials, writes the header and resets the counter.
-// Workspace of a shard: [uint32 arrival counter | uint32 tile counter (the
-// tensor-core compress hands out tiles with it) | pad to 16 | float2 partial
-// per CTA].
+// Workspace of a shard: [uint32 counter | pad to 16 | float2 partial per CTA].
 template <int THREADS>
 __device__ void finish_header(float part_smax, uint32_t part_cnt, uint8_t* ws_shard,
                               taco_header* hd, int64_t N, int64_t h, int block, int variant,
@@ -439,8 +437,7 @@ __device__ void finish_header(float part_smax, uint32_t part_cnt, uint8_t* ws_sh
     hd->q_max = q_max;
     hd->s_max = m;
     hd->n_clamped = n;
-    counter[0] = 0u;   // leave the workspace zero-filled for the next call: the arrival
-    counter[1] = 0u;   // count and the tile counter of the tensor-core compress
+    *counter = 0u;   // leave the workspace zero-filled for the next call
   }
 }
 
