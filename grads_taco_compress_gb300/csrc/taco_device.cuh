@@ -399,13 +399,15 @@ __device__ void finish_header(float part_smax, uint32_t part_cnt, uint8_t* ws_sh
       n += sh_cnt[w];
     }
     partials[blockIdx.x] = make_float2(m, __uint_as_float(n));
-    __threadfence();
-    const uint32_t arrived = atomicAdd(counter, 1u);
+    // one acquire-release arrival: it publishes this CTA's partial (release)
+    // and, in the last CTA, orders the reads of every other partial after
+    // their arrivals (acquire); the barrier below passes that on to the CTA
+    uint32_t arrived;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(arrived) : "l"(counter) : "memory");
     sh_last = (arrived == gridDim.x - 1);
   }
   __syncthreads();
   if (!sh_last) return;
-  __threadfence();
   float m = 0.f;
   uint32_t n = 0;
   for (int i = threadIdx.x; i < static_cast<int>(gridDim.x); i += THREADS) {
