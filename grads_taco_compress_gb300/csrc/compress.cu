@@ -13,8 +13,8 @@
 //   max|Hx| / 448) (ABSMAX: without the floor; STATIC: the per-tensor
 //   sqrt(n E*)/448) -> E4M3 codes with cvt.rn.satfinite, written into the
 //   tile's shared-memory stage and stored with one TMA bulk store per tile,
-//   one (alpha, s) pair store per block -> per-tensor header through per-CTA
-//   partials and a last-CTA reduction.
+//   one (alpha, s) pair store per block -> per-tensor header through running
+//   totals in the workspace, finished by the last CTA to arrive.
 // Grid: gridDim.y = shard, gridDim.x persistent CTAs per shard. Each warp
 // walks warp tiles (2048 elements, 32/LPB blocks) in grid-stride rounds and
 // then an even share of the blocks left over (WarpWork), keeping

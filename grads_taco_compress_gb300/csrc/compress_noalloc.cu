@@ -4,8 +4,8 @@
 // compress: a communication library's progress thread or collective callback
 // that must not call cudaMalloc (it can synchronise the device or deadlock
 // against work in flight), or a runtime whose memory is owned by an external
-// pool. This entry point needs no workspace from them: the per-CTA partials
-// and arrival counters that write the per-tensor header live in the static
+// pool. This entry point needs no workspace from them: the arrival counters
+// and running totals that write the per-tensor header live in the static
 // device array below, which every GPU that loads this library keeps until the
 // process exits.
 
@@ -16,7 +16,7 @@
 
 namespace {
 
-// Room for TACO_NOALLOC_MAX_SHARDS shards of compress workspace (131,200 B).
+// Room for TACO_NOALLOC_MAX_SHARDS shards of compress workspace (128 B).
 constexpr size_t kNoallocScratchBytes =
     static_cast<size_t>(TACO_NOALLOC_MAX_SHARDS) * taco::kWorkspaceShardStride;
 

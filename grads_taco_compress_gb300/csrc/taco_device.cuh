@@ -364,11 +364,15 @@ __device__ __forceinline__ float block_max(float v) {
   return v;
 }
 
-// Per-tensor header of one shard, written in the same launch: every thread
-// brings its (max s, count of s > 1); the CTA reduces them, writes one
-// partial into the shard's workspace and counts its arrival; the last CTA to
-// arrive reduces all partials, writes the header and resets the counter.
-// Workspace of a shard: [uint32 counter | pad to 16 | float2 partial per CTA].
+// Per-tensor header of one shard, written in the same launch. Every thread
+// brings its (max s, count of s > 1); the CTA reduces them and folds the
+// result into two running totals in the shard's workspace (an atomic max on
+// the float's bits, which order like the values because every s is positive
+// and fmaxf drops NaN, and an atomic add), then counts its arrival with one
+// acquire-release add. The CTA that arrives last takes both totals with one
+// 64-bit exchange that also zeroes them, writes the header and resets the
+// counter: two dependent round trips to L2 after the last CTA's work.
+// Workspace of a shard (16 bytes): [u32 arrivals | pad | u32 max-s bits | u32 count].
 template <int THREADS>
 __device__ void finish_header(float part_smax, uint32_t part_cnt, uint8_t* ws_shard,
                               taco_header* hd, int64_t N, int64_t h, int block, int variant,
@@ -376,7 +380,6 @@ __device__ void finish_header(float part_smax, uint32_t part_cnt, uint8_t* ws_sh
   constexpr int WARPS = THREADS / 32;
   __shared__ float sh_max[WARPS];
   __shared__ uint32_t sh_cnt[WARPS];
-  __shared__ bool sh_last;
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
 #pragma unroll
@@ -389,58 +392,33 @@ __device__ void finish_header(float part_smax, uint32_t part_cnt, uint8_t* ws_sh
     sh_cnt[warp] = part_cnt;
   }
   __syncthreads();
-  uint32_t* counter = reinterpret_cast<uint32_t*>(ws_shard);
-  float2* partials = reinterpret_cast<float2*>(ws_shard + 16);
-  if (threadIdx.x == 0) {
-    float m = 0.f;
-    uint32_t n = 0;
-    for (int w = 0; w < WARPS; ++w) {
-      m = fmaxf(m, sh_max[w]);
-      n += sh_cnt[w];
-    }
-    partials[blockIdx.x] = make_float2(m, __uint_as_float(n));
-    // one acquire-release arrival: it publishes this CTA's partial (release)
-    // and, in the last CTA, orders the reads of every other partial after
-    // their arrivals (acquire); the barrier below passes that on to the CTA
-    uint32_t arrived;
-    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(arrived) : "l"(counter) : "memory");
-    sh_last = (arrived == gridDim.x - 1);
-  }
-  __syncthreads();
-  if (!sh_last) return;
+  if (threadIdx.x != 0) return;
   float m = 0.f;
   uint32_t n = 0;
-  for (int i = threadIdx.x; i < static_cast<int>(gridDim.x); i += THREADS) {
-    const float2 p = __ldcg(partials + i);
-    m = fmaxf(m, p.x);
-    n += __float_as_uint(p.y);
+  for (int w = 0; w < WARPS; ++w) {
+    m = fmaxf(m, sh_max[w]);
+    n += sh_cnt[w];
   }
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
-    m = fmaxf(m, __shfl_xor_sync(kFullMask, m, o));
-    n += __shfl_xor_sync(kFullMask, n, o);
-  }
-  __syncthreads();
-  if (lane == 0) {
-    sh_max[warp] = m;
-    sh_cnt[warp] = n;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    for (int w = 1; w < WARPS; ++w) {
-      m = fmaxf(m, sh_max[w]);
-      n += sh_cnt[w];
-    }
-    hd->N = N;
-    hd->h = h;
-    hd->block = block;
-    hd->variant = variant;
-    hd->target_energy = target_energy;
-    hd->q_max = q_max;
-    hd->s_max = m;
-    hd->n_clamped = n;
-    *counter = 0u;   // leave the workspace zero-filled for the next call
-  }
+  uint32_t* counter = reinterpret_cast<uint32_t*>(ws_shard);
+  uint32_t* totals = reinterpret_cast<uint32_t*>(ws_shard + 8);   // 8-byte aligned pair
+  asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(totals), "r"(__float_as_uint(m)) : "memory");
+  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(totals + 1), "r"(n) : "memory");
+  // the release publishes this CTA's two updates; in the last CTA the
+  // acquire orders the exchange below after every other CTA's updates
+  uint32_t arrived;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(arrived) : "l"(counter) : "memory");
+  if (arrived != gridDim.x - 1) return;
+  unsigned long long t;
+  asm volatile("atom.exch.relaxed.gpu.global.b64 %0, [%1], 0;" : "=l"(t) : "l"(totals) : "memory");
+  hd->N = N;
+  hd->h = h;
+  hd->block = block;
+  hd->variant = variant;
+  hd->target_energy = target_energy;
+  hd->q_max = q_max;
+  hd->s_max = __uint_as_float(static_cast<uint32_t>(t));
+  hd->n_clamped = static_cast<uint32_t>(t >> 32);
+  *counter = 0u;   // with the exchange, leaves the workspace zero-filled for the next call
 }
 
 __device__ __forceinline__ uint32_t i8x4_from_f32(f2 y01, f2 y23) {

@@ -24,10 +24,11 @@ constexpr int compress_mma_threads(int block) { return 64 + 128 * compress_mma_g
 // Largest blocks per shard of the tensor-core compress (32-bit TMA coordinates).
 constexpr int64_t kMmaMaxBlocks = (int64_t{1} << 31) - 256;
 
-// Workspace of compress: per shard one arrival counter (16 bytes) followed by
-// one (max s, count) pair per CTA of the shard's grid row.
+// Largest grid row (CTAs per shard) of any launch.
 constexpr int kMaxCtasPerShard = 2048;
-constexpr size_t kWorkspaceShardStride = 16 + 8 * static_cast<size_t>(kMaxCtasPerShard);
+// Workspace of one shard: arrival counter, padding, running max-s bits and
+// running count (16 bytes).
+constexpr size_t kWorkspaceShardStride = 16;
 
 struct CompressArgs {
   const uint16_t* x;        // [P][N][h] bf16

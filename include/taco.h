@@ -93,9 +93,9 @@ typedef struct taco_header {
 size_t taco_shard_bytes(int64_t N, int64_t h, int block);
 size_t taco_shard_scales_offset(int64_t N, int64_t h, int block);
 
-/* Bytes of device workspace that compress needs for P shards. The
- * workspace holds per-CTA partial maxima and arrival counters used to write
- * the per-tensor header in the same launch. It must be zero-filled before
+/* Bytes of device workspace that compress needs for P shards (16 per
+ * shard). The workspace holds, per shard, an arrival counter and the running
+ * maximum and count used to write the per-tensor header in the same launch. It must be zero-filled before
  * its first use; each call leaves it zero-filled again. Calls that share a
  * workspace must not overlap on the GPU (use one workspace per stream). */
 size_t taco_workspace_bytes(int P);
@@ -151,10 +151,10 @@ taco_status taco_compress_shards_mma(const void* x_bf16, int P, int64_t N, int64
  * library's progress thread or collective callback, where cudaMalloc may
  * synchronise the device or deadlock against work in flight; a runtime
  * whose memory belongs to an external pool). It is taco_compress_shards
- * without the workspace argument: the per-CTA partials and counters live in
- * a static device array of the library (TACO_NOALLOC_MAX_SHARDS * 16,400 =
- * 131,200 bytes), which every GPU that loads the library holds until the
- * process exits. The caller still passes x, the bundle and the headers.
+ * without the workspace argument: the counters and running totals live in
+ * a static device array of the library (TACO_NOALLOC_MAX_SHARDS * 16 = 128
+ * bytes), which every GPU that loads the library holds until the process
+ * exits. The caller still passes x, the bundle and the headers.
  *   - P > TACO_NOALLOC_MAX_SHARDS returns TACO_ERR_WORKSPACE (the request does
  *     not fit the static scratch); other errors as taco_compress_shards, and a
  *     rejected call enqueues nothing.

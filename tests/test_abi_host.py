@@ -60,7 +60,7 @@ def test_shard_layout(lib):
     for N, h, n in [(4, 100, 64), (4, 128, 100), (-1, 128, 64), (4, 0, 64)]:
         assert lib.taco_shard_bytes(N, h, n) == 0
     assert lib.taco_workspace_bytes(0) == 0 and lib.taco_workspace_bytes(17) == 0
-    assert 0 < lib.taco_workspace_bytes(1) < lib.taco_workspace_bytes(16) <= WSB
+    assert lib.taco_workspace_bytes(1) == 16 and lib.taco_workspace_bytes(16) == 256 <= WSB
 
 
 def _compress(lib, x=A, P=1, N=4, h=256, block=128, E=4096.0, variant=0, bundle=A * 64,
@@ -76,7 +76,7 @@ def _compress(lib, x=A, P=1, N=4, h=256, block=128, E=4096.0, variant=0, bundle=
     (dict(P=0), ARG), (dict(P=17), ARG), (dict(variant=3), ARG), (dict(variant=-1), ARG),
     (dict(E=0.0), ARG), (dict(E=-1.0), ARG), (dict(E=float("nan")), ARG),
     (dict(E=float("inf")), ARG),
-    (dict(headers=None), NULL), (dict(ws=None), WS), (dict(wsb=100), WS),
+    (dict(headers=None), NULL), (dict(ws=None), WS), (dict(wsb=15), WS),
     (dict(x=None), NULL), (dict(bundle=None), NULL),
     (dict(x=A + 8), ALIGN), (dict(bundle=A * 64 + 4), ALIGN), (dict(headers=A * 128 + 4), ALIGN),
     (dict(ws=A * 256 + 8), ALIGN),
@@ -197,7 +197,7 @@ def test_reduce_recompress_rejects(lib):
     assert call(h=200, block=64) == SHAPE
     assert call(P=0) == ARG and call(P=17) == ARG
     assert call(variant=3) == ARG and call(E=0.0) == ARG and call(E=float("nan")) == ARG
-    assert call(hdr=None) == NULL and call(ws=None) == WS and call(wsb=64) == WS
+    assert call(hdr=None) == NULL and call(ws=None) == WS and call(wsb=15) == WS
     assert call(bundle=None) == NULL and call(shard=None) == NULL
     assert call(shard=A * 64 + 8) == ALIGN and call(out=A * 512 + 4) == ALIGN
     assert call(shard=A + 256) == ARG                     # output shard inside the inputs

@@ -120,7 +120,46 @@ def test_mma_deterministic_and_workspace_reset():
     b2, h2 = MMA(x, w.block, workspace=ws)
     torch.cuda.synchronize()
     assert torch.equal(b1, b2) and torch.equal(h1, h2)
-    assert int(ws.view(torch.uint8).reshape(2, -1)[:, :4].count_nonzero()) == 0
+    assert int(ws.count_nonzero()) == 0      # counters and running totals
+
+
+@pytest.mark.parametrize("entry", ["mma", "fwht", "recompress"])
+def test_header_totals_over_the_full_grid(entry):
+    """Per-tensor header from the running totals at full grid size: about
+    one block in eight clamped (E* = 30000 puts the rotated rms at 173 code
+    units) across every CTA, and the largest s in one constant block per
+    shard (all its energy in one rotated coefficient); repeated calls give
+    the same header and leave the workspace zero."""
+    w = W.WORKLOADS["gpt2-1.5b-act"]
+    E = 30000.0
+    v = W.make_shards(w, P=2)
+    one = W.f32_to_bf16_bits(np.array([0.5], np.float32))[0]
+    v[0, -3, 128:192] = one
+    v[1, w.N // 2 + 7, 0:64] = one ^ 0x8000
+    x = dev_bf16(v)
+    ws = tb.new_workspace(2)
+    if entry == "recompress":
+        bundle, _ = MMA(x, w.block, E)
+        out = [tb.taco_reduce_recompress(bundle, 2, w.N, w.h, w.block, E, workspace=ws) for _ in range(2)]
+        shards = [o[0][None] for o in out]
+        headers = [o[1][None] for o in out]
+        P = 1
+    else:
+        fn = MMA if entry == "mma" else tb.taco_compress_shards
+        out = [fn(x, w.block, E, workspace=ws) for _ in range(2)]
+        shards = [o[0] for o in out]
+        headers = [o[1] for o in out]
+        P = 2
+    torch.cuda.synchronize()
+    assert int(ws.count_nonzero()) == 0
+    assert torch.equal(headers[0], headers[1])
+    _, _, s = tb.shard_views(shards[0], P, w.N, w.h, w.block)
+    s = s.cpu().numpy()
+    hdr = tb.parse_headers(headers[0])
+    for p in range(P):
+        assert np.count_nonzero(s[p] > 1.0) > 1000
+        assert hdr[p]["s_max"] == s[p].max() and hdr[p]["s_max"] > 2.0
+        assert hdr[p]["n_clamped"] == np.count_nonzero(s[p] > 1.0)
 
 
 FULL = ["tiny-512x1024", "gpt2-1.5b-act", "gpt3-6.7b-act", "gpt3-6.7b-grad", "qwen-7b-long"]

@@ -175,8 +175,7 @@ def test_compress_deterministic_and_workspace_reset():
     b2, h2 = tb.taco_compress_shards(x, w.block, workspace=ws)
     torch.cuda.synchronize()
     assert torch.equal(b1, b2) and torch.equal(h1, h2)
-    counters = ws.view(torch.uint8).reshape(2, -1)[:, :4]
-    assert int(counters.count_nonzero()) == 0
+    assert int(ws.count_nonzero()) == 0      # counters and running totals
 
 
 def test_compress_does_not_write_outside_its_buffers():
