@@ -18,7 +18,7 @@
 // The energy comes from the rotated block (Parseval: sum t^2 = n sum x^2),
 // so no thread reads x itself: alpha = n sqrt(E*) / sqrt(sum t^2).
 //
-// CTA = 10 warps, one per SM (its registers do not fit twice), with a ring of
+// CTA = 11 warps, one per SM (its registers do not fit twice), with a ring of
 // 4 input stages for n <= 128 and 6 for n = 256 (a tile is 4 atoms), the
 // fastest shapes measured:
 //   warp 0     TMA producer: 3-D tensor loads of [128 blocks x 64 elements]
@@ -32,7 +32,18 @@
 //              warp may read). It loads its row with tcgen05.ld, finishes the
 //              rotation, computes alpha, s and the codes, writes the codes
 //              into a 64-byte-swizzled staging buffer that one thread stores
-//              with 3-D TMA tensor stores, and stores its (alpha, s) pair.
+//              with 3-D TMA tensor stores, and stores its (alpha, s) pair;
+//   warp 10    tile scheduler (below).
+// Tile schedule: the CTAs of a shard take 3/4 of the per-CTA share of
+// tiles round-robin (tile blockIdx.x + k * gridDim.x), then claim
+// the rest one at a time from the shard's counter in the workspace, so that
+// the CTAs that stream faster take more of them and the CTAs of a launch
+// finish together (with a static split the spread of per-SM progress grew
+// through the launch to several tiles). The scheduler lane keeps two claims
+// ready in a shared-memory ring, which hides the atomic's round trip from
+// the producer. A tile's index reaches the MMA lane with the barrier of its
+// first atom and the epilogue group with the group's `info` barrier; a -1
+// ends every role.
 // FMT selects the code format: 0 = FP8 E4M3 (Q_max 448), 1 = the INT8
 // fallback (Q_max 127, round half to even; pt summary §5, hardware without
 // FP8).
@@ -53,6 +64,8 @@ namespace {
 __device__ unsigned int g_compress_mma_fault;
 
 constexpr int kRows = 128;                    // blocks per tile (the MMA's M)
+constexpr int kRing = 8;                      // tile indices in flight, producer -> MMA lane
+constexpr int kClaims = 2;                    // claimed tiles in flight, scheduler -> producer
 constexpr uint32_t kAtomBytes = kRows * 64 * 2;       // 16 KB of bf16
 constexpr uint32_t kCodeAtomBytes = kRows * 64;       // 8 KB of codes
 constexpr uint32_t kHBytes = 64 * 64 * 2;             // H_64 in bf16
@@ -68,15 +81,22 @@ struct Smem {
   static constexpr uint32_t hmat = stages + kStages * kAtomBytes;
   static constexpr uint32_t codes = hmat + kHBytes;                 // [group][chunk] atoms
   static constexpr uint32_t bars = codes + NG * NC * kCodeAtomBytes;
-  // barriers: full[kStages], empty[kStages], tfull[NG], tempty[NG], mma_done
+  // barriers: full[kStages], empty[kStages], tfull[NG], tempty[NG], info[NG],
+  // cfull[kClaims], cempty[kClaims], mma_done
   static constexpr uint32_t full = bars;
   static constexpr uint32_t empty = full + 8 * kStages;
   static constexpr uint32_t tfull = empty + 8 * kStages;
   static constexpr uint32_t tempty = tfull + 8 * NG;
-  static constexpr uint32_t mma_done = tempty + 8 * NG;
+  static constexpr uint32_t info = tempty + 8 * NG;
+  static constexpr uint32_t cfull = info + 8 * NG;
+  static constexpr uint32_t cempty = cfull + 8 * kClaims;
+  static constexpr uint32_t mma_done = cempty + 8 * kClaims;
   static constexpr uint32_t tmem_slot = mma_done + 8;
   static constexpr uint32_t abort_flag = tmem_slot + 4;
-  static constexpr uint32_t end = abort_flag + 4;
+  static constexpr uint32_t tile_ring = abort_flag + 4;   // int[kRing]: tile of the CTA's tile k
+  static constexpr uint32_t tile_of = tile_ring + 4 * kRing;      // int[NG]: tile of accumulator g
+  static constexpr uint32_t claim = tile_of + 4 * NG;             // int[kClaims]: claimed tiles
+  static constexpr uint32_t end = claim + 4 * kClaims;
   static constexpr uint32_t bytes = end + 1024;                     // + alignment slack
 };
 
@@ -186,14 +206,21 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
   constexpr int NG = S::NG;
   constexpr int kThreads = S::threads;
   constexpr int kStages = S::kStages;
+  constexpr int kSchedWarp = 2 + 4 * NG;
+  // the producer writes tile k's ring slot after the empty waits of tile k-1,
+  // so the MMA lane has read every slot up to k - kRing by then
+  static_assert(kRing * NC >= kStages + 1, "a tile index is read before its ring slot is rewritten");
   constexpr uint32_t TMEM_COLS = NG * NB;   // one accumulator per epilogue group
   static_assert(TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "tensor memory columns");
   constexpr float QMAX = (FMT == 0) ? 448.0f : 127.0f;
 
   extern __shared__ unsigned char smem_raw[];
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  volatile uint32_t* abort_flag =
-      reinterpret_cast<volatile uint32_t*>(smem_raw + (base - smem_u32(smem_raw)) + S::abort_flag);
+  unsigned char* const sbase = smem_raw + (base - smem_u32(smem_raw));
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(sbase + S::abort_flag);
+  volatile int* tile_ring = reinterpret_cast<volatile int*>(sbase + S::tile_ring);
+  volatile int* tile_of = reinterpret_cast<volatile int*>(sbase + S::tile_of);
+  volatile int* claim = reinterpret_cast<volatile int*>(sbase + S::claim);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -201,7 +228,9 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
   const int64_t nblocks = a.nblocks;
   const int64_t ntiles = (nblocks + kRows - 1) / kRows;
   const int64_t G = gridDim.x;
-  const int count = static_cast<int>(ntiles > blockIdx.x ? (ntiles - blockIdx.x + G - 1) / G : 0);
+  // round-robin tiles per CTA: 3/4 of the even share, rounded up (a CTA with
+  // one tile starts it without waiting for a claim)
+  const int n_static = static_cast<int>((3 * (ntiles / G) + 3) / 4);
 
   // ---- set-up: barriers, H_64, tensor memory ----
   if (threadIdx.x == 0) {
@@ -212,6 +241,11 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
     for (int g = 0; g < NG; ++g) {
       mbar_init(base + S::tfull + 8 * g, 1);
       mbar_init(base + S::tempty + 8 * g, 4);   // one arrival per epilogue warp
+      mbar_init(base + S::info + 8 * g, 1);
+    }
+    for (int c = 0; c < kClaims; ++c) {
+      mbar_init(base + S::cfull + 8 * c, 1);
+      mbar_init(base + S::cempty + 8 * c, 1);
     }
     mbar_init(base + S::mma_done, 1);
     *abort_flag = 0u;
@@ -251,18 +285,32 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
       const uint64_t policy = l2_evict_first_policy();
       uint32_t i = 0;
       bool ok = true;
-      for (int k = 0; k < count && ok; ++k) {
-        const int row0 = static_cast<int>((blockIdx.x + k * G) * kRows);
-        for (int c = 0; c < NC; ++c, ++i) {
+      for (int k = 0; ok; ++k) {
+        int tile;
+        if (k < n_static) {
+          tile = static_cast<int>(blockIdx.x + static_cast<int64_t>(k) * G);
+        } else {
+          const uint32_t j = static_cast<uint32_t>(k - n_static), c = j % kClaims;
+          if (!wait_here(base + S::cfull + 8 * c, (j / kClaims) & 1u, abort_flag)) break;
+          tile = claim[c];
+          mbar_arrive(base + S::cempty + 8 * c);
+        }
+        tile_ring[k % kRing] = tile;   // published by the arrival on the first atom's barrier
+        for (int c = 0; c < (tile < 0 ? 1 : NC); ++c, ++i) {
           const uint32_t s = i % kStages, ph = (i / kStages) & 1u;
           if (!wait_here(base + S::empty + 8 * s, ph ^ 1u, abort_flag)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(base + S::full + 8 * s, kAtomBytes);
-          tma_load_3d(base + S::stages + s * kAtomBytes, &map_x, c * 64, row0, shard,
-                      base + S::full + 8 * s, policy);
+          if (tile < 0) {
+            mbar_arrive(base + S::full + 8 * s);   // the end: an arrival without a copy
+          } else {
+            mbar_arrive_expect_tx(base + S::full + 8 * s, kAtomBytes);
+            tma_load_3d(base + S::stages + s * kAtomBytes, &map_x, c * 64, tile * kRows, shard,
+                        base + S::full + 8 * s, policy);
+          }
         }
+        if (tile < 0) break;
       }
       if (!ok) {
         // copies still in flight land in their stages before the CTA exits
@@ -277,14 +325,31 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
     if (lane == 0) {
       uint32_t i = 0;
       bool ok = true;
-      for (int k = 0; k < count && ok; ++k) {
+      for (int k = 0; ok; ++k) {
         const int g = k % NG;
         const uint32_t use = static_cast<uint32_t>(k / NG);
         if (!wait_here(base + S::tempty + 8 * g, (use & 1u) ^ 1u, abort_flag)) break;
         tc_fence_after();
+        if (!wait_here(base + S::full + 8 * (i % kStages), (i / kStages) & 1u, abort_flag)) break;
+        // the tile of local tile k goes on to its epilogue group, whose
+        // accumulator (and tile_of slot) is free
+        const int tile = tile_ring[k % kRing];
+        tile_of[g] = tile;
+        mbar_arrive(base + S::info + 8 * g);
+        if (tile < 0) {
+          // the end: the other groups learn it once their accumulators are free
+          for (int j = 1; j < NG; ++j) {
+            const int g2 = (k + j) % NG;
+            const uint32_t use2 = static_cast<uint32_t>((k + j) / NG);
+            if (!wait_here(base + S::tempty + 8 * g2, (use2 & 1u) ^ 1u, abort_flag)) break;
+            tile_of[g2] = -1;
+            mbar_arrive(base + S::info + 8 * g2);
+          }
+          break;
+        }
         for (int c = 0; c < NC; ++c, ++i) {
           const uint32_t s = i % kStages, ph = (i / kStages) & 1u;
-          if (!wait_here(base + S::full + 8 * s, ph, abort_flag)) {
+          if (c > 0 && !wait_here(base + S::full + 8 * s, ph, abort_flag)) {
             ok = false;
             break;
           }
@@ -304,6 +369,23 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
       mbar_wait(base + S::mma_done, 0);
     }
     __syncwarp();
+  } else if (warp == kSchedWarp) {
+    // ---------------------------------------------------- tile scheduler ----
+    if (lane == 0) {
+      unsigned int* next =
+          reinterpret_cast<unsigned int*>(a.workspace + shard * kWorkspaceShardStride) + 1;
+      const int64_t first = static_cast<int64_t>(n_static) * G;   // first tile of the pool
+      for (uint32_t j = 0;; ++j) {
+        const uint32_t c = j % kClaims;
+        if (!wait_here(base + S::cempty + 8 * c, ((j / kClaims) & 1u) ^ 1u, abort_flag)) break;
+        const int64_t t = first + atomicAdd(next, 1u);
+        const int tile = t < ntiles ? static_cast<int>(t) : -1;
+        claim[c] = tile;
+        mbar_arrive(base + S::cfull + 8 * c);
+        if (tile < 0) break;
+      }
+    }
+    __syncwarp();
   } else {
     // -------------------------------------------------------- epilogue ----
     const int g = (warp - 2) >> 2;               // group: accumulator and tiles k % NG == g
@@ -316,14 +398,17 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
     float2* __restrict__ scales_out = reinterpret_cast<float2*>(shard_base + a.scales_off);
     if (leader) prefetch_map(&map_codes);
 
-    for (int k = g; k < count; k += NG) {
+    for (int k = g;; k += NG) {
       const uint32_t use = static_cast<uint32_t>(k / NG);
+      const bool got_info = wait_here(base + S::info + 8 * g, use & 1u, abort_flag);
+      const int tile_k = tile_of[g];
+      if (group_any(1 + g, !got_info || tile_k < 0 || *abort_flag != 0u)) break;
       const bool got = wait_here(base + S::tfull + 8 * g, use & 1u, abort_flag);
       if (leader) bulk_wait_read<0>();           // the group's last store has read the staging
       if (group_any(1 + g, !got || *abort_flag != 0u)) break;
       tc_fence_after();
 
-      const int64_t tile = blockIdx.x + static_cast<int64_t>(k) * G;
+      const int64_t tile = tile_k;
       const int64_t b = tile * kRows + row;
       const bool valid = b < nblocks;
 
@@ -394,7 +479,7 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
   tc_fence_before();
   finish_header<kThreads>(part_smax, part_cnt, a.workspace + shard * kWorkspaceShardStride,
                           a.headers + shard, a.N, a.h, NB, VARIANT, a.target_energy, QMAX);
-  if (warp >= 2 && (warp - 2) % 4 == 0 && lane == 0) bulk_wait_read<0>();
+  if (warp >= 2 && warp < kSchedWarp && (warp - 2) % 4 == 0 && lane == 0) bulk_wait_read<0>();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();

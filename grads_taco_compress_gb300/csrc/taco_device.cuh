@@ -372,7 +372,7 @@ __device__ __forceinline__ float block_max(float v) {
 // acquire-release add. The CTA that arrives last takes both totals with one
 // 64-bit exchange that also zeroes them, writes the header and resets the
 // counter: two dependent round trips to L2 after the last CTA's work.
-// Workspace of a shard (16 bytes): [u32 arrivals | pad | u32 max-s bits | u32 count].
+// Workspace of a shard (16 bytes): [u32 arrivals | u32 tile claims | u32 max-s bits | u32 count].
 template <int THREADS>
 __device__ void finish_header(float part_smax, uint32_t part_cnt, uint8_t* ws_shard,
                               taco_header* hd, int64_t N, int64_t h, int block, int variant,
@@ -418,7 +418,10 @@ __device__ void finish_header(float part_smax, uint32_t part_cnt, uint8_t* ws_sh
   hd->q_max = q_max;
   hd->s_max = __uint_as_float(static_cast<uint32_t>(t));
   hd->n_clamped = static_cast<uint32_t>(t >> 32);
-  *counter = 0u;   // with the exchange, leaves the workspace zero-filled for the next call
+  // with the exchange, leaves the workspace zero-filled for the next call
+  // (the arrival counter and the word after it, the tile counter of the
+  // tensor-core compress, whose claims all came before the arrivals)
+  *reinterpret_cast<unsigned long long*>(ws_shard) = 0ull;
 }
 
 __device__ __forceinline__ uint32_t i8x4_from_f32(f2 y01, f2 y23) {

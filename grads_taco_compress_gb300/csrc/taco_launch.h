@@ -17,17 +17,18 @@ constexpr int kDecompressThreads = 256;
 constexpr int kDecompressMinBlocks = 2;
 constexpr int kDecompressStages = 4;      // (tile, shard) stages in flight per warp
 constexpr int kVariants = 3;              // DUAL, ABSMAX, STATIC
-// Tensor-core compress: a producer warp, an MMA warp and groups of 4
-// epilogue warps, one accumulator of `block` TMEM columns per group.
+// Tensor-core compress: a producer warp, an MMA warp, groups of 4 epilogue
+// warps (one accumulator of `block` TMEM columns per group) and a tile
+// scheduler warp.
 constexpr int compress_mma_groups(int) { return 2; }
-constexpr int compress_mma_threads(int block) { return 64 + 128 * compress_mma_groups(block); }
+constexpr int compress_mma_threads(int block) { return 64 + 128 * compress_mma_groups(block) + 32; }
 // Largest blocks per shard of the tensor-core compress (32-bit TMA coordinates).
 constexpr int64_t kMmaMaxBlocks = (int64_t{1} << 31) - 256;
 
 // Largest grid row (CTAs per shard) of any launch.
 constexpr int kMaxCtasPerShard = 2048;
-// Workspace of one shard: arrival counter, padding, running max-s bits and
-// running count (16 bytes).
+// Workspace of one shard: arrival counter, tile-claim counter (tensor-core
+// compress), running max-s bits and running count (16 bytes).
 constexpr size_t kWorkspaceShardStride = 16;
 
 struct CompressArgs {
