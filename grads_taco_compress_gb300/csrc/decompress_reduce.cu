@@ -97,25 +97,52 @@ decompress_reduce_kernel(DecompressArgs a) {
   grid_dependency_wait();   // no global access before the preceding grid is done
 
   // Producer state, kept identical in every lane (lane 0 issues the copies):
-  // next stage = (tile number it_t of this warp, shard ip), its slot is, and
-  // the byte offsets of that tile inside a shard.
+  // next stage = (tile number it_t of this warp, shard ip) and its slot is.
+  // The reduce-recompress (MODE 1) keeps the tile's offsets, sizes and the
+  // cache policy from the tile's first shard on: that removes its register
+  // spills (n = 128, 256), while the other modes measured faster with them
+  // recomputed for every stage.
+  constexpr bool kKeepTile = (MODE == 1);
   int issued = 0, it_t = 0, ip = 0, is = 0;
+  uint64_t k_policy = 0, k_codes = 0, k_scales = 0;   // kept tile (MODE 1)
+  uint32_t k_cbytes = 0, k_sbytes = 0;
+  if constexpr (kKeepTile) k_policy = l2_evict_first_policy();
   auto issue_next = [&]() {
     if (lane == 0) {
-      int64_t tb0;
-      int tvb;
-      ww.tile(it_t, tb0, tvb);
-      const uint32_t vb = static_cast<uint32_t>(tvb);
-      const uint32_t cbytes = vb * NB;
-      const uint32_t sbytes = (vb * 8 + 15) & ~15u;   // stays inside the 256-byte padding
+      uint64_t policy, off_codes, off_scales;
+      uint32_t cbytes, sbytes;
+      if (!kKeepTile || ip == 0) {
+        int64_t tb0;
+        int tvb;
+        ww.tile(it_t, tb0, tvb);
+        const uint32_t vb = static_cast<uint32_t>(tvb);
+        off_codes = static_cast<uint64_t>(tb0) * NB;
+        off_scales = a.scales_off + static_cast<uint64_t>(tb0) * 8;
+        cbytes = vb * NB;
+        sbytes = (vb * 8 + 15) & ~15u;   // stays inside the 256-byte padding
+        if constexpr (kKeepTile) {
+          k_codes = off_codes;
+          k_scales = off_scales;
+          k_cbytes = cbytes;
+          k_sbytes = sbytes;
+        }
+      }
+      if constexpr (kKeepTile) {
+        policy = k_policy;
+        off_codes = k_codes;
+        off_scales = k_scales;
+        cbytes = k_cbytes;
+        sbytes = k_sbytes;
+      } else {
+        policy = l2_evict_first_policy();
+      }
       const uint32_t dst = stage0 + is * kStageBytes;
       const uint32_t bar = bar0 + 8 * is;
       const uint8_t* base = shard_of[ip];
-      const uint64_t policy = l2_evict_first_policy();
       fence_proxy_async_smem();
       mbar_arrive_expect_tx(bar, cbytes + sbytes);
-      tma_load_1d(dst, base + tb0 * NB, cbytes, bar, policy);
-      tma_load_1d(dst + kCodesBytes, base + a.scales_off + tb0 * 8, sbytes, bar, policy);
+      tma_load_1d(dst, base + off_codes, cbytes, bar, policy);
+      tma_load_1d(dst + kCodesBytes, base + off_scales, sbytes, bar, policy);
     }
     ++issued;
     is = (is + 1 == D) ? 0 : is + 1;
