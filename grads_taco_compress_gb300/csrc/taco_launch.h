@@ -13,8 +13,11 @@ namespace taco {
 constexpr int kCompressThreads = 256;
 constexpr int kCompressMinBlocks = 2;     // CTAs per SM the register budget allows
 constexpr int kCompressStages = 3;        // warp tiles (4 KB each) in flight per warp
-constexpr int kDecompressThreads = 256;
-constexpr int kDecompressMinBlocks = 2;
+// Decompress-reduce: 16 warps in one CTA per SM (213.5 KB of stages and
+// output buffers). Two CTAs of 8 warps per SM measured slower: the warps of
+// the CTA resident first were favoured and the other CTA finished alone.
+constexpr int kDecompressThreads = 512;
+constexpr int kDecompressMinBlocks = 1;
 constexpr int kDecompressStages = 4;      // (tile, shard) stages in flight per warp
 constexpr int kVariants = 3;              // DUAL, ABSMAX, STATIC
 // Tensor-core compress: a producer warp, an MMA warp, groups of 4 epilogue
