@@ -92,6 +92,38 @@ def test_mma_sixteen_shards():
     check_compress_against_oracle(x, 128, entry=MMA)
 
 
+@pytest.mark.parametrize("P,N,h,block", [(16, 2048, 1024, 64), (3, 40 * 128 // 16, 1024, 64), (5, 20000, 768, 256)])
+def test_mma_tile_schedule(P, N, h, block):
+    """Shapes that drive the tile schedule through its cases: 16 shards (a few
+    CTAs per shard, a claimed pool of about a quarter of the tiles), one tile
+    per CTA (empty pool) and a ragged last tile in the pool. Every element
+    against the CUDA-core compress, sampled rows against the oracle; a second
+    call on the same workspace gives the same bytes."""
+    rng = np.random.default_rng(P * 1000 + N)
+    v = rng.laplace(0, 0.05, size=(P, N, h)).astype(np.float32)
+    v[:, ::7, 3] *= 200.0
+    x = W.f32_to_bf16_bits(v)
+    ws = tb.new_workspace(P)
+    xd = dev_bf16(x)
+    b1, h1 = MMA(xd, block, workspace=ws)
+    b2, h2 = MMA(xd, block, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(b1, b2) and torch.equal(h1, h2)
+    assert int(ws.count_nonzero()) == 0
+    codes, alpha, s_, hdr, _ = gpu_compress(x, block, entry=MMA)
+    fc, fa, fs, _, _ = gpu_compress(x, block)
+    rows = _sample_rows(N, seed=P)
+    for p in range(P):
+        parity.compare_codes(codes[p], fc[p], f"codes[{p}] vs CUDA-core path")
+        parity.compare_scales(alpha[p], fa[p], f"alpha[{p}] vs CUDA-core path")
+        parity.compare_scales(s_[p], fs[p], f"s[{p}] vs CUDA-core path")
+        oc, oa, os_, _ = O.compress(x[p][rows], block, E_STAR)
+        parity.compare_codes(codes[p][rows], oc, f"codes[{p}] vs oracle")
+        parity.compare_scales(s_[p][rows], os_, f"s[{p}] vs oracle")
+        assert hdr[p]["s_max"] == s_[p].max()
+        assert hdr[p]["n_clamped"] == np.count_nonzero(s_[p] > 1.0)
+
+
 def test_mma_empty_tensor():
     x = torch.empty((3, 0, 128), dtype=torch.bfloat16, device="cuda")
     _, headers = MMA(x, 64)
