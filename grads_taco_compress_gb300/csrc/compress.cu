@@ -233,8 +233,6 @@ void (*kernel_fn(int variant))(CompressArgs) {
 
 }  // namespace
 
-int compress_tile_blocks(int block) { return 32 / (block / 64); }
-
 size_t compress_smem_bytes() {
   return static_cast<size_t>(kCompressThreads / 32) * kCompressStages * (kTileElems * 2 + 8);
 }

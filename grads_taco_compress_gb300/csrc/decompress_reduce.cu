@@ -317,8 +317,6 @@ decompress_reduce_kernel(DecompressArgs a) {
 
 }  // namespace
 
-int decompress_tile_blocks(int block) { return 32 / (block / 64); }
-
 size_t decompress_smem_bytes() {
   return static_cast<size_t>(kDecompressThreads / 32) *
          (kDecompressStages * (kStageBytes + 8) + kOutBytes);

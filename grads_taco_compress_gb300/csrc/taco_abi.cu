@@ -139,6 +139,16 @@ Layout shard_layout(int64_t N, int64_t h, int block) {
   return l;
 }
 
+// CTAs for a CUDA-core kernel of `warps` warps per CTA over `nblocks` blocks:
+// enough that every warp gets at least kMinWarpBlocks blocks (its share of a
+// grid-stride pass may be a partial tile), so that small tensors still spread
+// over many SMs; the caller caps it at the resident CTAs.
+constexpr int64_t kMinWarpBlocks = 4;
+int64_t ctas_wanted(int64_t nblocks, int warps) {
+  const int64_t per_cta = static_cast<int64_t>(warps) * kMinWarpBlocks;
+  return (nblocks + per_cta - 1) / per_cta;
+}
+
 taco_status decompress_common(const uint8_t* const* shards, int P, int64_t N, int64_t h,
                               int block, void* out, void* stream, int fmt = 0, bool mma = false) {
   taco_status st = check_shape(N, h, block);
@@ -177,8 +187,7 @@ taco_status decompress_common(const uint8_t* const* shards, int P, int64_t N, in
                ? TACO_OK
                : TACO_ERR_CUDA;
   }
-  const int64_t tiles = (a.nblocks + decompress_tile_blocks(block) - 1) / decompress_tile_blocks(block);
-  const int64_t needed = (tiles + kDecompressThreads / 32 - 1) / (kDecompressThreads / 32);
+  const int64_t needed = ctas_wanted(a.nblocks, kDecompressThreads / 32);
   int64_t grid = static_cast<int64_t>(info->sms) * info->occ_decompress[block_index(block)][fmt];
   if (grid > needed) grid = needed;
   if (grid < 1) grid = 1;
@@ -212,9 +221,7 @@ taco_status decompress_shards_common(const uint8_t* const* shards, int P, int64_
   a.inv_sqrt_n = static_cast<float>(1.0 / std::sqrt(static_cast<double>(block)));
   const DeviceInfo* info = nullptr;
   if (device_info(&info) != cudaSuccess) return TACO_ERR_CUDA;
-  const int tb = decompress_tile_blocks(block);
-  const int64_t tiles = (a.nblocks + tb - 1) / tb;
-  const int64_t needed = (tiles + kDecompressThreads / 32 - 1) / (kDecompressThreads / 32);
+  const int64_t needed = ctas_wanted(a.nblocks, kDecompressThreads / 32);
   const int64_t total = static_cast<int64_t>(info->sms) * info->occ_gather[block_index(block)][fmt];
   int64_t gx = (total + P - 1) / P;
   if (gx > needed) gx = needed;
@@ -275,9 +282,7 @@ taco_status reduce_recompress_common(const uint8_t* const* shards, int P, int64_
 
   const DeviceInfo* info = nullptr;
   if (device_info(&info) != cudaSuccess) return TACO_ERR_CUDA;
-  const int tb = decompress_tile_blocks(block);
-  const int64_t tiles = (a.nblocks + tb - 1) / tb;
-  const int64_t needed = (tiles + kDecompressThreads / 32 - 1) / (kDecompressThreads / 32);
+  const int64_t needed = ctas_wanted(a.nblocks, kDecompressThreads / 32);
   const int64_t total =
       static_cast<int64_t>(info->sms) * info->occ_recompress[block_index(block)][variant][fmt];
   int64_t grid = (total + Y - 1) / Y;
@@ -419,9 +424,7 @@ taco_status taco_compress_shards(const void* x_bf16, int P, int64_t N, int64_t h
   if (st != TACO_OK) return st;
   const DeviceInfo* info = nullptr;
   if (device_info(&info) != cudaSuccess) return TACO_ERR_CUDA;
-  const int tb = compress_tile_blocks(block);
-  const int64_t tiles = (a.nblocks + tb - 1) / tb;
-  const int64_t needed = (tiles + kCompressThreads / 32 - 1) / (kCompressThreads / 32);
+  const int64_t needed = ctas_wanted(a.nblocks, kCompressThreads / 32);
   const int64_t total = static_cast<int64_t>(info->sms) * info->occ_compress[block_index(block)][variant];
   int64_t gx = (total + P - 1) / P;
   if (gx > needed) gx = needed;

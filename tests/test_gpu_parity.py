@@ -163,8 +163,19 @@ def test_compress_single_equals_shards():
     sb = tb.shard_bytes(64, w.h, w.block)
     for p in range(3):
         shard, header = tb.taco_compress(dev_bf16(x[p]), w.block)
-        assert torch.equal(shard[:sb], bundle[p, :sb])
-        assert torch.equal(header, headers[p])
+        assert same_outputs(shard[None, :sb], header, bundle[p:p + 1, :sb], headers[p], 1, 64, w.h, w.block)
+
+
+def same_outputs(b1, h1, b2, h2, P, N, h, block):
+    """Two compress results hold the same codes, scale pairs and headers, bit
+    for bit. The bundle's alignment padding is never written, so it is not
+    compared."""
+    v1 = tb.shard_views(b1, P, N, h, block)
+    v2 = tb.shard_views(b2, P, N, h, block)
+    same = all(torch.equal(a.view(torch.uint8 if a.dtype == torch.uint8 else torch.int32),
+                           b.view(torch.uint8 if b.dtype == torch.uint8 else torch.int32))
+               for a, b in zip(v1, v2))
+    return same and torch.equal(h1, h2)
 
 
 def test_compress_deterministic_and_workspace_reset():
@@ -174,7 +185,7 @@ def test_compress_deterministic_and_workspace_reset():
     b1, h1 = tb.taco_compress_shards(x, w.block, workspace=ws)
     b2, h2 = tb.taco_compress_shards(x, w.block, workspace=ws)
     torch.cuda.synchronize()
-    assert torch.equal(b1, b2) and torch.equal(h1, h2)
+    assert same_outputs(b1, h1, b2, h2, 2, 300, w.h, w.block)
     assert int(ws.count_nonzero()) == 0      # counters and running totals
 
 
