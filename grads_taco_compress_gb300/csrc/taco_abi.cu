@@ -79,8 +79,11 @@ cudaError_t device_info(const DeviceInfo** out) {
                                                               kCompressThreads, csmem);
       }
       for (int f = 0; f < kFormats && err == cudaSuccess; ++f) {
-        const void* k = decompress_kernel_ptr(blocks[b], f);
+        const void* k = decompress_kernel_ptr(blocks[b], f, false);
         err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dsmem);
+        if (err == cudaSuccess)
+          err = cudaFuncSetAttribute(decompress_kernel_ptr(blocks[b], f, true),
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, dsmem);
         if (err == cudaSuccess)
           err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ_decompress[b][f], k,
                                                               kDecompressThreads, dsmem);

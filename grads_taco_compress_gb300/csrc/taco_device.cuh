@@ -254,6 +254,45 @@ struct WarpWork {
   }
 };
 
+// The warp tiles of one CTA as a list that its warps claim in order (a
+// shared-memory counter), so that warps the scheduler favours take more of
+// them. The list holds the tiles a static split would give the CTA's warps:
+// `rounds` full grid-stride rounds (item i: round i / warps, warp slot
+// i % warps), then the CTA's even share of the blocks left over, a
+// contiguous range on 4-block boundaries cut into tiles of bpt blocks (the
+// last may be shorter).
+struct CtaWork {
+  int64_t W, bpt, c, warps;   // warps of the grid, blocks per tile, CTA, warps per CTA
+  int64_t n_full;             // full-round items
+  int64_t lo, hi;             // this CTA's share of the rest, absolute blocks
+  int64_t total;              // items of this CTA
+
+  __device__ __forceinline__ CtaWork(int64_t nblocks, int64_t c_, int64_t G, int warps_, int bpt_)
+      : W(G * warps_), bpt(bpt_), c(c_), warps(warps_) {
+    const int64_t rounds = nblocks / (W * bpt);
+    const int64_t rem0 = rounds * W * bpt;
+    const int64_t rest = nblocks - rem0;
+    n_full = rounds * warps;
+    lo = rem0 + ((rest * c / G) & ~int64_t{3});
+    hi = rem0 + ((c + 1 == G) ? rest : ((rest * (c + 1) / G) & ~int64_t{3}));
+    if (hi < lo) hi = lo;
+    total = n_full + (hi - lo + bpt - 1) / bpt;
+  }
+  // first block and number of blocks of item i; false past the end
+  __device__ __forceinline__ bool item(int64_t i, int64_t& b0, int& vb) const {
+    if (i >= total) return false;
+    if (i < n_full) {
+      b0 = ((i / warps) * W + c * warps + i % warps) * bpt;
+      vb = static_cast<int>(bpt);
+    } else {
+      b0 = lo + (i - n_full) * bpt;
+      const int64_t left = hi - b0;
+      vb = static_cast<int>(left < bpt ? left : bpt);
+    }
+    return true;
+  }
+};
+
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -22,6 +22,7 @@ constexpr int kCompressStages = 3;        // warp tiles (4 KB each) in flight pe
 constexpr int kDecompressThreads = 512;
 constexpr int kDecompressMinBlocks = 1;
 constexpr int kDecompressStages = 4;      // (tile, shard) stages in flight per warp
+constexpr int64_t kClaimRounds = 3;      // decompress-reduce: claimed tiles from this many rounds per warp
 constexpr int kVariants = 3;              // DUAL, ABSMAX, STATIC
 // Tensor-core compress: a producer warp, an MMA warp, groups of 4 epilogue
 // warps (one accumulator of `block` TMEM columns per group) and a tile
@@ -91,7 +92,7 @@ cudaError_t launch_compress_mma(const CompressArgs& a, int block, int variant, i
 cudaError_t compress_mma_fault(unsigned int* bits, bool clear);
 
 size_t decompress_smem_bytes();
-const void* decompress_kernel_ptr(int block, int fmt);
+const void* decompress_kernel_ptr(int block, int fmt, bool claim);
 cudaError_t launch_decompress(const DecompressArgs& a, int block, int fmt, int grid,
                               cudaStream_t stream);
 const void* recompress_kernel_ptr(int block, int variant, int fmt);

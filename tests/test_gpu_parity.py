@@ -329,6 +329,34 @@ def test_full_size_decompress_reduce_sampled(name):
     assert np.all(np.isfinite(O.bf16_bits_to_f64(got)))
 
 
+@pytest.mark.parametrize("name", [n for n in FULL if n != "tiny-512x1024"])
+def test_full_size_decompress_reduce_every_element(name):
+    """Every output element of the full-size decompress-reduce is written and
+    equals the sum of the P shards expanded on their own (taco_decompress_shards),
+    within the bf16 roundings of the expansions. On the large workloads the
+    warps claim their CTA's tiles in order; a tile skipped or taken twice would
+    show here, where sampled rows could miss it."""
+    w = W.WORKLOADS[name]
+    codes, alpha, s = W.make_random_bundle(w.N, w.h, w.block, w.P, seed=6)
+    bundle = bundle_from_arrays(codes, alpha, s, w.block)
+    out = torch.full((w.N, w.h), 0x7FC0, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    tb.taco_decompress_reduce(bundle, w.P, w.N, w.h, w.block, out=out)
+    parts = tb.taco_decompress_shards(bundle, w.P, w.N, w.h, w.block).float()
+    torch.cuda.synchronize()
+    got = out.float()
+    assert bool(torch.isfinite(got).all())
+    want = parts.sum(dim=0)
+    # the bf16 roundings of the P expansions and of the sum (half an ulp:
+    # up to 2^-8 relative each, 8 significant bits), plus the fp32 rounding
+    # of both sides' Hadamard sums, which is relative to the block's
+    # magnitude, not to the element's; a tile skipped or taken twice is off
+    # by the whole value
+    mag = parts.abs().sum(dim=0)
+    bound = mag * 2.0 ** -7 + mag.max() * 2.0 ** -14
+    excess = ((got - want).abs() - bound).max().item()
+    assert excess <= 0.0, f"worst excess over the bound {excess:.3e} (max magnitude {mag.max().item():.3e})"
+
+
 def test_no_kernel_wait_timed_out():
     """After every launch above, no bounded wait of any kernel gave up."""
     assert tb.taco_get_fault() == 0
