@@ -427,13 +427,14 @@ cudaError_t launch_decompress(const DecompressArgs& a, int block, int fmt, int g
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  // Warps with at least kClaimRounds full grid-stride rounds claim their
-  // CTA's tiles in order (the warps the scheduler favours take more): 2-2.6%
-  // faster on the large tensors measured; with fewer rounds the fixed share
-  // per warp measured faster.
+  // With E4M3 codes, warps with at least kClaimRounds full grid-stride
+  // rounds claim their CTA's tiles in order (the warps the scheduler favours
+  // take more): 2-2.6% faster on the large tensors measured. With fewer
+  // rounds, and for the INT8 codes (2% slower claimed on gpt3-act), the fixed
+  // share per warp measured faster.
   const int64_t bpt = 32 / (block / 64);
   const int64_t rounds = a.nblocks / (static_cast<int64_t>(grid) * (kDecompressThreads / 32) * bpt);
-  void (*kern)(DecompressArgs) = decompress_fn(block, fmt, rounds >= kClaimRounds);
+  void (*kern)(DecompressArgs) = decompress_fn(block, fmt, fmt == 0 && rounds >= kClaimRounds);
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
