@@ -93,14 +93,24 @@ KERNEL_SOURCES = {
 COMMON_SOURCES = ("taco_device.cuh", "taco_launch.h", "taco_abi.cu")
 
 
+_C_COMMENT = re.compile(r"/\*.*?\*/|//[^\n]*", re.S)
+
+
+def _code_only(text: str) -> bytes:
+    """C/C++ source without comments and trailing blanks: what the compiler sees."""
+    lines = [ln.rstrip() for ln in _C_COMMENT.sub("", text).splitlines()]
+    return "\n".join(ln for ln in lines if ln).encode()
+
+
 def source_hash(kernel: str) -> str:
-    """Hash of one kernel's sources: ties an ncu traffic figure to the kernel it measured."""
+    """Hash of one kernel's sources, comments left out: ties an ncu traffic
+    figure to the code it measured."""
     h = hashlib.sha256()
     csrc = ROOT / "grads_taco_compress_gb300" / "csrc"
     for name in (KERNEL_SOURCES[kernel], *COMMON_SOURCES):
         h.update(name.encode())
-        h.update((csrc / name).read_bytes())
-    h.update((ROOT / "include" / "taco.h").read_bytes())
+        h.update(_code_only((csrc / name).read_text()))
+    h.update(_code_only((ROOT / "include" / "taco.h").read_text()))
     return h.hexdigest()[:16]
 
 

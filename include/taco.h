@@ -107,8 +107,9 @@ size_t taco_workspace_bytes(int P);
  * bytes) and its header at `header_out` (device, 8-byte aligned).
  *   block          n, one of 64, 128, 256
  *   target_energy  E* > 0, the per-element energy of every rescaled block
- *                  (TACO pt summary §2.B.1: "normalise the energy to a
- *                  target level"); 4096 puts the rotated RMS at 64 code units
+ *                  (TACO pt summary §2.B.1: each block is rescaled to one
+ *                  common energy level); 4096 puts the rotated RMS at 64
+ *                  code units
  *   variant        TACO_VARIANT_DUAL, TACO_VARIANT_ABSMAX or TACO_VARIANT_STATIC
  * N == 0 is valid: no code is written and the header reports s_max = 0. */
 taco_status taco_compress(const void* x_bf16, int64_t N, int64_t h, int block,
