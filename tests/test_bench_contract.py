@@ -60,3 +60,17 @@ def test_gpu_arm_line():
                  "decompress_reduce_int8", "decompress_reduce_mma", "emulated_two_shot_allreduce"):
         assert line["kernels"][name]["us"] > 0, name
     assert line["e2e"]["h2d_bytes_per_step"] == 4 * 8192 * 1600 * 2
+
+
+def test_profile_hash_ignores_comments():
+    """The hash that ties a committed ncu traffic figure to its kernel covers
+    code only: a comment edit keeps it, a code edit changes it."""
+    sys.path.insert(0, str(ROOT))
+    import bench
+    a = "int f(int x) {  // scale\n  /* twice */ return 2 * x;\n}\n"
+    b = "// a new comment\nint f(int x) {\n  return 2 * x;   /* the same code */\n}\n"
+    c = "int f(int x) {\n  return 3 * x;\n}\n"
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only(a) != bench._code_only(c)
+    for kernel in ("compress", "compress_fwht", "decompress_reduce", "reduce_recompress"):
+        assert len(bench.source_hash(kernel)) == 16
