@@ -67,7 +67,7 @@ def test_profile_hash_ignores_comments():
     code only: a comment edit keeps it, a code edit changes it."""
     sys.path.insert(0, str(ROOT))
     import bench
-    a = "int f(int x) {  // scale\n  /* twice */ return 2 * x;\n}\n"
+    a = "int f(int x) {  // scale\n  /* twice */return 2 * x;\n}\n"
     b = "// a new comment\nint f(int x) {\n  return 2 * x;   /* the same code */\n}\n"
     c = "int f(int x) {\n  return 3 * x;\n}\n"
     assert bench._code_only(a) == bench._code_only(b)
