@@ -8,9 +8,11 @@
 //   x_hat  = bf16( H_n z )                                 (one inverse rotation)
 // H_n / sqrt(n) is symmetric and orthogonal, so it is its own inverse, and the
 // sum can be taken before the rotation because the rotation is linear.
-// Each warp walks warp tiles (2048 elements) in grid-stride rounds and then
-// an even share of the blocks left over (WarpWork). For one tile it consumes
-// P stages, one per shard; lane 0 keeps
+// One CTA of 16 warps per SM. Each warp walks warp tiles (2048 elements) in
+// grid-stride rounds and then an even share of the blocks left over
+// (WarpWork); with CLAIM (E4M3 decompress-reduce, at least kClaimRounds full
+// rounds per warp) the warps of a CTA claim the same tiles in order instead
+// (CtaWork). For one tile a warp consumes P stages, one per shard; lane 0 keeps
 // kDecompressStages stages in flight, each a pair of 1-D cp.async.bulk
 // copies (the tile's codes and its (alpha, s) pairs) completed on one mbarrier.
 // Codes are decoded in pairs with cvt.rn.f16x2.e4m3x2 (FMT 0) or, for the
