@@ -70,6 +70,9 @@ cudaError_t device_info(const DeviceInfo** out) {
     const int blocks[3] = {64, 128, 256};
     const int csmem = static_cast<int>(compress_smem_bytes());
     const int dsmem = static_cast<int>(decompress_smem_bytes());
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(decompress_pw_kernel_ptr(), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(decompress_pw_smem_bytes()));
     for (int b = 0; b < 3 && err == cudaSuccess; ++b) {
       for (int v = 0; v < kVariants && err == cudaSuccess; ++v) {
         const void* k = compress_kernel_ptr(blocks[b], v);

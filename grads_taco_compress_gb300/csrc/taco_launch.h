@@ -93,6 +93,9 @@ cudaError_t compress_mma_fault(unsigned int* bits, bool clear);
 
 size_t decompress_smem_bytes();
 const void* decompress_kernel_ptr(int block, int fmt, bool claim);
+// decompress-reduce of E4M3 codes of 64-element blocks (producer warp)
+size_t decompress_pw_smem_bytes();
+const void* decompress_pw_kernel_ptr();
 cudaError_t launch_decompress(const DecompressArgs& a, int block, int fmt, int grid,
                               cudaStream_t stream);
 const void* recompress_kernel_ptr(int block, int variant, int fmt);
