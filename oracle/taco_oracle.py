@@ -19,7 +19,8 @@ Compress, per block of ``n`` contiguous elements of one row
    [PT] §2.B.2 "Dual-Scale quantization (DS)",
    [PT] §2.A   "Why FP8?" -> E4M3 )
   1. energy   E_k = raw (uncentred) second moment of the block, mean over n
-  2. alpha_k  = sqrt(E* / E_k), rounded once to fp32 (alpha_k = 1 if E_k = 0)
+  2. alpha_k  = sqrt(E* / E_k), rounded once to fp32 and kept inside
+              [2^-126, 2^126] (alpha_k = 1 if E_k = 0)
   3. rotate   y = (H_n / sqrt(n)) (alpha_k x), Sylvester H_n, rounded to fp32
   4. s_k      = max(1, max_i |y_i| / Q_max), Q_max = 448, rounded to fp32
   5. q_i      = E4M3 round-to-nearest-even with saturation of fp32(y_i / s_k)
@@ -57,6 +58,18 @@ Readings taken where the pages are silent (each one is a choice):
     below give 0x80).
   * The value handed to the E4M3 rounding is an fp32 number on both the
     oracle and the GPU path, so both take that integer decision in fp32.
+  * alpha is stored as an fp32 number, and the pages put no magnitude limit
+    on a block, so the rescale has to be defined where sqrt(E*/E_k) does not
+    fit: alpha_k is sqrt(E*/E_k) rounded to fp32 and then clamped to
+    [2^-126, 2^126], the range in which both alpha_k and 1/alpha_k are
+    normal fp32 numbers. A block whose energy is more than 2^252 away from
+    E* (for E* = 4096: an RMS below 2^-120, i.e. bf16 subnormals and the
+    smallest normals, or above 2^132, which bf16 cannot hold) is rescaled
+    only part of the way; its codes still decode with the alpha that was
+    applied, and no finite input gives a NaN or infinite code, alpha or s.
+    Inside the range the operator is exactly equivariant under powers of
+    two: compress(2^k x) has the codes and s of compress(x) and alpha
+    scaled by exactly 2^-k.
 
 Parity pins live in ``tests/test_oracle_pins.py`` (Hadamard against its
 closed form and scipy, the E4M3 codec against torch's float8_e4m3fn and the
@@ -77,6 +90,8 @@ Q_MAX_INT8 = 127.0
 FORMAT_E4M3 = 0
 FORMAT_INT8 = 1
 DEFAULT_TARGET_ENERGY = 4096.0
+ALPHA_MIN = 2.0 ** -126        # alpha and 1/alpha both normal fp32 numbers
+ALPHA_MAX = 2.0 ** 126
 VARIANT_DUAL = 0
 VARIANT_ABSMAX = 1
 VARIANT_STATIC = 2
@@ -265,10 +280,11 @@ def compress_values_stages(x_values: np.ndarray, block: int,
     # 1. block energy: raw second moment, mean over the block ([PT] §2.B.1)
     energy = np.sum(x * x, axis=-1) / n
 
-    # 2. pre-rotation scale alpha_k: energy of alpha_k x equals E* ([PT] §2.B.2)
+    # 2. pre-rotation scale alpha_k: energy of alpha_k x equals E* ([PT] §2.B.2),
+    #    as far as an fp32 alpha whose reciprocal is a normal fp32 number allows
     alpha = np.ones((N, K), dtype=np.float32)
     nz = energy > 0
-    alpha[nz] = np.sqrt(target_energy / energy[nz]).astype(np.float32)
+    alpha[nz] = np.clip(np.sqrt(target_energy / energy[nz]), ALPHA_MIN, ALPHA_MAX).astype(np.float32)
 
     # 3. orthogonal Hadamard rotation of the rescaled block ([PT] §2.B.1)
     H = sylvester_hadamard(n).astype(np.float64)

@@ -291,6 +291,118 @@ def check_static_variant(O):
         assert st["header"]["s_max"] == float(s_ref)
 
 
+# --------------------------------------------------------------------------
+# Blocks at the ends of the bf16 range: alpha kept inside [2^-126, 2^126]
+# --------------------------------------------------------------------------
+def _exact_pow2_scale(bits: np.ndarray, k: int) -> np.ndarray:
+    """bf16 patterns of 2^k x, exact (every |x| and |2^k x| a normal number)."""
+    v = (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64) * 2.0 ** k
+    return _bf16_bits(v.astype(np.float32))
+
+
+def check_power_of_two_equivariance(O):
+    """compress(2^k x) = compress(x) with alpha scaled by exactly 2^-k.
+
+    Energy, alpha and the rotation are homogeneous in x: E(2^k x) = 4^k E(x),
+    so sqrt(E*/E) scales by exactly 2^-k, and alpha x, y, s and the codes do
+    not change. This holds for k across the whole bf16 exponent range as long
+    as alpha stays inside [2^-126, 2^126]; an energy or alpha computed in a
+    narrower format than the input's range breaks it at one end.
+    """
+    rng = np.random.default_rng(22)
+    for n in (64, 128, 256):
+        v = rng.standard_normal((6, 2 * n)) * np.exp2(rng.uniform(-5, 5, (6, 2 * n)))
+        v = np.where(np.abs(v) < 2.0 ** -12, 2.0 ** -12, v)      # every |x| in [2^-12, 2^12]
+        x0 = (v.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+        x0[2, :n] = 0                                            # a zero block stays a zero block
+        for fmt in (O.FORMAT_E4M3, O.FORMAT_INT8):
+            for variant in O.VARIANTS:
+                c0, a0, s0, _ = O.compress(x0, n, E_STAR, variant, fmt)
+                for k in list(range(-112, 111, 9)) + [-113, 114]:
+                    ck, ak, sk, _ = O.compress(_exact_pow2_scale(x0, k), n, E_STAR, variant, fmt)
+                    assert np.array_equal(ck, c0), (n, fmt, variant, k)
+                    assert np.array_equal(sk, s0), (n, fmt, variant, k)
+                    want = np.where(a0 == 1.0, 1.0, a0.astype(np.float64) * 2.0 ** -k)
+                    want[2, 0] = 1.0
+                    assert np.array_equal(ak.astype(np.float64), want), (n, fmt, variant, k)
+
+
+def _extreme_rows():
+    for line in (GOLDEN / "extreme_blocks.txt").read_text().splitlines():
+        line = line.split("#")[0].strip()
+        if line:
+            n, case, c, E, alpha, s, code, recon = line.split()
+            ev = lambda t: float(eval(t, {"__builtins__": {}}, {}))
+            yield int(n), case, ev(c), ev(E), ev(alpha), float(s), int(code, 16), recon
+
+
+def check_alpha_clamp_closed_forms(O):
+    """Spike and constant blocks whose sqrt(E*/E) leaves [2^-126, 2^126]."""
+    for n, case, c, E, alpha_ref, s_ref, code, recon in _extreme_rows():
+        H = O.sylvester_hadamard(n)
+        j = 5
+        xv = np.zeros(n, dtype=np.float64)
+        if case == "spike":
+            xv[j] = c
+            want = np.where(np.sign(c) * H[:, j] > 0, code, code | 0x80)
+        else:
+            xv[:] = c
+            want = np.zeros(n, dtype=np.int64)
+            want[0] = code if c > 0 else code | 0x80
+        x = _bf16_bits(xv.astype(np.float32))[None, :]
+        codes, alpha, s, _ = O.compress(x, n, E)
+        assert float(alpha[0, 0]) == alpha_ref, (n, case, c, float(alpha[0, 0]))
+        assert float(s[0, 0]) == s_ref, (n, case, c)
+        got = codes[0].astype(np.int64)
+        nonzero = want & 0x7F != 0
+        assert np.array_equal(got[nonzero], want[nonzero]), (n, case, c)
+        assert np.all(got[~nonzero] & 0x7F == 0), (n, case, c)
+        rec = O.decompress_reduce(codes[None], alpha[None], s[None], n)
+        if recon == "exact":
+            assert np.array_equal(rec, x), (n, case, c)
+        elif recon == "zero":
+            assert np.all(O.bf16_bits_to_f64(rec) == 0.0), (n, case, c)
+
+
+def check_extreme_magnitudes(O):
+    """Blocks anywhere in the bf16 range, subnormals included.
+
+    No finite input gives a NaN code, alpha stays inside [2^-126, 2^126], s is
+    finite (>= 1 for the dual scale), and the reconstruction is within the
+    E4M3 error of the alpha and s actually stored: per block
+      ||x_hat - x||_2 <= (s / alpha) (||max(|r| 2^-4, 2^-10)||_2 + 2^-22 ||r||_2),
+    r = y / s the value rounded to E4M3 (half a step: 2^-4 relative in the
+    normal range, 2^-10 in the subnormal range; 2^-22 covers the two fp32
+    roundings of y and y / s), since the rotation is orthonormal.
+    """
+    rng = np.random.default_rng(23)
+    for n in (64, 128, 256):
+        rows, K = 40, 3
+        ex = rng.integers(-134, 127, size=(rows, K, 1)).astype(np.float64)
+        v = rng.standard_normal((rows, K, n)) * np.exp2(ex)
+        v[::5, 1, :] = 0.0
+        v[1::5, 1, :] *= np.exp2(rng.uniform(-40, 0, (len(v[1::5]), n)))   # wide range inside a block
+        v[2::5, 2, 7] = 3.0e38                                              # one huge element
+        v = np.clip(v, -3.3e38, 3.3e38).reshape(rows, K * n)
+        x = (v.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+        xv = O.bf16_bits_to_f64(x).reshape(rows, K, n)
+        for variant in O.VARIANTS:
+            st = O.compress_stages(x, n, E_STAR, variant)
+            codes, alpha, s = st["codes"], st["alpha"].astype(np.float64), st["s"].astype(np.float64)
+            assert not np.any((codes & 0x7F) == 0x7F), (n, variant)
+            assert np.all(np.isfinite(alpha)) and np.all((alpha >= 2.0 ** -126) & (alpha <= 2.0 ** 126))
+            assert np.all(np.isfinite(s)) and np.all(s > 0)
+            if variant == O.VARIANT_DUAL:
+                assert np.all(s >= 1.0)
+            rec = O.decompress_reduce_f64(codes[None], st["alpha"][None], st["s"][None], n)
+            err = np.linalg.norm(rec.reshape(rows, K, n) - xv, axis=-1)
+            r = st["y"].astype(np.float64) / s[..., None]
+            half_step = np.maximum(np.abs(r) * 2.0 ** -4, 2.0 ** -10)
+            bound = (s / alpha) * (np.linalg.norm(half_step, axis=-1)
+                                   + 2.0 ** -22 * np.linalg.norm(r, axis=-1))
+            assert np.all(err <= bound * (1 + 1e-9)), (n, variant, float(np.max(err / bound)))
+
+
 def _nearest_int_tie_even(v: float) -> int:
     """Nearest integer by comparing the two neighbours (no library rounding)."""
     lo = math.floor(v)

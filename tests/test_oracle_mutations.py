@@ -48,6 +48,14 @@ MUTATIONS = {
     "int8_scale_uses_fp8_qmax": ("    qm = q_max(fmt)\n", "    qm = Q_MAX\n"),
     "recompress_skips_alpha": ("    st = compress_values_stages(x_hat, block, target_energy, variant, fmt)\n    return st[\"codes\"], st[\"alpha\"]",
                                "    st = compress_values_stages(x_hat, block, target_energy, variant, fmt)\n    return st[\"codes\"], st[\"alpha\"] * 0 + 1"),
+    "energy_in_fp32": ("energy = np.sum(x * x, axis=-1) / n",
+                       "energy = np.sum(x.astype(np.float32) ** 2, axis=-1, dtype=np.float32).astype(np.float64) / n"),
+    "alpha_unclamped": ("np.clip(np.sqrt(target_energy / energy[nz]), ALPHA_MIN, ALPHA_MAX)",
+                        "np.sqrt(target_energy / energy[nz])"),
+    "alpha_clamp_at_fp32_max": ("ALPHA_MAX = 2.0 ** 126", "ALPHA_MAX = float(np.finfo(np.float32).max)"),
+    "alpha_clamp_low_subnormal": ("ALPHA_MIN = 2.0 ** -126", "ALPHA_MIN = 2.0 ** -149"),
+    "alpha_applied_unclamped": ("    scaled = alpha.astype(np.float64)[..., None] * x\n",
+                                "    scaled = np.where(energy > 0, np.sqrt(target_energy / np.where(energy > 0, energy, 1.0)), 1.0)[..., None] * x\n"),
 }
 
 
