@@ -114,57 +114,81 @@ compress_kernel(CompressArgs a) {
     const uint32_t stage = stage0 + cs * TILE_BYTES;
 
     f2 v[kCH][4];
-    {
-      const uint32_t base = stage + sub * (NB * 2);
+    float alpha, tmax;
+    // Pass 0 takes every block as it is. A non-zero block whose sum of
+    // squares is not a trusted fp32 number (subnormal squares, or a sum or
+    // transform that may overflow) makes the warp run a second pass over the
+    // same stage, with that block scaled by 2^-k (k the exponent of its max
+    // |t| from pass 0, 128 if that overflowed; exact) and 2^-k put back into
+    // alpha. The other blocks keep k = 0 and repeat pass 0's arithmetic.
+    int k_exp = 0;
+    for (int pass = 0;; ++pass) {
+      const int nk = -k_exp, nk1 = nk >> 1;            // 2^-k = 2^nk1 2^(nk - nk1), both normal
+      const float p1 = exp2i(nk1), p2 = exp2i(nk - nk1);
+      {
+        const uint32_t base = stage + sub * (NB * 2);
+        const f2 s1{p1, p1}, s2{p2, p2};
+#pragma unroll
+        for (int q = 0; q < kCH; ++q) {
+          const uint4 r = lds128(base + 16 * (j + LPB * (q ^ cx)));
+          v[q][0] = f2{bf16_lo(r.x), bf16_hi(r.x)};
+          v[q][1] = f2{bf16_lo(r.y), bf16_hi(r.y)};
+          v[q][2] = f2{bf16_lo(r.z), bf16_hi(r.z)};
+          v[q][3] = f2{bf16_lo(r.w), bf16_hi(r.w)};
+          if (pass > 0) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[q][i] = mul2(mul2(v[q][i], s1), s2);
+          }
+        }
+      }
+
+      // Block energy e = sum x^2 (E = e / NB): four packed accumulators, then
+      // the lanes of the block.
+      f2 ea[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll
+      for (int q = 0; q < kCH; ++q)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ea[i] = fma2(v[q][i], v[q][i], ea[i]);
+      const f2 e01 = add2(ea[0], ea[1]), e23 = add2(ea[2], ea[3]);
+      const float e = block_sum<LPB>((e01.x + e01.y) + (e23.x + e23.y));
+
+      // alpha = sqrt(E*/E) = 2^-k sqrt(n E*) / sqrt(e): reciprocal square
+      // root with one Newton step (error about one ulp), kept in
+      // [2^-126, 2^126]; 1 for an all-zero block. It does not depend on the
+      // rotation, so its latency overlaps the FWHT.
+      float r = rsqrtf(e);
+      r = fmaf(fmaf(-0.5f * e * r, r, 0.5f), r, r);
+      alpha = (e > 0.f) ? clamp_alpha(a.sqrt_nE * r * p1 * p2) : 1.0f;
+
+      // Rotation of the (scaled) block: t = H x.
+      fwht_in_registers<kCH>(v, cx);
+      fwht_across_lanes<kCH, LPB>(v, j);
+
+      // max |t| = max(max t, -min t): a tree of 3-input max / min per chunk,
+      // then over the chunks.
+      float hq[kCH], lq[kCH];
 #pragma unroll
       for (int q = 0; q < kCH; ++q) {
-        const uint4 r = lds128(base + 16 * (j + LPB * (q ^ cx)));
-        v[q][0] = f2{bf16_lo(r.x), bf16_hi(r.x)};
-        v[q][1] = f2{bf16_lo(r.y), bf16_hi(r.y)};
-        v[q][2] = f2{bf16_lo(r.z), bf16_hi(r.z)};
-        v[q][3] = f2{bf16_lo(r.w), bf16_hi(r.w)};
+        hq[q] = max3(max3(v[q][0].x, v[q][0].y, v[q][1].x), max3(v[q][1].y, v[q][2].x, v[q][2].y),
+                     fmaxf(v[q][3].x, v[q][3].y));
+        lq[q] = min3(min3(v[q][0].x, v[q][0].y, v[q][1].x), min3(v[q][1].y, v[q][2].x, v[q][2].y),
+                     fminf(v[q][3].x, v[q][3].y));
       }
+      const float thi = max3(max3(hq[0], hq[1], hq[2]), max3(hq[3], hq[4], hq[5]), fmaxf(hq[6], hq[7]));
+      const float tlo = min3(min3(lq[0], lq[1], lq[2]), min3(lq[3], lq[4], lq[5]), fminf(lq[6], lq[7]));
+      tmax = block_max<LPB>(fmaxf(thi, -tlo));
+      if (pass > 0) break;
+      const bool far = !(e >= kEnergyLo && e <= kEnergyHi) && !(tmax == 0.f);
+      if (!__any_sync(kFullMask, far)) break;
+      // max |x| <= max |t| <= n max |x|: the scaled block's max lies in [2^-8, 2)
+      k_exp = far ? (tmax <= 0x1.fffffep127f ? ilogbf(tmax) : 128) : 0;
     }
+    // y = alpha 2^k t / sqrt(n): 2^k undoes the scaling of the block
+    const float cscale = alpha * exp2i((k_exp + 1) >> 1) * exp2i(k_exp - ((k_exp + 1) >> 1)) * a.inv_sqrt_n;
     if (++cs == D) {
       cs = 0;
       cphase ^= 1u;
     }
-
-    // Block energy e = sum x^2 (E = e / NB): four packed accumulators, then
-    // the lanes of the block.
-    f2 ea[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
-#pragma unroll
-    for (int q = 0; q < kCH; ++q)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) ea[i] = fma2(v[q][i], v[q][i], ea[i]);
-    const f2 e01 = add2(ea[0], ea[1]), e23 = add2(ea[2], ea[3]);
-    const float e = block_sum<LPB>((e01.x + e01.y) + (e23.x + e23.y));
-
-    // alpha = sqrt(E*/E) = sqrt(n E*) / sqrt(e): reciprocal square root with
-    // one Newton step (error about one ulp); 1 for an all-zero block. It does
-    // not depend on the rotation, so its latency overlaps the FWHT.
-    float r = rsqrtf(e);
-    r = fmaf(fmaf(-0.5f * e * r, r, 0.5f), r, r);
-    const float alpha = (e > 0.f) ? a.sqrt_nE * r : 1.0f;
-    const float cscale = alpha * a.inv_sqrt_n;        // y = cscale * t
-
-    // Rotation of the raw block: t = H x.
-    fwht_in_registers<kCH>(v, cx);
-    fwht_across_lanes<kCH, LPB>(v, j);
-
-    // max |t| = max(max t, -min t): a tree of 3-input max / min per chunk,
-    // then over the chunks.
-    float hq[kCH], lq[kCH];
-#pragma unroll
-    for (int q = 0; q < kCH; ++q) {
-      hq[q] = max3(max3(v[q][0].x, v[q][0].y, v[q][1].x), max3(v[q][1].y, v[q][2].x, v[q][2].y),
-                   fmaxf(v[q][3].x, v[q][3].y));
-      lq[q] = min3(min3(v[q][0].x, v[q][0].y, v[q][1].x), min3(v[q][1].y, v[q][2].x, v[q][2].y),
-                   fminf(v[q][3].x, v[q][3].y));
-    }
-    const float thi = max3(max3(hq[0], hq[1], hq[2]), max3(hq[3], hq[4], hq[5]), fmaxf(hq[6], hq[7]));
-    const float tlo = min3(min3(lq[0], lq[1], lq[2]), min3(lq[3], lq[4], lq[5]), fminf(lq[6], lq[7]));
-    const float tmax = block_max<LPB>(fmaxf(thi, -tlo));
 
     const float amax = cscale * tmax;
     const float sc = (VARIANT == 0)   ? fmaxf(1.0f, amax * (1.0f / 448.0f))

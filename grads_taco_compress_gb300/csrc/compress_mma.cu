@@ -170,10 +170,23 @@ __device__ __forceinline__ void slice_stats(const float (&u)[NC][SL], f2 (&ea)[4
   }
 }
 
+// u *= 2^-k (two exact power-of-two factors).
+template <int NC, int SL>
+__device__ __forceinline__ void scale_slice(float (&u)[NC][SL], f2 s1, f2 s2) {
+#pragma unroll
+  for (int c = 0; c < NC; ++c)
+#pragma unroll
+    for (int i = 0; i < SL; i += 2) {
+      const f2 t = mul2(mul2(f2{u[c][i], u[c][i + 1]}, s1), s2);
+      u[c][i] = t.x;
+      u[c][i + 1] = t.y;
+    }
+}
+
 // Codes of one slice into the group's staging atoms: chunk c of block row
 // `row` is 64 bytes at row * 64 of atom c, its 16-byte pieces permuted by the
 // 64-byte swizzle (piece ^= (row >> 1) & 3) that the tensor store undoes.
-template <int NC, int SL, int FMT>
+template <int NC, int SL, int FMT, bool CLAMP>
 __device__ __forceinline__ void slice_codes(const float (&u)[NC][SL], int slice, float g,
                                             uint32_t stage_codes, int row) {
   const f2 g2{g, g};
@@ -189,11 +202,114 @@ __device__ __forceinline__ void slice_codes(const float (&u)[NC][SL], int slice,
         const int i = q * 16 + 4 * k;
         const f2 y0 = mul2(f2{u[c][i], u[c][i + 1]}, g2);
         const f2 y1 = mul2(f2{u[c][i + 2], u[c][i + 3]}, g2);
-        w[k] = (FMT == 0) ? e4m3x4_from_f32(y0.x, y0.y, y1.x, y1.y) : i8x4_from_f32(y0, y1);
+        w[k] = (FMT == 0) ? e4m3x4_from_f32(y0.x, y0.y, y1.x, y1.y) : i8x4_from_f32<CLAMP>(y0, y1);
       }
       const int piece = (slice * SL) / 16 + q;
       sts128(rbase + c * kCodeAtomBytes + 16 * (piece ^ sw), make_uint4(w[0], w[1], w[2], w[3]));
     }
+}
+
+// How far the tensor cores' fp32 image t = H_n x of a block is used, by its
+// largest magnitude max |t| (>= max |x|, and 0 only for an all-zero block).
+// The tensor cores keep bf16 subnormal inputs and fp32 subnormal sums exact
+// (measured), and no partial sum of a block overflows while max |t| <= 2^119
+// (each is at most n max |x| <= 2^127).
+//   [2^-40, 2^56] or 0: t is squared and summed as it is (the squares that
+//       fall into fp32's subnormal range weigh less than 2^-60 of the sum);
+//   [2^-120, 2^119] otherwise: the sum of squares is taken again from
+//       tensor memory with t scaled by 2^-k (k = the exponent of max |t|,
+//       exact) and 2^-k goes back into alpha; t itself is used as it is
+//       (its subnormal grid is below 2^-29 max |t|, finer than a code);
+//   anything else (a block of bf16 subnormals only, or one whose rotation
+//       overflowed fp32): done again from x in global memory (exact_block).
+constexpr float kTrustLo = 0x1p-40f;
+constexpr float kTrustHi = 0x1p56f;
+constexpr float kRescaleLo = 0x1p-120f;
+constexpr float kRescaleHi = 0x1p119f;
+
+// One block from its bf16 values in global memory, for the thread that owns
+// its row of the tile: x scaled by 2^-k (k the exponent of max |x|, exact),
+// the energy from the scaled values, alpha = 2^-k sqrt(n E*) / sqrt(sum x'^2)
+// kept in [2^-126, 2^126], and the Hadamard transform t' of the scaled block
+// in fp32; the rotated values are then alpha 2^k t' / sqrt(n) for any
+// magnitude of x. Writes the block's codes into the row of the staging atoms
+// (the layout slice_codes writes) and returns (alpha, s). Rare by
+// construction, so it keeps the block in local memory and leaves the
+// register budget of the fast path alone.
+template <int NB, int VARIANT, int FMT>
+__device__ __noinline__ float2 exact_block(const uint16_t* __restrict__ xb, float sqrt_nE,
+                                           float inv_sqrt_n, float s_static, uint32_t stage_codes,
+                                           int row) {
+  constexpr float QMAX = (FMT == 0) ? 448.0f : 127.0f;
+  float v[NB];
+  float m = 0.0f;
+#pragma unroll 1
+  for (int i = 0; i < NB; i += 64) {
+    uint4 w[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) w[q] = __ldg(reinterpret_cast<const uint4*>(xb + i) + q);   // 8 loads in flight
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const uint32_t ws[4] = {w[q].x, w[q].y, w[q].z, w[q].w};
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        v[i + 8 * q + 2 * r] = bf16_lo(ws[r]);
+        v[i + 8 * q + 2 * r + 1] = bf16_hi(ws[r]);
+        m = max3(m, fabsf(bf16_lo(ws[r])), fabsf(bf16_hi(ws[r])));
+      }
+    }
+  }
+  float alpha = 1.0f, c = 0.0f, tm = 0.0f;
+  if (m > 0.0f) {
+    const int k = ilogbf(m);                  // m 2^-k in [1, 2)
+    f2 ea[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll 1
+    for (int i = 0; i < NB; i += 8) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const f2 xs{ldexpf(v[i + 2 * q], -k), ldexpf(v[i + 2 * q + 1], -k)};
+        v[i + 2 * q] = xs.x;
+        v[i + 2 * q + 1] = xs.y;
+        ea[q] = fma2(xs, xs, ea[q]);
+      }
+    }
+    const f2 e01 = add2(ea[0], ea[1]), e23 = add2(ea[2], ea[3]);
+    alpha = alpha_scaled(sqrt_nE, (e01.x + e01.y) + (e23.x + e23.y), k);
+    c = ldexpf(alpha, k) * inv_sqrt_n;        // rotated value = c t'
+#pragma unroll 1
+    for (int hs = 1; hs < NB; hs <<= 1)       // Sylvester order: t_j = sum_i (-1)^popc(i&j) x_i
+#pragma unroll 1
+      for (int i = 0; i < NB; i += 2 * hs)
+#pragma unroll 1
+        for (int j = i; j < i + hs; ++j) {
+          const float p = v[j], q = v[j + hs];
+          v[j] = p + q;
+          v[j + hs] = p - q;
+        }
+#pragma unroll 1
+    for (int i = 0; i < NB; ++i) tm = fmaxf(tm, fabsf(v[i]));
+  }
+  const float amax = c * tm;
+  const float sc = (VARIANT == 0)   ? fmaxf(1.0f, amax * (1.0f / QMAX))
+                   : (VARIANT == 1) ? (amax > 0.f ? amax * (1.0f / QMAX) : 1.0f)
+                                    : s_static;
+  const float g = __fdividef(c, sc);
+  const f2 g2{g, g};
+  const uint32_t rbase = stage_codes + row * 64;
+  const int sw = (row >> 1) & 3;
+#pragma unroll 1
+  for (int i = 0; i < NB; i += 16) {
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const f2 y0 = mul2(f2{v[i + 4 * q], v[i + 4 * q + 1]}, g2);
+      const f2 y1 = mul2(f2{v[i + 4 * q + 2], v[i + 4 * q + 3]}, g2);
+      w[q] = (FMT == 0) ? e4m3x4_from_f32(y0.x, y0.y, y1.x, y1.y) : i8x4_from_f32<VARIANT == 2>(y0, y1);
+    }
+    const int chunk = i >> 6, piece = (i & 63) >> 4;
+    sts128(rbase + chunk * kCodeAtomBytes + 16 * (piece ^ sw), make_uint4(w[0], w[1], w[2], w[3]));
+  }
+  return make_float2(alpha, sc);
 }
 
 template <int NB, int VARIANT, int FMT>
@@ -426,36 +542,81 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
       const f2 e01 = add2(ea[0], ea[1]), e23 = add2(ea[2], ea[3]);
       const float e = (e01.x + e01.y) + (e23.x + e23.y);   // = n * sum x^2
 
-      // alpha = sqrt(E* / E), E = e / n^2: n sqrt(E*) / sqrt(e), one Newton step
+      // alpha = sqrt(E* / E), E = e / n^2: n sqrt(E*) / sqrt(e), one Newton
+      // step, kept in [2^-126, 2^126]; 1 for an all-zero block
       float r = rsqrtf(e);
       r = fmaf(fmaf(-0.5f * e * r, r, 0.5f), r, r);
-      const float alpha = (e > 0.f) ? a.n_sqrtE * r : 1.0f;
-      const float cscale = alpha * a.inv_sqrt_n;             // y = cscale * t
+      float alpha = (e > 0.f) ? clamp_alpha(a.n_sqrtE * r) : 1.0f;
       const float thi = max3(hi[0], hi[1], fmaxf(hi[2], hi[3]));
       const float tlo = min3(lo[0], lo[1], fminf(lo[2], lo[3]));
-      const float amax = cscale * fmaxf(thi, -tlo);
-      const float sc = (VARIANT == 0)   ? fmaxf(1.0f, amax * (1.0f / QMAX))
-                       : (VARIANT == 1) ? (amax > 0.f ? amax * (1.0f / QMAX) : 1.0f)
-                                        : a.s_static;
-      const float gsc = __fdividef(cscale, sc);              // code value = gsc * t
+      const float tmx = fmaxf(thi, -tlo);
+      const bool fast = (tmx >= kTrustLo && tmx <= kTrustHi) || tmx == 0.f;
+      const bool rescale = !fast && tmx >= kRescaleLo && tmx <= kRescaleHi;
+      const bool exact = !fast && !rescale;       // NaN lands here too
+      // A rescaled block also takes its codes from 2^-k t with the factor
+      // times 2^k: t / s of a block of tiny t can exceed the fp32 range
+      // (ABSMAX: 448 / max |t|) although every code is finite. Lanes that
+      // need no rescale take k = 0, which changes nothing.
+      const bool any_rescale = __any_sync(kFullMask, rescale);
+      const int kr = rescale ? ilogbf(tmx) : 0;
+      const int nkr = -kr, nkr1 = nkr >> 1;       // 2^-k = 2^nkr1 2^(nkr - nkr1), both normal
+      const f2 s1{exp2i(nkr1), exp2i(nkr1)}, s2{exp2i(nkr - nkr1), exp2i(nkr - nkr1)};
+      if (any_rescale) {
+        // the sum of squares of 2^-k t, from tensor memory (the warp reads
+        // together)
+        const int k = kr;
+        f2 eb[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll 1
+        for (int sl = 0; sl < NC; ++sl) {
+          if constexpr (NC > 1) {
+            load_slice<NC, SL>(tacc, sl, u);
+            chunk_butterflies<NC, SL>(u);
+          }
+#pragma unroll
+          for (int c = 0; c < NC; ++c)
+#pragma unroll
+            for (int i = 0; i < SL; i += 2) {
+              const f2 t = mul2(mul2(f2{u[c][i], u[c][i + 1]}, s1), s2);
+              eb[(i >> 1) & 3] = fma2(t, t, eb[(i >> 1) & 3]);
+            }
+        }
+        const f2 f01 = add2(eb[0], eb[1]), f23 = add2(eb[2], eb[3]);
+        if (rescale) alpha = alpha_scaled(a.n_sqrtE, (f01.x + f01.y) + (f23.x + f23.y), k);
+      }
+      const float cscale = alpha * a.inv_sqrt_n;             // y = cscale * t
+      const float amax = cscale * tmx;
+      float sc = (VARIANT == 0)   ? fmaxf(1.0f, amax * (1.0f / QMAX))
+                 : (VARIANT == 1) ? (amax > 0.f ? amax * (1.0f / QMAX) : 1.0f)
+                                  : a.s_static;
+      const float gsc = __fdividef(ldexpf(cscale, kr), sc);  // code value = gsc * (2^-k t)
 
       // pass 2: codes (one slice: the values are still in registers)
       if constexpr (NC == 1) {
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(base + S::tempty + 8 * g);
-        slice_codes<NC, SL, FMT>(u, 0, gsc, staging, row);
+        if (any_rescale) scale_slice<NC, SL>(u, s1, s2);
+        slice_codes<NC, SL, FMT, VARIANT == 2>(u, 0, gsc, staging, row);
       } else {
 #pragma unroll 1
         for (int sl = 0; sl < NC; ++sl) {
           load_slice<NC, SL>(tacc, sl, u);
           chunk_butterflies<NC, SL>(u);
-          slice_codes<NC, SL, FMT>(u, sl, gsc, staging, row);
+          if (any_rescale) scale_slice<NC, SL>(u, s1, s2);
+          slice_codes<NC, SL, FMT, VARIANT == 2>(u, sl, gsc, staging, row);
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(base + S::tempty + 8 * g);
       }
+      if (exact && valid) {
+        const float2 as = exact_block<NB, VARIANT, FMT>(
+            a.x + static_cast<int64_t>(shard) * a.shard_elems + b * NB, a.sqrt_nE, a.inv_sqrt_n,
+            a.s_static, staging, row);
+        alpha = as.x;
+        sc = as.y;
+      }
+      __syncwarp();
       fence_proxy_async_smem();   // codes visible to the tensor store
       group_sync(1 + g);
       if (leader) {

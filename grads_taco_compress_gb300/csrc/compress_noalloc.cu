@@ -45,37 +45,21 @@ cudaError_t scratch_address(void** out) {
   return cudaSuccess;
 }
 
-inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
 }  // namespace
 
 extern "C" taco_status taco_compress_shards_noalloc(const void* x_bf16, int P, int64_t N, int64_t h,
                                                     int block, float target_energy, int variant,
                                                     void* bundle_out, taco_header* headers_out,
                                                     void* stream) {
-  // Checks that taco_compress_shards makes too, taken first so that a rejected
-  // call enqueues nothing (not even the scratch clear below).
-  if (block != 64 && block != 128 && block != 256) return TACO_ERR_BLOCK;
-  if (N < 0 || h <= 0 || h % block != 0 || (N > 0 && N > (int64_t{1} << 40) / h)) return TACO_ERR_SHAPE;
-  if (P < 1 || P > TACO_MAX_SHARDS) return TACO_ERR_ARG;
-  if (P > TACO_NOALLOC_MAX_SHARDS) return TACO_ERR_WORKSPACE;   // beyond the static scratch
-  if (variant != TACO_VARIANT_DUAL && variant != TACO_VARIANT_ABSMAX &&
-      variant != TACO_VARIANT_STATIC)
-    return TACO_ERR_ARG;
-  if (!(target_energy > 0.0f) || !std::isfinite(target_energy)) return TACO_ERR_ARG;
-  if (!headers_out) return TACO_ERR_NULL;
-  if (!aligned(headers_out, 8)) return TACO_ERR_ALIGN;
-  if (N > 0) {
-    if (!x_bf16 || !bundle_out) return TACO_ERR_NULL;
-    if (!aligned(x_bf16, 16) || !aligned(bundle_out, 16)) return TACO_ERR_ALIGN;
-    const uintptr_t xa = reinterpret_cast<uintptr_t>(x_bf16), ba = reinterpret_cast<uintptr_t>(bundle_out);
-    const size_t in_bytes = static_cast<size_t>(P) * N * h * 2;
-    const size_t out_bytes = static_cast<size_t>(P) * taco_shard_bytes(N, h, block);
-    if (xa < ba + out_bytes && ba < xa + in_bytes) return TACO_ERR_ARG;   // overlapping buffers
-  }
-
   void* scratch = nullptr;
-  if (scratch_address(&scratch) != cudaSuccess) return TACO_ERR_CUDA;
+  if (scratch_address(&scratch) != cudaSuccess) return TACO_ERR_CUDA;   // a lookup, nothing enqueued
+  // The checks of taco_compress_shards with the static scratch as the
+  // workspace (P beyond its room gives TACO_ERR_WORKSPACE), taken before
+  // the scratch clear so that a rejected call enqueues nothing.
+  const taco_status st = taco::check_compress_args(x_bf16, P, N, h, block, target_energy, variant,
+                                                   bundle_out, headers_out, scratch,
+                                                   kNoallocScratchBytes);
+  if (st != TACO_OK) return st;
   const size_t need = static_cast<size_t>(P) * taco::kWorkspaceShardStride;
   // The arrival counters must start at zero; the array keeps whatever the
   // previous call (on any stream) left in it.

@@ -267,8 +267,7 @@ decompress_reduce_kernel(DecompressArgs a) {
       const float e = block_sum<LPB>((e01.x + e01.y) + (e23.x + e23.y));
       float r = rsqrtf(e);
       r = fmaf(fmaf(-0.5f * e * r, r, 0.5f), r, r);
-      const float alpha = (e > 0.f) ? a.sqrt_E * r : 1.0f;
-      const float cscale = alpha * a.sqrt_n;          // rotated block = cscale * z
+      float alpha = (e > 0.f) ? clamp_alpha(a.sqrt_E * r) : 1.0f;   // kept in [2^-126, 2^126]
       float hq[kCH], lq[kCH];
 #pragma unroll
       for (int q = 0; q < kCH; ++q) {
@@ -279,7 +278,36 @@ decompress_reduce_kernel(DecompressArgs a) {
       }
       const float zhi = max3(max3(hq[0], hq[1], hq[2]), max3(hq[3], hq[4], hq[5]), fmaxf(hq[6], hq[7]));
       const float zlo = min3(min3(lq[0], lq[1], lq[2]), min3(lq[3], lq[4], lq[5]), fminf(lq[6], lq[7]));
-      const float amax = cscale * block_max<LPB>(fmaxf(zhi, -zlo));
+      const float zmax = block_max<LPB>(fmaxf(zhi, -zlo));
+      // A non-zero block whose sum of squares is not a trusted fp32 number:
+      // its energy is taken again from 2^-k z (k the exponent of max |z|;
+      // exact) and 2^-k is put back into alpha. z itself is not changed, and
+      // blocks that are not far take k = 0 and repeat the arithmetic above.
+      const bool far = !(e >= kEnergyLo && e <= kEnergyHi) && !(zmax == 0.f);
+      const bool any_far = __any_sync(kFullMask, far);
+      const int k = (far && zmax <= 0x1.fffffep127f) ? ilogbf(zmax) : 0;
+      const int nk = -k, nk1 = nk >> 1;              // 2^-k = 2^nk1 2^(nk - nk1), both normal
+      const f2 s1{exp2i(nk1), exp2i(nk1)}, s2{exp2i(nk - nk1), exp2i(nk - nk1)};
+      if (any_far) {
+        f2 eb[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll
+        for (int q = 0; q < kCH; ++q)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const f2 t = mul2(mul2(z[q][i], s1), s2);
+            eb[i] = fma2(t, t, eb[i]);
+          }
+        const f2 f01 = add2(eb[0], eb[1]), f23 = add2(eb[2], eb[3]);
+        const float e2 = block_sum<LPB>((f01.x + f01.y) + (f23.x + f23.y));
+        float r2 = rsqrtf(e2);
+        r2 = fmaf(fmaf(-0.5f * e2 * r2, r2, 0.5f), r2, r2);
+        alpha = (e2 > 0.f) ? clamp_alpha(a.sqrt_E * r2 * s1.x * s2.x) : 1.0f;
+      }
+      // rotated block = alpha sqrt(n) z; a far block takes its codes from
+      // 2^-k z with alpha 2^k sqrt(n), which stays in the fp32 range where
+      // alpha sqrt(n) or y / s would not (k = 0 elsewhere: no change)
+      const float cscale = ldexpf(alpha, k) * a.sqrt_n;
+      const float amax = cscale * ldexpf(zmax, -k);
       constexpr float QMAX = (FMT == 0) ? 448.0f : 127.0f;
       const float sc = (VARIANT == 0)   ? fmaxf(1.0f, amax * (1.0f / QMAX))
                        : (VARIANT == 1) ? (amax > 0.f ? amax * (1.0f / QMAX) : 1.0f)
@@ -288,23 +316,10 @@ decompress_reduce_kernel(DecompressArgs a) {
       const f2 g2{g, g};
       if (lane == 0) bulk_wait_read<0>();   // the previous store has read the buffer
       __syncwarp();
-      {
-        const uint32_t base = out0 + sub * NB;
-#pragma unroll
-        for (int q = 0; q < kCH; ++q) {
-          const f2 y0 = mul2(z[q][0], g2), y1 = mul2(z[q][1], g2);
-          const f2 y2 = mul2(z[q][2], g2), y3 = mul2(z[q][3], g2);
-          uint2 w;
-          if constexpr (FMT == 0) {
-            w.x = e4m3x4_from_f32(y0.x, y0.y, y1.x, y1.y);
-            w.y = e4m3x4_from_f32(y2.x, y2.y, y3.x, y3.y);
-          } else {
-            w.x = i8x4_from_f32(y0, y1);
-            w.y = i8x4_from_f32(y2, y3);
-          }
-          sts64(base + 8 * (j + LPB * (q ^ cx)), w);
-        }
-      }
+      if (any_far)
+        store_codes<FMT, LPB, true, VARIANT == 2>(z, g2, s1, s2, out0 + sub * NB, j, cx);
+      else
+        store_codes<FMT, LPB, false, VARIANT == 2>(z, g2, s1, s2, out0 + sub * NB, j, cx);
       if (sub < vb && j == 0) {
         reinterpret_cast<float2*>(rc_shard + a.scales_off)[b0 + sub] = make_float2(alpha, sc);
         part_smax = fmaxf(part_smax, sc);
@@ -367,195 +382,7 @@ decompress_reduce_kernel(DecompressArgs a) {
   if (lane == 0) bulk_wait_read<0>();
 }
 
-// ---------------------------------------------------------------------------
-// Decompress-reduce with a producer warp (E4M3 codes, n = 64). One CTA per
-// SM: warp 15 alone issues the copies, one shard of a 480-block CTA tile per
-// stage (the tile's codes and (alpha, s) pairs, two 1-D bulk copies), into
-// a ring of kPwStages stages that the 15 consumer warps share; consumer warp
-// w reads blocks 32 w .. 32 w + 31 of the tile (one per lane, as in the
-// kernel above) and arrives on the stage's "empty" barrier once it has read
-// them. The arithmetic of a lane is the kernel above's, so the outputs are
-// the same bits; the consumers no longer spend issue slots on copy
-// bookkeeping (a fifth of them above), which measured 16.2 -> 15.7 us on
-// gpt2-1.5b-act. CTA tiles go in grid-stride rounds, then each CTA takes its
-// even share of the blocks left over (4-block boundaries) in pieces of at
-// most one tile.
-constexpr int kPwCons = 15;                                // consumer warps
-constexpr int kPwStages = 4;
-constexpr int kPwTileBlocks = kPwCons * 32;                // 480 blocks
-constexpr uint32_t kPwCodes = kPwTileBlocks * 64;          // 30720 B
-constexpr uint32_t kPwStage = kPwCodes + kPwTileBlocks * 8;   // + 3840 B of scale pairs
-constexpr uint32_t kPwOut = 32 * 64 * 2;                   // bf16 output of one warp tile
-constexpr uint32_t kPwBars = kPwStages * kPwStage + kPwCons * kPwOut;
-static_assert(kPwCons + 1 == kDecompressThreads / 32, "one producer warp and the consumers");
-
-struct PwItems {
-  int64_t G, c, n_full, lo, hi, total;
-  __device__ __forceinline__ PwItems(int64_t nblocks, int64_t c_, int64_t G_) : G(G_), c(c_) {
-    const int64_t rounds = nblocks / (G * kPwTileBlocks);
-    const int64_t rem0 = rounds * G * kPwTileBlocks;
-    const int64_t rest = nblocks - rem0;
-    n_full = rounds;
-    lo = rem0 + ((rest * c / G) & ~int64_t{3});
-    hi = rem0 + ((c + 1 == G) ? rest : ((rest * (c + 1) / G) & ~int64_t{3}));
-    if (hi < lo) hi = lo;
-    total = n_full + (hi - lo + kPwTileBlocks - 1) / kPwTileBlocks;
-  }
-  // first block and number of blocks of the CTA's tile k (k < total)
-  __device__ __forceinline__ void get(int64_t k, int64_t& b0, int& vb) const {
-    if (k < n_full) {
-      b0 = (k * G + c) * kPwTileBlocks;
-      vb = kPwTileBlocks;
-    } else {
-      b0 = lo + (k - n_full) * kPwTileBlocks;
-      const int64_t left = hi - b0;
-      vb = static_cast<int>(left < kPwTileBlocks ? left : kPwTileBlocks);
-    }
-  }
-};
-
-// bounded wait; gives up when the CTA's abort flag is set or after
-// kWaitLimitNs, setting the flag and the kernel's fault bit
-__device__ __forceinline__ bool pw_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer_ns();
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
-      *abort_flag = 1u;
-      atomicOr(&g_decompress_fault, kFaultDecompressWait);
-      return false;
-    }
-  }
-}
-
-__global__ void __launch_bounds__(kDecompressThreads, 1) decompress_reduce_pw_kernel(DecompressArgs a) {
-  extern __shared__ __align__(128) unsigned char smem[];
-  const uint32_t base = smem_u32(smem);
-  const uint32_t full0 = base + kPwBars, empty0 = full0 + 8 * kPwStages;
-  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + kPwBars + 16 * kPwStages);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const PwItems it(a.nblocks, blockIdx.x, gridDim.x);
-  const int P = a.P;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kPwStages; ++s) {
-      mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, kPwCons);
-    }
-    *abort_flag = 0u;
-    fence_mbar_init();
-  }
-  __syncthreads();
-  grid_launch_dependents();
-  grid_dependency_wait();   // no global access before the preceding grid is done
-
-  if (warp == kPwCons) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      const uint64_t policy = l2_evict_first_policy();
-      uint32_t i = 0;
-      bool ok = true;
-      for (int64_t k = 0; k < it.total && ok; ++k) {
-        int64_t b0;
-        int vb;
-        it.get(k, b0, vb);
-        const uint32_t cbytes = static_cast<uint32_t>(vb) * 64;
-        const uint32_t sbytes = (static_cast<uint32_t>(vb) * 8 + 15) & ~15u;   // inside the 256-byte padding
-        for (int p = 0; p < P; ++p, ++i) {
-          const uint32_t s = i % kPwStages, ph = (i / kPwStages) & 1u;
-          if (!pw_wait(empty0 + 8 * s, ph ^ 1u, abort_flag)) {
-            ok = false;
-            break;
-          }
-          const uint32_t dst = base + s * kPwStage;
-          fence_proxy_async_smem();
-          mbar_arrive_expect_tx(full0 + 8 * s, cbytes + sbytes);
-          tma_load_1d(dst, a.shard[p] + b0 * 64, cbytes, full0 + 8 * s, policy);
-          tma_load_1d(dst + kPwCodes, a.shard[p] + a.scales_off + b0 * 8, sbytes, full0 + 8 * s, policy);
-        }
-      }
-      // the copies in flight land before the CTA may exit
-      const uint32_t first = i > static_cast<uint32_t>(kPwStages) ? i - kPwStages : 0u;
-      for (uint32_t j = first; j < i; ++j) mbar_wait(full0 + 8 * (j % kPwStages), (j / kPwStages) & 1u);
-    }
-    __syncwarp();
-    return;
-  }
-
-  // -------------------------------------------------------------- consumers
-  const int cx = lane & (kCH - 1);
-  const uint32_t out0 = base + kPwStages * kPwStage + warp * kPwOut;
-  const uint32_t row = 32 * warp + lane;   // this lane's block of a tile
-  uint32_t i = 0;
-  bool ok = true;
-  for (int64_t k = 0; k < it.total && ok; ++k) {
-    int64_t b0;
-    int vb;
-    it.get(k, b0, vb);
-    int wvb = vb - 32 * warp;   // this warp's blocks of the tile
-    wvb = wvb < 0 ? 0 : (wvb > 32 ? 32 : wvb);
-    f2 z[kCH][4];
-#pragma unroll
-    for (int q = 0; q < kCH; ++q)
-#pragma unroll
-      for (int r = 0; r < 4; ++r) z[q][r] = f2{0.f, 0.f};
-    for (int p = 0; p < P; ++p, ++i) {
-      const uint32_t s = i % kPwStages, ph = (i / kPwStages) & 1u;
-      const bool got = pw_wait(full0 + 8 * s, ph, abort_flag);
-      if (!__all_sync(kFullMask, got)) {   // keep the warp's decision uniform
-        ok = false;
-        break;
-      }
-      const uint32_t st = base + s * kPwStage;
-      const uint2 as = lds64(st + kPwCodes + 8 * row);   // (alpha, s) of the block
-      uint2 w[kCH];
-#pragma unroll
-      for (int q = 0; q < kCH; ++q) w[q] = lds64(st + row * 64 + 8 * (q ^ cx));
-      __syncwarp();   // every lane has read the stage: the warp releases it
-      if (lane == 0) mbar_arrive(empty0 + 8 * s);
-      const float d = __fdividef(__uint_as_float(as.y), __uint_as_float(as.x)) * a.inv_sqrt_n;
-      const f2 d2{d, d};
-#pragma unroll
-      for (int q = 0; q < kCH; ++q) {
-        f2 c0, c1, c2, c3;
-        decode4<0>(w[q].x, c0, c1);
-        decode4<0>(w[q].y, c2, c3);
-        z[q][0] = fma2(d2, c0, z[q][0]);
-        z[q][1] = fma2(d2, c1, z[q][1]);
-        z[q][2] = fma2(d2, c2, z[q][2]);
-        z[q][3] = fma2(d2, c3, z[q][3]);
-      }
-    }
-    if (!ok || wvb == 0) continue;
-    fwht_in_registers<kCH>(z, cx);
-    if (lane == 0) bulk_wait_read<0>();   // the previous store has read the buffer
-    __syncwarp();
-#pragma unroll
-    for (int q = 0; q < kCH; ++q) {
-      uint4 o;
-      o.x = pack_bf16x2(z[q][0].x, z[q][0].y);
-      o.y = pack_bf16x2(z[q][1].x, z[q][1].y);
-      o.z = pack_bf16x2(z[q][2].x, z[q][2].y);
-      o.w = pack_bf16x2(z[q][3].x, z[q][3].y);
-      sts128(out0 + lane * 128 + 16 * (q ^ cx), o);
-    }
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-      tma_store_1d(a.out + (b0 + 32 * warp) * 64, out0, static_cast<uint32_t>(wvb) * 128);
-      bulk_commit();
-    }
-  }
-  if (lane == 0) bulk_wait_read<0>();
-}
-
 }  // namespace
-
-size_t decompress_pw_smem_bytes() { return kPwBars + 2 * 8 * kPwStages + 16; }
-
-const void* decompress_pw_kernel_ptr() { return reinterpret_cast<const void*>(decompress_reduce_pw_kernel); }
 
 size_t decompress_smem_bytes() {
   // per warp: stages, their barriers, the output tile and the 4-slot tile ring
@@ -617,12 +444,6 @@ cudaError_t launch_decompress(const DecompressArgs& a, int block, int fmt, int g
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (block == 64 && fmt == 0) {
-    // E4M3 codes of 64-element blocks: the producer-warp kernel
-    cfg.dynamicSmemBytes = decompress_pw_smem_bytes();
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, decompress_reduce_pw_kernel, a);
-    return e != cudaSuccess ? e : cudaGetLastError();
-  }
   // With E4M3 codes, warps with at least kClaimRounds full grid-stride
   // rounds claim their CTA's tiles in order (the warps the scheduler favours
   // take more): 2-2.6% faster on the large tensors measured. With fewer

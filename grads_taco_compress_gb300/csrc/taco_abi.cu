@@ -12,6 +12,11 @@ namespace taco {
 namespace {
 
 constexpr int64_t kMaxElements = int64_t{1} << 40;   // per shard
+// Largest target energy E* accepted (2^120): the rotated values of a block
+// then stay far inside the fp32 range in every variant (|y| <= sqrt(n E*)),
+// and so do the factors the kernels form from alpha. Codes saturate at 448,
+// so an E* beyond 448^2 already sends every block to the overflow guard.
+constexpr float kMaxTargetEnergy = 0x1p120f;
 constexpr int kMaxDevices = 64;
 
 inline size_t pad256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
@@ -49,6 +54,7 @@ struct DeviceInfo {
   int sms = 0;
   int occ_compress[3][kVariants] = {};
   int occ_decompress[3][kFormats] = {};
+  int occ_pw[2][3][kVariants][kFormats] = {};   // producer-warp kernels [mode][block][variant][fmt]
   int occ_recompress[3][kVariants][kFormats] = {};
   int occ_gather[3][kFormats] = {};
   int occ_mma[3][kVariants][kFormats] = {};
@@ -70,9 +76,17 @@ cudaError_t device_info(const DeviceInfo** out) {
     const int blocks[3] = {64, 128, 256};
     const int csmem = static_cast<int>(compress_smem_bytes());
     const int dsmem = static_cast<int>(decompress_smem_bytes());
-    if (err == cudaSuccess)
-      err = cudaFuncSetAttribute(decompress_pw_kernel_ptr(), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(decompress_pw_smem_bytes()));
+    for (int m = 0; m < 2 && err == cudaSuccess; ++m)
+      for (int b = 0; b < 3 && err == cudaSuccess; ++b)
+        for (int v = 0; v < (m == 0 ? 1 : kVariants) && err == cudaSuccess; ++v)
+          for (int f = 0; f < kFormats && err == cudaSuccess; ++f) {
+            const void* k = decompress_pw_kernel_ptr(m, blocks[b], v, f);
+            const int psmem = static_cast<int>(decompress_pw_smem_bytes(blocks[b]));
+            err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, psmem);
+            if (err == cudaSuccess)
+              err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ_pw[m][b][v][f], k,
+                                                                  kDecompressThreads, psmem);
+          }
     for (int b = 0; b < 3 && err == cudaSuccess; ++b) {
       for (int v = 0; v < kVariants && err == cudaSuccess; ++v) {
         const void* k = compress_kernel_ptr(blocks[b], v);
@@ -193,14 +207,21 @@ taco_status decompress_common(const uint8_t* const* shards, int P, int64_t N, in
                ? TACO_OK
                : TACO_ERR_CUDA;
   }
-  const int64_t needed = ctas_wanted(a.nblocks, kDecompressThreads / 32);
-  int64_t grid = static_cast<int64_t>(info->sms) * info->occ_decompress[block_index(block)][fmt];
+  // the grid of the kernel launch_decompress runs: its own occupancy, and no
+  // more CTAs than its smallest share of blocks fills
+  const bool pw = decompress_uses_pw(0, block, fmt);
+  const int64_t needed = pw ? (a.nblocks + kPwMinBlocksPerCta - 1) / kPwMinBlocksPerCta
+                            : ctas_wanted(a.nblocks, kDecompressThreads / 32);
+  const int occ = pw ? info->occ_pw[0][block_index(block)][0][fmt] : info->occ_decompress[block_index(block)][fmt];
+  if (occ < 1) return TACO_ERR_CUDA;
+  int64_t grid = static_cast<int64_t>(info->sms) * occ;
   if (grid > needed) grid = needed;
   if (grid < 1) grid = 1;
-  if (launch_decompress(a, block, fmt, static_cast<int>(grid), static_cast<cudaStream_t>(stream)) !=
-      cudaSuccess)
-    return TACO_ERR_CUDA;
-  return TACO_OK;
+  const cudaError_t e = pw ? launch_decompress_pw(a, 0, block, 0, fmt, static_cast<int>(grid), 1,
+                                                  static_cast<cudaStream_t>(stream))
+                           : launch_decompress(a, block, fmt, static_cast<int>(grid),
+                                               static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? TACO_OK : TACO_ERR_CUDA;
 }
 
 taco_status decompress_shards_common(const uint8_t* const* shards, int P, int64_t N, int64_t h,
@@ -250,7 +271,7 @@ taco_status reduce_recompress_common(const uint8_t* const* shards, int P, int64_
   if (P < 1 || Y < 1 || P * Y > TACO_MAX_SHARDS) return TACO_ERR_ARG;
   if (Y > 1 && out) return TACO_ERR_ARG;
   if (!valid_variant(variant)) return TACO_ERR_ARG;
-  if (!(target_energy > 0.0f) || !std::isfinite(target_energy)) return TACO_ERR_ARG;
+  if (!(target_energy > 0.0f) || !(target_energy <= kMaxTargetEnergy)) return TACO_ERR_ARG;
   if (!header_out) return TACO_ERR_NULL;
   if (!workspace || workspace_bytes < Y * kWorkspaceShardStride) return TACO_ERR_WORKSPACE;
   if (!aligned(header_out, 8) || !aligned(workspace, 16)) return TACO_ERR_ALIGN;
@@ -288,41 +309,59 @@ taco_status reduce_recompress_common(const uint8_t* const* shards, int P, int64_
 
   const DeviceInfo* info = nullptr;
   if (device_info(&info) != cudaSuccess) return TACO_ERR_CUDA;
-  const int64_t needed = ctas_wanted(a.nblocks, kDecompressThreads / 32);
-  const int64_t total =
-      static_cast<int64_t>(info->sms) * info->occ_recompress[block_index(block)][variant][fmt];
+  const bool pw = decompress_uses_pw(1, block, fmt);
+  const int64_t needed = pw ? (a.nblocks + kPwMinBlocksPerCta - 1) / kPwMinBlocksPerCta
+                            : ctas_wanted(a.nblocks, kDecompressThreads / 32);
+  const int occ = pw ? info->occ_pw[1][block_index(block)][variant][fmt]
+                     : info->occ_recompress[block_index(block)][variant][fmt];
+  if (occ < 1) return TACO_ERR_CUDA;
+  const int64_t total = static_cast<int64_t>(info->sms) * occ;
   int64_t grid = (total + Y - 1) / Y;
   if (grid > needed) grid = needed;
   if (grid > kMaxCtasPerShard) grid = kMaxCtasPerShard;
   if (grid < 1) grid = 1;
-  if (launch_reduce_recompress(a, block, variant, fmt, static_cast<int>(grid), Y,
-                               static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return TACO_ERR_CUDA;
+  const cudaError_t e = pw ? launch_decompress_pw(a, 1, block, variant, fmt, static_cast<int>(grid), Y,
+                                                  static_cast<cudaStream_t>(stream))
+                           : launch_reduce_recompress(a, block, variant, fmt, static_cast<int>(grid), Y,
+                                                      static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? TACO_OK : TACO_ERR_CUDA;
+}
+
+}  // namespace
+
+taco_status check_compress_args(const void* x_bf16, int P, int64_t N, int64_t h, int block,
+                                float target_energy, int variant, const void* bundle_out,
+                                const taco_header* headers_out, const void* workspace,
+                                size_t workspace_bytes) {
+  taco_status st = check_shape(N, h, block);
+  if (st != TACO_OK) return st;
+  if (P < 1 || P > TACO_MAX_SHARDS) return TACO_ERR_ARG;
+  if (!valid_variant(variant)) return TACO_ERR_ARG;
+  if (!(target_energy > 0.0f) || !(target_energy <= kMaxTargetEnergy)) return TACO_ERR_ARG;
+  if (!headers_out) return TACO_ERR_NULL;
+  if (!workspace || workspace_bytes < taco_workspace_bytes(P)) return TACO_ERR_WORKSPACE;
+  if (!aligned(headers_out, 8) || !aligned(workspace, 16)) return TACO_ERR_ALIGN;
+  if (N > 0) {
+    if (!x_bf16 || !bundle_out) return TACO_ERR_NULL;
+    if (!aligned(x_bf16, 16) || !aligned(bundle_out, 16)) return TACO_ERR_ALIGN;
+    const size_t in_bytes = static_cast<size_t>(P) * N * h * 2;
+    if (overlap(x_bf16, in_bytes, bundle_out, P * shard_layout(N, h, block).bytes)) return TACO_ERR_ARG;
+  }
   return TACO_OK;
 }
+
+namespace {
 
 // Argument checks and kernel arguments shared by both compress entries.
 taco_status compress_args(const void* x_bf16, int P, int64_t N, int64_t h, int block,
                           float target_energy, int variant, void* bundle_out,
                           taco_header* headers_out, void* workspace, size_t workspace_bytes,
                           CompressArgs* out) {
-  taco_status st = check_shape(N, h, block);
+  const taco_status st = check_compress_args(x_bf16, P, N, h, block, target_energy, variant,
+                                             bundle_out, headers_out, workspace, workspace_bytes);
   if (st != TACO_OK) return st;
-  if (P < 1 || P > TACO_MAX_SHARDS) return TACO_ERR_ARG;
-  if (!valid_variant(variant)) return TACO_ERR_ARG;
-  if (!(target_energy > 0.0f) || !std::isfinite(target_energy)) return TACO_ERR_ARG;
-  const double sqrt_nE = std::sqrt(static_cast<double>(block) * target_energy);
-  if (!(sqrt_nE < 3.0e38)) return TACO_ERR_ARG;
-  if (!headers_out) return TACO_ERR_NULL;
-  if (!workspace || workspace_bytes < taco_workspace_bytes(P)) return TACO_ERR_WORKSPACE;
-  if (!aligned(headers_out, 8) || !aligned(workspace, 16)) return TACO_ERR_ALIGN;
   const Layout l = shard_layout(N, h, block);
-  const size_t in_bytes = static_cast<size_t>(P) * N * h * 2;
-  if (N > 0) {
-    if (!x_bf16 || !bundle_out) return TACO_ERR_NULL;
-    if (!aligned(x_bf16, 16) || !aligned(bundle_out, 16)) return TACO_ERR_ALIGN;
-    if (overlap(x_bf16, in_bytes, bundle_out, P * l.bytes)) return TACO_ERR_ARG;
-  }
+  const double sqrt_nE = std::sqrt(static_cast<double>(block) * target_energy);
 
   CompressArgs& a = *out;
   a.x = static_cast<const uint16_t*>(x_bf16);
@@ -636,13 +675,14 @@ taco_status taco_e4m3_decode_f32(const uint8_t* in, float* out, int64_t n, void*
 
 taco_status taco_get_fault(uint32_t* bits, int clear) {
   if (!bits) return TACO_ERR_NULL;
-  unsigned int c = 0, d = 0, t = 0, m = 0, dm = 0;
+  unsigned int c = 0, d = 0, t = 0, m = 0, dm = 0, dp = 0;
   if (compress_fault(&c, clear != 0) != cudaSuccess) return TACO_ERR_CUDA;
+  if (decompress_pw_fault(&dp, clear != 0) != cudaSuccess) return TACO_ERR_CUDA;
   if (compress_mma_fault(&m, clear != 0) != cudaSuccess) return TACO_ERR_CUDA;
   if (decompress_mma_fault(&dm, clear != 0) != cudaSuccess) return TACO_ERR_CUDA;
   if (decompress_fault(&d, clear != 0) != cudaSuccess) return TACO_ERR_CUDA;
   if (selftest_fault(&t, clear != 0) != cudaSuccess) return TACO_ERR_CUDA;
-  *bits = c | d | t | m | dm;
+  *bits = c | d | t | m | dm | dp;
   return TACO_OK;
 }
 

@@ -38,6 +38,38 @@ constexpr unsigned kFaultSelftestWait = 4u;
 constexpr unsigned kFaultCompressMmaWait = 8u;
 constexpr unsigned kFaultDecompressMmaWait = 16u;
 
+// ------------------------------------------------------- alpha range ----
+// alpha = sqrt(E*/E) is stored as an fp32 number and kept inside
+// [2^-126, 2^126], where alpha and 1/alpha are both normal fp32 numbers: a
+// block whose energy is further than 2^252 from E* is rescaled only part of
+// the way, and every decoder can form s / alpha in fp32.
+constexpr float kAlphaMin = 0x1p-126f;
+constexpr float kAlphaMax = 0x1p126f;
+__device__ __forceinline__ float clamp_alpha(float a) { return fminf(fmaxf(a, kAlphaMin), kAlphaMax); }
+
+// A sum of squares accumulated in fp32 is trusted inside [2^-100, 2^100]:
+// the squares that fall into fp32's subnormal range then weigh less than
+// 2^-40 of it, and neither the sum nor a Hadamard transform of the block
+// (|t| <= 256 max|x|) can overflow. Blocks outside are rescaled by a power
+// of two first (exactly), which the operator's energy and rotation commute
+// with.
+constexpr float kEnergyLo = 0x1p-100f;
+constexpr float kEnergyHi = 0x1p100f;
+
+// 2^e for -126 <= e <= 127, exactly.
+__device__ __forceinline__ float exp2i(int e) { return __int_as_float((e + 127) << 23); }
+
+// alpha for a block whose sum of squares, after scaling the block by 2^-k,
+// is e2 (> 0): sqrt(E*/E) = 2^-k * root_E / sqrt(e2), where root_E folds in
+// the block's normalisation (sqrt(n E*) for e2 = sum x^2, n sqrt(E*) for
+// e2 = sum t^2 of the rotated block, sqrt(E*) for e2 = sum z^2 of a reduced
+// one). rsqrt with one Newton step, then 2^-k, then the clamp.
+__device__ __forceinline__ float alpha_scaled(float root_E, float e2, int k) {
+  float r = rsqrtf(e2);
+  r = fmaf(fmaf(-0.5f * e2 * r, r, 0.5f), r, r);
+  return clamp_alpha(ldexpf(root_E * r, -k));
+}
+
 // ------------------------------------------------------------- f32 pairs ----
 // Two fp32 values in one 64-bit register pair, for the packed f32x2 ALU ops.
 struct __align__(8) f2 {
@@ -119,6 +151,10 @@ __device__ __forceinline__ f2 e4m3x2_to_f2(uint32_t two_codes) {
 constexpr float kI8Round = 12582912.0f;   // 1.5 * 2^23
 
 // Four scaled values -> four codes in one word, element 0 in the low byte.
+// With CLAMP, values beyond +-127 become +-127 first: the STATIC scale
+// bounds |y / s| by 127 only while alpha is not clamped, the other scale
+// rules always.
+template <bool CLAMP = false>
 __device__ __forceinline__ uint32_t i8x4_from_f32(f2 y01, f2 y23);
 
 // Four codes (element 0 in the low byte) -> four exact fp32 values: the
@@ -463,7 +499,12 @@ __device__ void finish_header(float part_smax, uint32_t part_cnt, uint8_t* ws_sh
   *reinterpret_cast<unsigned long long*>(ws_shard) = 0ull;
 }
 
+template <bool CLAMP>
 __device__ __forceinline__ uint32_t i8x4_from_f32(f2 y01, f2 y23) {
+  if constexpr (CLAMP) {
+    y01 = f2{fminf(fmaxf(y01.x, -127.0f), 127.0f), fminf(fmaxf(y01.y, -127.0f), 127.0f)};
+    y23 = f2{fminf(fmaxf(y23.x, -127.0f), 127.0f), fminf(fmaxf(y23.y, -127.0f), 127.0f)};
+  }
   const f2 m{kI8Round, kI8Round};
   const f2 r01 = add2(y01, m), r23 = add2(y23, m);
   const uint32_t lo = __byte_perm(__float_as_uint(r01.x), __float_as_uint(r01.y), 0x0040);
@@ -479,6 +520,31 @@ __device__ __forceinline__ void i8x4_to_f32(uint32_t four_codes, f2& v01, f2& v2
   v23 = sub2(f2{__uint_as_float(__byte_perm(t, 0x4B400000u, 0x7652)),
                 __uint_as_float(__byte_perm(t, 0x4B400000u, 0x7653))}, off);
 }
+
+// Codes of one warp tile's lane (8 chunks of 8 elements, the layout above)
+// into shared memory at `base` (byte j + LPB (q ^ cx) * 8 of the block's row):
+// code = g * v, with v = 2^-k z when SCALED (s1 s2 = 2^-k), else z.
+template <int FMT, int LPB, bool SCALED, bool CLAMP>
+__device__ __forceinline__ void store_codes(const f2 (&z)[kCH][4], f2 g2, f2 s1, f2 s2, uint32_t base,
+                                            int j, int cx) {
+#pragma unroll
+  for (int q = 0; q < kCH; ++q) {
+    f2 v[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) v[r] = SCALED ? mul2(mul2(z[q][r], s1), s2) : z[q][r];
+    const f2 y0 = mul2(v[0], g2), y1 = mul2(v[1], g2), y2 = mul2(v[2], g2), y3 = mul2(v[3], g2);
+    uint2 w;
+    if constexpr (FMT == 0) {
+      w.x = e4m3x4_from_f32(y0.x, y0.y, y1.x, y1.y);
+      w.y = e4m3x4_from_f32(y2.x, y2.y, y3.x, y3.y);
+    } else {
+      w.x = i8x4_from_f32<CLAMP>(y0, y1);
+      w.y = i8x4_from_f32<CLAMP>(y2, y3);
+    }
+    sts64(base + 8 * (j + LPB * (q ^ cx)), w);
+  }
+}
+
 
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float r;

@@ -78,6 +78,13 @@ struct DecompressArgs {
   float s_static;           // fp32(sqrt(block * E*) / 448), STATIC variant
 };
 
+// The argument checks of the compress entry points, without any CUDA call:
+// TACO_OK, or the status such a call returns before it enqueues anything.
+taco_status check_compress_args(const void* x_bf16, int P, int64_t N, int64_t h, int block,
+                                float target_energy, int variant, const void* bundle_out,
+                                const taco_header* headers_out, const void* workspace,
+                                size_t workspace_bytes);
+
 size_t compress_smem_bytes();
 const void* compress_kernel_ptr(int block, int variant);
 cudaError_t launch_compress(const CompressArgs& a, int block, int variant, int grid_x, int P,
@@ -93,9 +100,30 @@ cudaError_t compress_mma_fault(unsigned int* bits, bool clear);
 
 size_t decompress_smem_bytes();
 const void* decompress_kernel_ptr(int block, int fmt, bool claim);
-// decompress-reduce of E4M3 codes of 64-element blocks (producer warp)
-size_t decompress_pw_smem_bytes();
-const void* decompress_pw_kernel_ptr();
+// Producer-warp kernels (decompress_pw.cu): mode 0 decompress-reduce, mode 1
+// reduce-recompress (gridDim.y = batch reductions), any block and format.
+size_t decompress_pw_smem_bytes(int block);
+int64_t decompress_pw_tile_blocks(int block);
+const void* decompress_pw_kernel_ptr(int mode, int block, int variant, int fmt);
+cudaError_t launch_decompress_pw(const DecompressArgs& a, int mode, int block, int variant, int fmt,
+                                 int grid, int batch, cudaStream_t stream);
+cudaError_t decompress_pw_fault(unsigned int* bits, bool clear);
+// Whether a launch of this mode (0 decompress-reduce, 1 reduce-recompress),
+// block size and code format runs the producer-warp kernel. Measured against
+// the per-warp-copy kernel (decompress_reduce.cu), back-to-back launches on
+// GB300: n = 64 is faster in every mode and format (gpt2-1.5b-act: E4M3
+// decompress-reduce equal at 15.57 us, INT8 17.11 -> 15.82 us,
+// reduce-recompress 17.01 -> 15.22 us E4M3 and 17.92 -> 15.90 us INT8); at
+// n = 128 and 256 the per-warp copies with claimed tiles stay ahead by 1-10%
+// (gpt3-6.7b-act decompress-reduce 56.7 us against 59.5 us).
+inline bool decompress_uses_pw(int mode, int block, int fmt) {
+  (void)mode;
+  (void)fmt;
+  return block == 64;
+}
+// The fewest blocks a CTA of the producer-warp kernel is given (two of its
+// consumer warps' worth), so that small tensors still spread over many SMs.
+constexpr int64_t kPwMinBlocksPerCta = 64;
 cudaError_t launch_decompress(const DecompressArgs& a, int block, int fmt, int grid,
                               cudaStream_t stream);
 const void* recompress_kernel_ptr(int block, int variant, int fmt);

@@ -9,7 +9,10 @@
  *
  *   compress, per block of n contiguous elements of a row (n = 64, 128, 256):
  *     E      = mean of x^2 over the block            (raw second moment)
- *     alpha  = sqrt(E* / E)      (1 when E == 0)      (pre-rotation scale)
+ *     alpha  = sqrt(E* / E)      (1 when E == 0)      (pre-rotation scale),
+ *              rounded to fp32 and kept in [2^-126, 2^126], where alpha and
+ *              1/alpha are both normal fp32 numbers (a block whose energy is
+ *              further than 2^252 from E* is rescaled only part of the way)
  *     y      = (H_n / sqrt(n)) (alpha x)              (Sylvester Hadamard)
  *     s      = max(1, max|y| / 448)                   (post-rotation scale)
  *     q      = E4M3(y / s)   round-to-nearest-even, saturating at +-448
@@ -43,7 +46,7 @@ typedef enum taco_status {
   TACO_ERR_SHAPE = 2,      /* N < 0, h <= 0, h % block != 0, or N*h too large  */
   TACO_ERR_BLOCK = 3,      /* block is not 64, 128 or 256                      */
   TACO_ERR_ALIGN = 4,      /* a tensor or bundle pointer is not 16-byte aligned */
-  TACO_ERR_ARG = 5,        /* target energy not finite and > 0, P out of
+  TACO_ERR_ARG = 5,        /* target energy not in (0, 2^120], P out of
                               [1, TACO_MAX_SHARDS], unknown variant            */
   TACO_ERR_CUDA = 6,       /* a CUDA call or launch failed                     */
   TACO_ERR_WORKSPACE = 7   /* workspace NULL or smaller than taco_workspace_bytes */
@@ -106,11 +109,20 @@ size_t taco_workspace_bytes(int P);
  * shard at `shard_out` (device, 16-byte aligned, taco_shard_bytes(N,h,block)
  * bytes) and its header at `header_out` (device, 8-byte aligned).
  *   block          n, one of 64, 128, 256
- *   target_energy  E* > 0, the per-element energy of every rescaled block
- *                  (TACO pt summary §2.B.1: each block is rescaled to one
- *                  common energy level); 4096 puts the rotated RMS at 64
- *                  code units
+ *   target_energy  E* in (0, 2^120], the per-element energy of every
+ *                  rescaled block (TACO pt summary §2.B.1: each block is
+ *                  rescaled to one common energy level); 4096 puts the
+ *                  rotated RMS at 64 code units
  *   variant        TACO_VARIANT_DUAL, TACO_VARIANT_ABSMAX or TACO_VARIANT_STATIC
+ *   workspace      device memory of taco_workspace_bytes(1) bytes, 16-byte
+ *                  aligned, zero before its first use. The pages specify no
+ *                  API; this argument is this library's addition to the plain
+ *                  compress(x, block, E*) signature, because the per-tensor
+ *                  header is written in the same launch (the CTA that
+ *                  finishes last reads counters that every CTA updates) and
+ *                  the library itself never allocates.
+ * Every finite bf16 input is accepted, subnormals and values near the bf16
+ * maximum included; no finite input gives a NaN code.
  * N == 0 is valid: no code is written and the header reports s_max = 0. */
 taco_status taco_compress(const void* x_bf16, int64_t N, int64_t h, int block,
                           float target_energy, int variant, void* shard_out,
@@ -138,7 +150,11 @@ taco_status taco_compress_shards(const void* x_bf16, int P, int64_t N, int64_t h
  * is taken from the rotated block (sum t^2 = n sum x^2). The outputs meet the
  * same parity bar as taco_compress_shards; a code can differ from that
  * path's by one E4M3 step where the fp32 rotated value differs in its last
- * bits. Extra limit: at most 2^31 - 256 blocks per shard (the tensor
+ * bits. A block whose largest rotated magnitude lies outside [2^-40, 2^56]
+ * takes a slower path: its energy is summed again from the rotated values
+ * scaled by a power of two, or, for blocks of bf16 subnormals only and
+ * blocks near the bf16 maximum whose rotation overflows fp32, the block is
+ * redone from x. Extra limit: at most 2^31 - 256 blocks per shard (the tensor
  * copies address rows with 32-bit coordinates), else TACO_ERR_SHAPE.
  * N == 0 writes the headers as taco_compress_shards does. */
 taco_status taco_compress_shards_mma(const void* x_bf16, int P, int64_t N, int64_t h,

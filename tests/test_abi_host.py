@@ -75,7 +75,7 @@ def _compress(lib, x=A, P=1, N=4, h=256, block=128, E=4096.0, variant=0, bundle=
     (dict(N=1 << 34, h=1 << 10), SHAPE),
     (dict(P=0), ARG), (dict(P=17), ARG), (dict(variant=3), ARG), (dict(variant=-1), ARG),
     (dict(E=0.0), ARG), (dict(E=-1.0), ARG), (dict(E=float("nan")), ARG),
-    (dict(E=float("inf")), ARG),
+    (dict(E=float("inf")), ARG), (dict(E=2.0 ** 121), ARG),
     (dict(headers=None), NULL), (dict(ws=None), WS), (dict(wsb=15), WS),
     (dict(x=None), NULL), (dict(bundle=None), NULL),
     (dict(x=A + 8), ALIGN), (dict(bundle=A * 64 + 4), ALIGN), (dict(headers=A * 128 + 4), ALIGN),
@@ -197,6 +197,7 @@ def test_reduce_recompress_rejects(lib):
     assert call(h=200, block=64) == SHAPE
     assert call(P=0) == ARG and call(P=17) == ARG
     assert call(variant=3) == ARG and call(E=0.0) == ARG and call(E=float("nan")) == ARG
+    assert call(E=2.0 ** 121) == ARG
     assert call(hdr=None) == NULL and call(ws=None) == WS and call(wsb=15) == WS
     assert call(bundle=None) == NULL and call(shard=None) == NULL
     assert call(shard=A * 64 + 8) == ALIGN and call(out=A * 512 + 4) == ALIGN
