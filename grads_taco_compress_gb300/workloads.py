@@ -67,8 +67,8 @@ WORKLOADS = {
                              dict(b=0.01, ln_sigma=1.5, n_channels=8, channel_gain=100.0)),
 }
 
-#: the workload the benchmark times at one GPU
-BENCH_WORKLOAD = "gpt2-1.5b-act"
+#: the workload the benchmark's step times at one GPU: the largest one
+BENCH_WORKLOAD = "qwen-7b-long"
 
 
 def f32_to_bf16_bits(v32: np.ndarray) -> np.ndarray:

@@ -60,6 +60,15 @@ def test_gpu_arm_line():
                  "decompress_reduce_int8", "decompress_reduce_mma", "emulated_two_shot_allreduce"):
         assert line["kernels"][name]["us"] > 0, name
     assert line["e2e"]["h2d_bytes_per_step"] == 4 * 8192 * 1600 * 2
+    # every configuration, each kernel timed alone against the same peak
+    import grads_taco_compress_gb300.workloads as W
+    assert set(line["by_workload"]) == set(W.WORKLOADS)
+    for name, r in line["by_workload"].items():
+        for k in ("compress", "decompress_reduce"):
+            rec = r[k]
+            assert rec["us"] > 0 and abs(rec["frac"] - rec["hbm_gbs"] / roof["peak"]) < 1e-3, (name, k)
+    tiny = line["by_workload"]["tiny-512x1024"]
+    assert tiny["compress"]["graph_batch"]["us_per_launch"] > 0 and "note" in tiny
 
 
 def test_profile_hash_ignores_comments():
