@@ -9,3 +9,15 @@ for p in (str(ROOT), str(ROOT / "tests")):
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA device and the built library")
+
+
+import pytest  # noqa: E402
+
+
+@pytest.fixture(scope="session")
+def oracle_rows():
+    """The oracle over row ranges on every host core (full-size parity)."""
+    from oracle_rows import OracleRows
+    pool = OracleRows()
+    yield pool
+    pool.close()

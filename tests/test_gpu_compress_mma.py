@@ -17,7 +17,7 @@ from grads_taco_compress_gb300 import binding as tb
 from grads_taco_compress_gb300 import workloads as W
 from oracle import taco_oracle as O
 import test_gpu_parity as GP
-from test_gpu_parity import E_STAR, _sample_rows, check_compress_against_oracle, dev_bf16, gpu_compress
+from test_gpu_parity import E_STAR, check_compress_against_oracle, dev_bf16, gpu_compress, report
 
 pytestmark = pytest.mark.gpu
 
@@ -93,11 +93,11 @@ def test_mma_sixteen_shards():
 
 
 @pytest.mark.parametrize("P,N,h,block", [(16, 2048, 1024, 64), (3, 40 * 128 // 16, 1024, 64), (5, 20000, 768, 256)])
-def test_mma_tile_schedule(P, N, h, block):
+def test_mma_tile_schedule(P, N, h, block, oracle_rows):
     """Shapes that drive the tile schedule through its cases: 16 shards (a few
     CTAs per shard, a claimed pool of about a quarter of the tiles), one tile
     per CTA (empty pool) and a ragged last tile in the pool. Every element
-    against the CUDA-core compress, sampled rows against the oracle; a second
+    against the CUDA-core compress and against the oracle; a second
     call on the same workspace gives the same codes, scales and headers."""
     rng = np.random.default_rng(P * 1000 + N)
     v = rng.laplace(0, 0.05, size=(P, N, h)).astype(np.float32)
@@ -112,14 +112,14 @@ def test_mma_tile_schedule(P, N, h, block):
     assert int(ws.count_nonzero()) == 0
     codes, alpha, s_, hdr, _ = gpu_compress(x, block, entry=MMA)
     fc, fa, fs, _, _ = gpu_compress(x, block)
-    rows = _sample_rows(N, seed=P)
+    oc, oa, os_ = oracle_rows.compress(x, block, E_STAR)
     for p in range(P):
         parity.compare_codes(codes[p], fc[p], f"codes[{p}] vs CUDA-core path")
         parity.compare_scales(alpha[p], fa[p], f"alpha[{p}] vs CUDA-core path")
         parity.compare_scales(s_[p], fs[p], f"s[{p}] vs CUDA-core path")
-        oc, oa, os_, _ = O.compress(x[p][rows], block, E_STAR)
-        parity.compare_codes(codes[p][rows], oc, f"codes[{p}] vs oracle")
-        parity.compare_scales(s_[p][rows], os_, f"s[{p}] vs oracle")
+        parity.compare_codes(codes[p], oc[p], f"codes[{p}] vs oracle")
+        parity.compare_scales(alpha[p], oa[p], f"alpha[{p}] vs oracle")
+        parity.compare_scales(s_[p], os_[p], f"s[{p}] vs oracle")
         assert hdr[p]["s_max"] == s_[p].max()
         assert hdr[p]["n_clamped"] == np.count_nonzero(s_[p] > 1.0)
 
@@ -198,20 +198,23 @@ FULL = ["tiny-512x1024", "gpt2-1.5b-act", "gpt3-6.7b-act", "gpt3-6.7b-grad", "qw
 
 
 @pytest.mark.parametrize("name", FULL)
-def test_mma_full_size_sampled_and_against_cuda_core_path(name):
-    """Full size: sampled rows against the oracle, every element against the
-    CUDA-core compress (same parity bar), header as the reduction of s."""
+def test_mma_full_size_every_element_and_against_cuda_core_path(name, oracle_rows):
+    """The benchmark's compress launch at full size: every code, alpha and s
+    against the oracle and against the CUDA-core compress (same parity bar),
+    header as the reduction of s."""
+    from oracle_rows import cached_compress
     w = W.WORKLOADS[name]
     x = W.make_shards(w)
     codes, alpha, s, hdr, _ = gpu_compress(x, w.block, entry=MMA)
-    rows = _sample_rows(w.N, seed=3)
+    oc, oa, os_ = cached_compress(oracle_rows, name, x, w.block, E_STAR)
+    stats = []
     for p in range(w.P):
-        oc, oa, os_, _ = O.compress(x[p][rows], w.block, E_STAR)
-        parity.compare_codes(codes[p][rows], oc, f"{name} codes[{p}]")
-        parity.compare_scales(alpha[p][rows], oa, f"{name} alpha[{p}]")
-        parity.compare_scales(s[p][rows], os_, f"{name} s[{p}]")
+        stats.append(parity.compare_codes(codes[p], oc[p], f"{name} codes[{p}]"))
+        parity.compare_scales(alpha[p], oa[p], f"{name} alpha[{p}]")
+        parity.compare_scales(s[p], os_[p], f"{name} s[{p}]")
         assert hdr[p]["s_max"] == s[p].max()
         assert hdr[p]["n_clamped"] == np.count_nonzero(s[p] > 1.0)
+    report(f"{name} tensor-core compress", stats)
     fc, fa, fs, _, _ = gpu_compress(x, w.block)
     for p in range(w.P):
         parity.compare_codes(codes[p], fc[p], f"{name} codes[{p}] vs CUDA-core path")

@@ -16,7 +16,7 @@ import parity
 from grads_taco_compress_gb300 import binding as tb
 from grads_taco_compress_gb300 import workloads as W
 from oracle import taco_oracle as O
-from test_gpu_parity import E_STAR, _sample_rows, bundle_from_arrays, host_bits
+from test_gpu_parity import E_STAR, bundle_from_arrays, host_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -95,16 +95,15 @@ def test_mma_decompress_guards_empty_and_block_256():
 
 
 @pytest.mark.parametrize("name", ["tiny-512x1024", "gpt2-1.5b-act", "gpt3-6.7b-act", "qwen-7b-long"])
-def test_mma_decompress_full_size_sampled(name):
-    """The benchmark's launch shape at full size: sampled rows against the oracle,
-    every element against the CUDA-core kernel."""
+def test_mma_decompress_full_size_every_element(name, oracle_rows):
+    """The benchmark's launch shape at full size: every element against the
+    oracle and against the CUDA-core kernel."""
     w = W.WORKLOADS[name]
     codes, alpha, s = W.make_random_bundle(w.N, w.h, w.block, w.P, seed=9)
     bundle = bundle_from_arrays(codes, alpha, s, w.block)
     got = host_bits(MMA(bundle, w.P, w.N, w.h, w.block))
-    rows = _sample_rows(w.N, seed=5)
-    want = O.decompress_reduce(codes[:, rows], alpha[:, rows], s[:, rows], w.block)
-    parity.compare_recon(O.bf16_bits_to_f64(got[rows]), O.bf16_bits_to_f64(want))
+    want = oracle_rows.decompress_reduce(codes, alpha, s, w.block)
+    parity.compare_recon(O.bf16_bits_to_f64(got), O.bf16_bits_to_f64(want))
     ref = host_bits(tb.taco_decompress_reduce(bundle, w.P, w.N, w.h, w.block))
     parity.compare_recon(O.bf16_bits_to_f64(got), O.bf16_bits_to_f64(ref), "against the CUDA-core kernel")
     assert np.all(np.isfinite(O.bf16_bits_to_f64(got)))

@@ -16,7 +16,7 @@ import parity
 from grads_taco_compress_gb300 import binding as tb
 from grads_taco_compress_gb300 import workloads as W
 from oracle import taco_oracle as O
-from test_gpu_parity import E_STAR, _sample_rows, bundle_from_arrays, dev_bf16, gpu_compress, host_bits
+from test_gpu_parity import E_STAR, bundle_from_arrays, dev_bf16, gpu_compress, host_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -108,21 +108,22 @@ def test_int8_empty_tensor():
 
 
 @pytest.mark.parametrize("name", ["gpt2-1.5b-act", "gpt3-6.7b-grad"])
-def test_int8_full_size_sampled(name):
+def test_int8_full_size_every_element(name, oracle_rows):
+    """Full size: every INT8 code, alpha and s against the oracle, and the
+    GPU's compress + decompress-reduce against the oracle's, every element."""
     w = W.WORKLOADS[name]
     x = W.make_shards(w)
     codes, alpha, s, hdr, bundle = gpu_compress(x, w.block, entry=tb.taco_compress_shards_int8)
-    rows = _sample_rows(w.N, seed=4)
+    oc, oa, os_ = oracle_rows.compress(x, w.block, E_STAR, O.VARIANT_DUAL, I8)
     for p in range(w.P):
-        oc, oa, os_, _ = O.compress(x[p][rows], w.block, E_STAR, O.VARIANT_DUAL, I8)
-        parity.compare_int8_codes(codes[p][rows], oc, f"{name} codes[{p}]")
-        parity.compare_scales(alpha[p][rows], oa, f"{name} alpha[{p}]")
-        parity.compare_scales(s[p][rows], os_, f"{name} s[{p}]")
+        parity.compare_int8_codes(codes[p], oc[p], f"{name} codes[{p}]")
+        parity.compare_scales(alpha[p], oa[p], f"{name} alpha[{p}]")
+        parity.compare_scales(s[p], os_[p], f"{name} s[{p}]")
         assert hdr[p]["s_max"] == s[p].max()
     assert not np.any(codes == 0x80)
     out = host_bits(tb.taco_decompress_reduce_int8(bundle, w.P, w.N, w.h, w.block))
-    want = O.decompress_reduce(codes[:, rows], alpha[:, rows], s[:, rows], w.block, I8)
-    parity.compare_recon(O.bf16_bits_to_f64(out[rows]), O.bf16_bits_to_f64(want))
+    want = oracle_rows.decompress_reduce(oc, oa, os_, w.block, I8)
+    parity.compare_recon(O.bf16_bits_to_f64(out), O.bf16_bits_to_f64(want))
 
 
 def _random_int8_bundle(N, h, block, P, seed):
