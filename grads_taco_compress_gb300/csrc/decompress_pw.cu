@@ -224,14 +224,9 @@ __global__ void __launch_bounds__(kDecompressThreads, 1) decompress_pw_kernel(De
       if (!ok || wvb == 0) continue;
 
       if constexpr (MODE == 1) {
-        // energy of x_hat: sum x_hat^2 / n = sum z^2
-        f2 ea[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
-#pragma unroll
-        for (int q = 0; q < kCH; ++q)
-#pragma unroll
-          for (int r = 0; r < 4; ++r) ea[r] = fma2(z[q][r], z[q][r], ea[r]);
-        const f2 e01 = add2(ea[0], ea[1]), e23 = add2(ea[2], ea[3]);
-        const float e = block_sum<LPB>((e01.x + e01.y) + (e23.x + e23.y));
+        // energy of x_hat: sum x_hat^2 / n = sum z^2, summed in an order that
+        // does not depend on the block's place in the tile
+        const float e = block_sum<LPB>(lane_sum_squares<false>(z, f2{1.f, 1.f}, f2{1.f, 1.f}));
         float rr = rsqrtf(e);
         rr = fmaf(fmaf(-0.5f * e * rr, rr, 0.5f), rr, rr);
         float alpha = (e > 0.f) ? clamp_alpha(a.sqrt_E * rr) : 1.0f;   // kept in [2^-126, 2^126]
@@ -255,16 +250,7 @@ __global__ void __launch_bounds__(kDecompressThreads, 1) decompress_pw_kernel(De
         const int nk = -kx, nk1 = nk >> 1;           // 2^-k = 2^nk1 2^(nk - nk1), both normal
         const f2 s1{exp2i(nk1), exp2i(nk1)}, s2{exp2i(nk - nk1), exp2i(nk - nk1)};
         if (any_far) {
-          f2 eb[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
-#pragma unroll
-          for (int q = 0; q < kCH; ++q)
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-              const f2 t = mul2(mul2(z[q][r], s1), s2);
-              eb[r] = fma2(t, t, eb[r]);
-            }
-          const f2 f01 = add2(eb[0], eb[1]), f23 = add2(eb[2], eb[3]);
-          const float e2 = block_sum<LPB>((f01.x + f01.y) + (f23.x + f23.y));
+          const float e2 = block_sum<LPB>(lane_sum_squares<true>(z, s1, s2));
           float r2 = rsqrtf(e2);
           r2 = fmaf(fmaf(-0.5f * e2 * r2, r2, 0.5f), r2, r2);
           alpha = (e2 > 0.f) ? clamp_alpha(a.sqrt_E * r2 * s1.x * s2.x) : 1.0f;

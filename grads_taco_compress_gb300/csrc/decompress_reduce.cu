@@ -257,14 +257,9 @@ decompress_reduce_kernel(DecompressArgs a) {
     if (!ok) break;
 
     if constexpr (MODE == 1) {
-      // energy of x_hat: sum x_hat^2 / n = sum z^2
-      f2 ea[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
-#pragma unroll
-      for (int q = 0; q < kCH; ++q)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) ea[i] = fma2(z[q][i], z[q][i], ea[i]);
-      const f2 e01 = add2(ea[0], ea[1]), e23 = add2(ea[2], ea[3]);
-      const float e = block_sum<LPB>((e01.x + e01.y) + (e23.x + e23.y));
+      // energy of x_hat: sum x_hat^2 / n = sum z^2, summed in an order that
+      // does not depend on the block's place in the tile
+      const float e = block_sum<LPB>(lane_sum_squares<false>(z, f2{1.f, 1.f}, f2{1.f, 1.f}));
       float r = rsqrtf(e);
       r = fmaf(fmaf(-0.5f * e * r, r, 0.5f), r, r);
       float alpha = (e > 0.f) ? clamp_alpha(a.sqrt_E * r) : 1.0f;   // kept in [2^-126, 2^126]
@@ -289,16 +284,7 @@ decompress_reduce_kernel(DecompressArgs a) {
       const int nk = -k, nk1 = nk >> 1;              // 2^-k = 2^nk1 2^(nk - nk1), both normal
       const f2 s1{exp2i(nk1), exp2i(nk1)}, s2{exp2i(nk - nk1), exp2i(nk - nk1)};
       if (any_far) {
-        f2 eb[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
-#pragma unroll
-        for (int q = 0; q < kCH; ++q)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const f2 t = mul2(mul2(z[q][i], s1), s2);
-            eb[i] = fma2(t, t, eb[i]);
-          }
-        const f2 f01 = add2(eb[0], eb[1]), f23 = add2(eb[2], eb[3]);
-        const float e2 = block_sum<LPB>((f01.x + f01.y) + (f23.x + f23.y));
+        const float e2 = block_sum<LPB>(lane_sum_squares<true>(z, s1, s2));
         float r2 = rsqrtf(e2);
         r2 = fmaf(fmaf(-0.5f * e2 * r2, r2, 0.5f), r2, r2);
         alpha = (e2 > 0.f) ? clamp_alpha(a.sqrt_E * r2 * s1.x * s2.x) : 1.0f;

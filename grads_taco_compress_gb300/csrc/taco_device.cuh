@@ -521,6 +521,34 @@ __device__ __forceinline__ void i8x4_to_f32(uint32_t four_codes, f2& v01, f2& v2
                 __uint_as_float(__byte_perm(t, 0x4B400000u, 0x7653))}, off);
 }
 
+// Sum of squares of a lane's 64 values (each scaled by s1 s2 when SCALED),
+// in an order that does not depend on the chunk-slot swizzle: each register
+// chunk in element order, then a tree that first adds registers q and q ^ 1,
+// then those sums at distance 2, then 4. XOR-ing the chunk slots with c maps
+// each pair of the tree onto a pair of the same level, and fp32 addition is
+// commutative, so the result depends only on the block's values and not on
+// where the block sits in its warp tile.
+template <bool SCALED>
+__device__ __forceinline__ float lane_sum_squares(const f2 (&z)[kCH][4], f2 s1, f2 s2) {
+  f2 c[kCH];
+#pragma unroll
+  for (int q = 0; q < kCH; ++q) {
+    f2 v[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) v[r] = SCALED ? mul2(mul2(z[q][r], s1), s2) : z[q][r];
+    f2 a = mul2(v[0], v[0]);
+    a = fma2(v[1], v[1], a);
+    a = fma2(v[2], v[2], a);
+    c[q] = fma2(v[3], v[3], a);
+  }
+#pragma unroll
+  for (int m = 1; m < kCH; m <<= 1)
+#pragma unroll
+    for (int q = 0; q < kCH; ++q)
+      if ((q & (2 * m - 1)) == 0) c[q] = add2(c[q], c[q + m]);
+  return c[0].x + c[0].y;
+}
+
 // Codes of one warp tile's lane (8 chunks of 8 elements, the layout above)
 // into shared memory at `base` (byte j + LPB (q ^ cx) * 8 of the block's row):
 // code = g * v, with v = 2^-k z when SCALED (s1 s2 = 2^-k), else z.

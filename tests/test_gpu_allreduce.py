@@ -93,3 +93,28 @@ def test_decompress_shards_each_shard_alone(block, P):
         assert torch.equal(out[p].view(torch.int16), single.view(torch.int16))
         want = O.decompress_reduce(codes[p:p + 1], alpha[p:p + 1], s[p:p + 1], block)
         parity.compare_recon(O.bf16_bits_to_f64(host_bits(out[p])), O.bf16_bits_to_f64(want))
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "int8"])
+@pytest.mark.parametrize("name,R,M,S", [("gpt2-1.5b-act", 4, 128, 4), ("gpt3-6.7b-act", 8, 64, 2),
+                                        ("gpt3-6.7b-grad", 2, 48, 3), ("tiny-512x1024", 2, 128, 8)])
+def test_pipelined_allreduce_equals_serial(name, R, M, S, fmt):
+    """Segments on three streams give the serial AllReduce's bits (every
+    block's arithmetic is the same), eagerly and replayed from a graph."""
+    from grads_taco_compress_gb300.allreduce import PipelinedTwoShotAllReduce
+    w = dataclasses.replace(W.WORKLOADS[name], P=R)
+    xs = dev_bf16(W.make_shards(w, N=M))
+    E = 900.0 if fmt == "int8" else E_STAR
+    serial = EmulatedTwoShotAllReduce(R, M, w.h, w.block, target_energy=E, fmt=fmt)(xs).clone()
+    pipe = PipelinedTwoShotAllReduce(R, M, w.h, w.block, segments=S, target_energy=E, fmt=fmt)
+    eager = pipe(xs).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(eager.view(torch.int16), serial.view(torch.int16))
+    g = pipe.capture(xs)
+    pipe.out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(pipe.out.view(torch.int16), serial.view(torch.int16))
+    if fmt == "e4m3":
+        want = oracle_allreduce(W.make_shards(w, N=M), w.block)
+        parity.compare_recon(O.bf16_bits_to_f64(host_bits(eager)), O.bf16_bits_to_f64(want), "pipelined output")
