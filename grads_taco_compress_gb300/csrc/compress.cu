@@ -7,7 +7,8 @@
 // energy, ASH and DS quantisation fused in one kernel, no intermediate
 // global-memory round trip):
 //   TMA bulk copy of the bf16 tile into shared memory -> block energy (fp32,
-//   packed FMAs, lane shuffles) -> FWHT of the raw block in registers and
+//   packed FMAs, lane shuffles; a block far from 1 is redone scaled by a
+//   power of two, far_tile) -> FWHT of the raw block in registers and
 //   shuffles (the rotation is linear, so alpha is applied afterwards together
 //   with 1/sqrt(n) and 1/s) -> alpha = sqrt(E*/E), s = max(1, alpha/sqrt(n) *
 //   max|Hx| / 448) (ABSMAX: without the floor; STATIC: the per-tensor
@@ -34,6 +35,73 @@ namespace taco {
 namespace {
 
 __device__ unsigned int g_compress_fault;
+
+// The warp's tile again, for a warp with at least one non-zero block whose
+// sum of squares is not a trusted fp32 number (subnormal squares, or a sum or
+// transform that may overflow). Runs after the common path has written its
+// codes into the stage (which no longer holds x), so every block of the tile
+// is read again from global memory (`xb`: the tile's first block) and scaled
+// by 2^-k (k the lane's: the exponent of the block's max |t| from the common
+// path, 128 if that overflowed; 0 for the blocks that were in range, which
+// repeats their computation exactly); its energy, alpha (2^-k put back, kept
+// in [2^-126, 2^126]), s and codes are computed as in the kernel and the
+// codes overwrite the stage's. Returns (alpha, s) of the lane's block. Rare,
+// so it is a call of its own: the common path keeps its registers.
+template <int NB, int VARIANT>
+__device__ __noinline__ float2 far_tile(const uint16_t* __restrict__ xb, bool valid, uint32_t stage, int sub,
+                                        int j, int cx, int k, float sqrt_nE, float inv_sqrt_n, float s_static) {
+  constexpr int LPB = NB / 64;
+  const int nk = -k, nk1 = nk >> 1;                   // 2^-k = 2^nk1 2^(nk - nk1), both normal
+  const f2 s1{exp2i(nk1), exp2i(nk1)}, s2{exp2i(nk - nk1), exp2i(nk - nk1)};
+  f2 v[kCH][4];
+  const uint4* src = reinterpret_cast<const uint4*>(xb + sub * NB);
+#pragma unroll
+  for (int q = 0; q < kCH; ++q) {
+    const uint4 r = valid ? __ldg(src + j + LPB * (q ^ cx)) : make_uint4(0u, 0u, 0u, 0u);
+    v[q][0] = mul2(mul2(f2{bf16_lo(r.x), bf16_hi(r.x)}, s1), s2);
+    v[q][1] = mul2(mul2(f2{bf16_lo(r.y), bf16_hi(r.y)}, s1), s2);
+    v[q][2] = mul2(mul2(f2{bf16_lo(r.z), bf16_hi(r.z)}, s1), s2);
+    v[q][3] = mul2(mul2(f2{bf16_lo(r.w), bf16_hi(r.w)}, s1), s2);
+  }
+  f2 ea[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll
+  for (int q = 0; q < kCH; ++q)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ea[i] = fma2(v[q][i], v[q][i], ea[i]);
+  const f2 e01 = add2(ea[0], ea[1]), e23 = add2(ea[2], ea[3]);
+  const float e = block_sum<LPB>((e01.x + e01.y) + (e23.x + e23.y));
+  float r = rsqrtf(e);
+  r = fmaf(fmaf(-0.5f * e * r, r, 0.5f), r, r);
+  const float alpha = (e > 0.f) ? clamp_alpha(sqrt_nE * r * s1.x * s2.x) : 1.0f;
+  // y = alpha 2^k t' / sqrt(n): 2^k undoes the scaling of the block
+  const float cscale = alpha * exp2i(-nk1) * exp2i(nk1 - nk) * inv_sqrt_n;
+  fwht_in_registers<kCH>(v, cx);
+  fwht_across_lanes<kCH, LPB>(v, j);
+  float hi = -INFINITY, lo = INFINITY;
+#pragma unroll
+  for (int q = 0; q < kCH; ++q)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      hi = max3(hi, v[q][i].x, v[q][i].y);
+      lo = min3(lo, v[q][i].x, v[q][i].y);
+    }
+  const float amax = cscale * block_max<LPB>(fmaxf(hi, -lo));
+  const float sc = (VARIANT == 0)   ? fmaxf(1.0f, amax * (1.0f / 448.0f))
+                   : (VARIANT == 1) ? (amax > 0.f ? amax * (1.0f / 448.0f) : 1.0f)
+                                    : s_static;
+  const f2 g2{__fdividef(cscale, sc), __fdividef(cscale, sc)};
+  const uint32_t cbase = stage + sub * NB;
+#pragma unroll
+  for (int q = 0; q < kCH; ++q) {
+    const f2 y0 = mul2(v[q][0], g2), y1 = mul2(v[q][1], g2);
+    const f2 y2 = mul2(v[q][2], g2), y3 = mul2(v[q][3], g2);
+    uint2 w;
+    w.x = e4m3x4_from_f32(y0.x, y0.y, y1.x, y1.y);
+    w.y = e4m3x4_from_f32(y2.x, y2.y, y3.x, y3.y);
+    sts64(cbase + 8 * (j + LPB * (q ^ cx)), w);
+  }
+  return make_float2(alpha, sc);
+}
 
 template <int NB, int VARIANT>
 __global__ void __launch_bounds__(kCompressThreads, kCompressMinBlocks)
@@ -100,34 +168,54 @@ compress_kernel(CompressArgs a) {
   uint32_t cphase = 0;
   bool ok = true;
 
-  for (; k < count; ++k) {
-    const bool got = mbar_wait(bar0 + 8 * cs, cphase);
-    if (!__all_sync(kFullMask, got)) {   // keep the warp's decision uniform
-      ok = false;
-      break;
+  // The tile being finished: its first block and blocks, stage, and this
+  // lane's block's (alpha, s).
+  int64_t b0 = 0;
+  int vb = 0;
+  uint32_t stage = 0;
+  float alpha = 1.0f, sc = 1.0f;
+  // Scale pair and header partials of the lane's block, the bulk store of the
+  // tile's codes, and the refill of the previous tile's stage.
+  auto finish_tile = [&]() {
+    if (sub < vb && j == 0) {
+      scales_out[b0 + sub] = make_float2(alpha, sc);     // 8 contiguous bytes per lane
+      part_smax = fmaxf(part_smax, sc);
+      part_cnt += (sc > 1.0f) ? 1u : 0u;
     }
-    int64_t b0;   // first block of the tile
-    int vb;       // blocks in the tile
-    ww.tile(k, b0, vb);
-    const int64_t b = b0 + sub;
-    const bool valid = sub < vb;
-    const uint32_t stage = stage0 + cs * TILE_BYTES;
+    fence_proxy_async_smem();   // this lane's codes are visible to the bulk store
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_1d(codes + b0 * NB, stage, static_cast<uint32_t>(vb) * NB);
+      bulk_commit();
+    }
+    // Refill the stage of the previous tile once its codes have left it.
+    if (k >= 1 && it < count) {
+      if (lane == 0) bulk_wait_read<1>();
+      issue_next();
+    }
+  };
 
-    f2 v[kCH][4];
-    float alpha, tmax;
-    // Pass 0 takes every block as it is. A non-zero block whose sum of
-    // squares is not a trusted fp32 number (subnormal squares, or a sum or
-    // transform that may overflow) makes the warp run a second pass over the
-    // same stage, with that block scaled by 2^-k (k the exponent of its max
-    // |t| from pass 0, 128 if that overflowed; exact) and 2^-k put back into
-    // alpha. The other blocks keep k = 0 and repeat pass 0's arithmetic.
-    int k_exp = 0;
-    for (int pass = 0;; ++pass) {
-      const int nk = -k_exp, nk1 = nk >> 1;            // 2^-k = 2^nk1 2^(nk - nk1), both normal
-      const float p1 = exp2i(nk1), p2 = exp2i(nk - nk1);
+  while (k < count) {
+    // The common path, tile after tile. A tile with a non-zero block whose
+    // sum of squares is not a trusted fp32 number (values far below or above
+    // 1) leaves the loop unfinished and is redone below with each such block
+    // scaled by a power of two (far_tile); keeping that call out of this loop
+    // keeps the loop's code what it is without it.
+    bool redo = false;
+    float tmax_far = 0.0f;
+    bool far = false;
+    for (; k < count; ++k) {
+      const bool got = mbar_wait(bar0 + 8 * cs, cphase);
+      if (!__all_sync(kFullMask, got)) {   // keep the warp's decision uniform
+        ok = false;
+        break;
+      }
+      ww.tile(k, b0, vb);
+      stage = stage0 + cs * TILE_BYTES;
+
+      f2 v[kCH][4];
       {
         const uint32_t base = stage + sub * (NB * 2);
-        const f2 s1{p1, p1}, s2{p2, p2};
 #pragma unroll
         for (int q = 0; q < kCH; ++q) {
           const uint4 r = lds128(base + 16 * (j + LPB * (q ^ cx)));
@@ -135,11 +223,11 @@ compress_kernel(CompressArgs a) {
           v[q][1] = f2{bf16_lo(r.y), bf16_hi(r.y)};
           v[q][2] = f2{bf16_lo(r.z), bf16_hi(r.z)};
           v[q][3] = f2{bf16_lo(r.w), bf16_hi(r.w)};
-          if (pass > 0) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) v[q][i] = mul2(mul2(v[q][i], s1), s2);
-          }
         }
+      }
+      if (++cs == D) {
+        cs = 0;
+        cphase ^= 1u;
       }
 
       // Block energy e = sum x^2 (E = e / NB): four packed accumulators, then
@@ -152,15 +240,16 @@ compress_kernel(CompressArgs a) {
       const f2 e01 = add2(ea[0], ea[1]), e23 = add2(ea[2], ea[3]);
       const float e = block_sum<LPB>((e01.x + e01.y) + (e23.x + e23.y));
 
-      // alpha = sqrt(E*/E) = 2^-k sqrt(n E*) / sqrt(e): reciprocal square
-      // root with one Newton step (error about one ulp), kept in
-      // [2^-126, 2^126]; 1 for an all-zero block. It does not depend on the
-      // rotation, so its latency overlaps the FWHT.
+      // alpha = sqrt(E*/E) = sqrt(n E*) / sqrt(e): reciprocal square root
+      // with one Newton step (error about one ulp), kept in [2^-126, 2^126];
+      // 1 for an all-zero block. It does not depend on the rotation, so its
+      // latency overlaps the FWHT.
       float r = rsqrtf(e);
       r = fmaf(fmaf(-0.5f * e * r, r, 0.5f), r, r);
-      alpha = (e > 0.f) ? clamp_alpha(a.sqrt_nE * r * p1 * p2) : 1.0f;
+      alpha = (e > 0.f) ? clamp_alpha(a.sqrt_nE * r) : 1.0f;
+      const float cscale = alpha * a.inv_sqrt_n;      // y = cscale * t
 
-      // Rotation of the (scaled) block: t = H x.
+      // Rotation of the raw block: t = H x.
       fwht_in_registers<kCH>(v, cx);
       fwht_across_lanes<kCH, LPB>(v, j);
 
@@ -176,58 +265,47 @@ compress_kernel(CompressArgs a) {
       }
       const float thi = max3(max3(hq[0], hq[1], hq[2]), max3(hq[3], hq[4], hq[5]), fmaxf(hq[6], hq[7]));
       const float tlo = min3(min3(lq[0], lq[1], lq[2]), min3(lq[3], lq[4], lq[5]), fminf(lq[6], lq[7]));
-      tmax = block_max<LPB>(fmaxf(thi, -tlo));
-      if (pass > 0) break;
-      const bool far = !(e >= kEnergyLo && e <= kEnergyHi) && !(tmax == 0.f);
-      if (!__any_sync(kFullMask, far)) break;
-      // max |x| <= max |t| <= n max |x|: the scaled block's max lies in [2^-8, 2)
-      k_exp = far ? (tmax <= 0x1.fffffep127f ? ilogbf(tmax) : 128) : 0;
-    }
-    // y = alpha 2^k t / sqrt(n): 2^k undoes the scaling of the block
-    const float cscale = alpha * exp2i((k_exp + 1) >> 1) * exp2i(k_exp - ((k_exp + 1) >> 1)) * a.inv_sqrt_n;
-    if (++cs == D) {
-      cs = 0;
-      cphase ^= 1u;
-    }
+      const float tmax = block_max<LPB>(fmaxf(thi, -tlo));
 
-    const float amax = cscale * tmax;
-    const float sc = (VARIANT == 0)   ? fmaxf(1.0f, amax * (1.0f / 448.0f))
-                     : (VARIANT == 1) ? (amax > 0.f ? amax * (1.0f / 448.0f) : 1.0f)
-                                      : a.s_static;
-    const float g = __fdividef(cscale, sc);           // code value = g * t
-    const f2 g2{g, g};
+      const float amax = cscale * tmax;
+      sc = (VARIANT == 0)   ? fmaxf(1.0f, amax * (1.0f / 448.0f))
+           : (VARIANT == 1) ? (amax > 0.f ? amax * (1.0f / 448.0f) : 1.0f)
+                            : a.s_static;
+      const float g = __fdividef(cscale, sc);         // code value = g * t
+      const f2 g2{g, g};
 
-    // Codes go back into the stage this tile came from (the tile's codes are
-    // half its bytes), then leave as one bulk store.
-    __syncwarp();   // every lane has read the stage before any lane overwrites it
-    {
-      const uint32_t base = stage + sub * NB;
+      // Codes go back into the stage this tile came from (the tile's codes
+      // are half its bytes), then leave as one bulk store.
+      __syncwarp();   // every lane has read the stage before any lane overwrites it
+      {
+        const uint32_t base = stage + sub * NB;
 #pragma unroll
-      for (int q = 0; q < kCH; ++q) {
-        const f2 y0 = mul2(v[q][0], g2), y1 = mul2(v[q][1], g2);
-        const f2 y2 = mul2(v[q][2], g2), y3 = mul2(v[q][3], g2);
-        uint2 w;
-        w.x = e4m3x4_from_f32(y0.x, y0.y, y1.x, y1.y);
-        w.y = e4m3x4_from_f32(y2.x, y2.y, y3.x, y3.y);
-        sts64(base + 8 * (j + LPB * (q ^ cx)), w);
+        for (int q = 0; q < kCH; ++q) {
+          const f2 y0 = mul2(v[q][0], g2), y1 = mul2(v[q][1], g2);
+          const f2 y2 = mul2(v[q][2], g2), y3 = mul2(v[q][3], g2);
+          uint2 w;
+          w.x = e4m3x4_from_f32(y0.x, y0.y, y1.x, y1.y);
+          w.y = e4m3x4_from_f32(y2.x, y2.y, y3.x, y3.y);
+          sts64(base + 8 * (j + LPB * (q ^ cx)), w);
+        }
       }
+      far = !(e >= kEnergyLo && e <= kEnergyHi) && !(tmax == 0.f);
+      if (__any_sync(kFullMask, far)) {
+        tmax_far = tmax;
+        redo = true;
+        break;
+      }
+      finish_tile();
     }
-    if (valid && j == 0) {
-      scales_out[b] = make_float2(alpha, sc);            // 8 contiguous bytes per lane
-      part_smax = fmaxf(part_smax, sc);
-      part_cnt += (sc > 1.0f) ? 1u : 0u;
-    }
-    fence_proxy_async_smem();   // this lane's codes are visible to the bulk store
-    __syncwarp();
-    if (lane == 0) {
-      tma_store_1d(codes + b0 * NB, stage, static_cast<uint32_t>(vb) * NB);
-      bulk_commit();
-    }
-    // Refill the stage of the previous tile once its codes have left it.
-    if (k >= 1 && it < count) {
-      if (lane == 0) bulk_wait_read<1>();
-      issue_next();
-    }
+    if (!redo) break;
+    // max |x| <= max |t| <= n max |x|: the scaled block's max lies in [2^-8, 2)
+    const int kf = far ? (tmax_far <= 0x1.fffffep127f ? ilogbf(tmax_far) : 128) : 0;
+    const float2 as = far_tile<NB, VARIANT>(x + b0 * NB, sub < vb, stage, sub, j, cx, kf, a.sqrt_nE,
+                                            a.inv_sqrt_n, a.s_static);
+    alpha = as.x;
+    sc = as.y;
+    finish_tile();
+    ++k;
   }
 
   if (!ok) {

@@ -19,8 +19,8 @@
 // so no thread reads x itself: alpha = n sqrt(E*) / sqrt(sum t^2).
 //
 // CTA = 11 warps, one per SM (its registers do not fit twice), with a ring of
-// 4 input stages for n <= 128 and 6 for n = 256 (a tile is 4 atoms), the
-// fastest shapes measured:
+// 5 input stages for n = 64 and 6 for n = 128 and 256, the fastest shapes
+// measured with the tile schedule below (4, 7 and 8 stages were slower):
 //   warp 0     TMA producer: 3-D tensor loads of [128 blocks x 64 elements]
 //              bf16 atoms (16 KB, 128-byte swizzle) into a ring of stages;
 //   warp 1     owns the tensor memory (2 accumulators x n columns) and one
@@ -76,7 +76,7 @@ struct Smem {
   static constexpr int NC = NB / 64;
   static constexpr int NG = compress_mma_groups(NB);               // epilogue groups
   static constexpr int threads = compress_mma_threads(NB);
-  static constexpr int kStages = NB == 256 ? 6 : 4;                 // 16 KB atoms in flight
+  static constexpr int kStages = NB == 64 ? 5 : 6;                  // 16 KB atoms in flight
   static constexpr uint32_t stages = 0;
   static constexpr uint32_t hmat = stages + kStages * kAtomBytes;
   static constexpr uint32_t codes = hmat + kHBytes;                 // [group][chunk] atoms
@@ -553,10 +553,6 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
       const bool fast = (tmx >= kTrustLo && tmx <= kTrustHi) || tmx == 0.f;
       const bool rescale = !fast && tmx >= kRescaleLo && tmx <= kRescaleHi;
       const bool exact = !fast && !rescale;       // NaN lands here too
-      // A rescaled block also takes its codes from 2^-k t with the factor
-      // times 2^k: t / s of a block of tiny t can exceed the fp32 range
-      // (ABSMAX: 448 / max |t|) although every code is finite. Lanes that
-      // need no rescale take k = 0, which changes nothing.
       const bool any_rescale = __any_sync(kFullMask, rescale);
       const int kr = rescale ? ilogbf(tmx) : 0;
       const int nkr = -kr, nkr1 = nkr >> 1;       // 2^-k = 2^nkr1 2^(nkr - nkr1), both normal
@@ -588,21 +584,27 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
       float sc = (VARIANT == 0)   ? fmaxf(1.0f, amax * (1.0f / QMAX))
                  : (VARIANT == 1) ? (amax > 0.f ? amax * (1.0f / QMAX) : 1.0f)
                                   : a.s_static;
-      const float gsc = __fdividef(ldexpf(cscale, kr), sc);  // code value = gsc * (2^-k t)
+      // code value = gsc * t. Where that factor leaves the fp32 range (a
+      // rescaled block of tiny t: ABSMAX's 448 / max |t|, or a tiny E* in
+      // STATIC) the warp takes its codes from 2^-k t with the factor times
+      // 2^k instead, which stays finite; lanes with k = 0 are unchanged.
+      const float gplain = __fdividef(cscale, sc);
+      const bool scaled = __any_sync(kFullMask, rescale && !(gplain <= 0x1.fffffep127f));
+      const float gsc = scaled ? __fdividef(ldexpf(cscale, kr), sc) : gplain;
 
       // pass 2: codes (one slice: the values are still in registers)
       if constexpr (NC == 1) {
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(base + S::tempty + 8 * g);
-        if (any_rescale) scale_slice<NC, SL>(u, s1, s2);
+        if (scaled) scale_slice<NC, SL>(u, s1, s2);
         slice_codes<NC, SL, FMT, VARIANT == 2>(u, 0, gsc, staging, row);
       } else {
 #pragma unroll 1
         for (int sl = 0; sl < NC; ++sl) {
           load_slice<NC, SL>(tacc, sl, u);
           chunk_butterflies<NC, SL>(u);
-          if (any_rescale) scale_slice<NC, SL>(u, s1, s2);
+          if (scaled) scale_slice<NC, SL>(u, s1, s2);
           slice_codes<NC, SL, FMT, VARIANT == 2>(u, sl, gsc, staging, row);
         }
         tc_fence_before();

@@ -17,7 +17,7 @@
 // What differs is who moves the data. One CTA of 16 warps per SM: warp 15
 // alone issues the copies, one shard of a CTA tile per stage (the tile's
 // codes and its (alpha, s) pairs, two 1-D bulk copies), into a ring of
-// kPwStages stages that the 15 consumer warps share. A CTA tile is 15 warp
+// kStages stages that the 15 consumer warps share. A CTA tile is 15 warp
 // tiles of 2048 elements (480, 240 or 120 blocks); consumer warp w reads warp
 // tile w of every stage and arrives on the stage's "empty" barrier once it
 // has read it, so the consumers spend no issue slots on copy bookkeeping.
@@ -37,7 +37,6 @@ namespace {
 __device__ unsigned int g_decompress_pw_fault;
 
 constexpr int kPwCons = 15;                                  // consumer warps
-constexpr int kPwStages = 4;
 constexpr uint32_t kPwCodes = kPwCons * kTileElems;          // codes of one CTA tile: 30720 B
 static_assert(kPwCons + 1 == kDecompressThreads / 32, "one producer warp and the consumers");
 
@@ -46,10 +45,11 @@ struct PwShape {
   static constexpr int LPB = NB / 64;                        // lanes per block
   static constexpr int BPT = 32 / LPB;                       // blocks per warp tile
   static constexpr int TB = kPwCons * BPT;                   // blocks per CTA tile
+  static constexpr int kStages = 4;                          // stages in the ring
   static constexpr uint32_t stage = kPwCodes + TB * 8;       // codes + (alpha, s) pairs
   static constexpr uint32_t out = kTileElems * 2;            // per consumer warp: a bf16 warp tile
-  static constexpr uint32_t bars = kPwStages * stage + kPwCons * out;
-  static constexpr uint32_t smem = bars + 2 * 8 * kPwStages + 16;
+  static constexpr uint32_t bars = kStages * stage + kPwCons * out;
+  static constexpr uint32_t smem = bars + 2 * 8 * kStages + 16;
   static_assert(stage % 16 == 0 && out % 16 == 0, "TMA destinations 16-byte aligned");
 };
 
@@ -116,6 +116,7 @@ template <int NB, int MODE, int VARIANT, int FMT>
 __global__ void __launch_bounds__(kDecompressThreads, 1) decompress_pw_kernel(DecompressArgs a) {
   using S = PwShape<NB>;
   constexpr int LPB = S::LPB, BPT = S::BPT, TB = S::TB;
+  constexpr int kPwStages = S::kStages;
   extern __shared__ __align__(128) unsigned char smem[];
   const uint32_t base = smem_u32(smem);
   const uint32_t full0 = base + S::bars, empty0 = full0 + 8 * kPwStages;
