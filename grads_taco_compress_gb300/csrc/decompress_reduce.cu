@@ -60,10 +60,17 @@ __global__ void __launch_bounds__(kDecompressThreads, kDecompressMinBlocks)
 decompress_reduce_kernel(DecompressArgs a) {
   constexpr int LPB = NB / 64;
   constexpr int BPT = 32 / LPB;
-  constexpr int D = kDecompressStages;
+  // Stages in flight per warp: 3 for the n = 128 decompress-reduce of E4M3
+  // codes, 4 for the other shapes, modes and formats (measured on GB300:
+  // qwen-7b-long 96.2 -> 93.8 us and gpt3-6.7b-act 57.1 -> 56.0 us with 3;
+  // the reduce-recompress at n = 128, the INT8 codes (95.9 -> 96.9 us) and
+  // every launch at n = 256 were as fast or faster with 4, and 2 was slower
+  // everywhere). The shared memory is sized for 4.
+  constexpr int D = (NB == 128 && MODE == 0 && FMT == 0) ? 3 : kDecompressStages;
   constexpr int WARPS = kDecompressThreads / 32;
   static_assert(LPB >= 1 && LPB <= 4, "block size");
   static_assert(BPT * 8 <= kScaleBytes, "scale slot");
+  static_assert(D <= kDecompressStages, "the shared memory holds kDecompressStages stages per warp");
 
   extern __shared__ __align__(128) unsigned char smem[];
 
