@@ -34,16 +34,24 @@
 //              into a 64-byte-swizzled staging buffer that one thread stores
 //              with 3-D TMA tensor stores, and stores its (alpha, s) pair;
 //   warp 10    tile scheduler (below).
-// Tile schedule: the CTAs of a shard take 3/4 of the per-CTA share of
-// tiles round-robin (tile blockIdx.x + k * gridDim.x), then claim
-// the rest one at a time from the shard's counter in the workspace, so that
-// the CTAs that stream faster take more of them and the CTAs of a launch
-// finish together (with a static split the spread of per-SM progress grew
-// through the launch to several tiles). The scheduler lane keeps two claims
-// ready in a shared-memory ring, which hides the atomic's round trip from
-// the producer. A tile's index reaches the MMA lane with the barrier of its
-// first atom and the epilogue group with the group's `info` barrier; a -1
-// ends every role.
+// Tile schedule: the CTAs of shard y (gridDim.x of them, blockIdx.y == y)
+// take 3/4 of the per-CTA share of that shard's tiles round-robin (tile
+// blockIdx.x + k * gridDim.x), then every CTA claims the rest of all shards'
+// tiles one at a time from one counter in the workspace (shard 0's tile
+// word), shards interleaved. So the CTAs that stream faster take more, and
+// the CTAs of a launch finish together: with a static split the spread of
+// per-SM progress grew through the launch to several tiles, and with one
+// pool per shard whole shards finished apart (gpt3-6.7b-grad: the median
+// CTA of the slowest shard 6 us after that of the fastest). The scheduler
+// lane keeps two claims ready in a shared-memory ring, which hides the
+// atomic's round trip from the producer. A tile travels as one int, its
+// shard in bits 24 and up (a tile index needs 24 bits); it reaches the MMA
+// lane with the barrier of its first atom and the epilogue group with the
+// group's `info` barrier; a -1 ends every role.
+// Before it waits for the preceding grid, the producer asks L2 for the
+// tiles of its first ring of stages (a prefetch returns no data, so it is
+// safe before that grid's writes are visible): the launch's first loads
+// then find their data in L2 instead of waiting a DRAM round trip.
 // FMT selects the code format: 0 = FP8 E4M3 (Q_max 448), 1 = the INT8
 // fallback (Q_max 127, round half to even; pt summary §5, hardware without
 // FP8).
@@ -69,6 +77,10 @@ constexpr int kClaims = 2;                    // claimed tiles in flight, schedu
 constexpr uint32_t kAtomBytes = kRows * 64 * 2;       // 16 KB of bf16
 constexpr uint32_t kCodeAtomBytes = kRows * 64;       // 8 KB of codes
 constexpr uint32_t kHBytes = 64 * 64 * 2;             // H_64 in bf16
+constexpr int kItemShift = 24;                        // tile item: shard << 24 | tile
+static_assert((kMmaMaxBlocks + kRows - 1) / kRows < (int64_t{1} << kItemShift) &&
+                  (int64_t{TACO_MAX_SHARDS} << kItemShift) <= INT32_MAX,
+              "a tile item fits an int");
 
 // Shared memory map (offsets from a 1024-byte aligned base) and CTA shape.
 template <int NB>
@@ -96,7 +108,10 @@ struct Smem {
   static constexpr uint32_t tile_ring = abort_flag + 4;   // int[kRing]: tile of the CTA's tile k
   static constexpr uint32_t tile_of = tile_ring + 4 * kRing;      // int[NG]: tile of accumulator g
   static constexpr uint32_t claim = tile_of + 4 * NG;             // int[kClaims]: claimed tiles
-  static constexpr uint32_t end = claim + 4 * kClaims;
+  // u32[TACO_MAX_SHARDS] each: the CTA's largest s bits and count of s > 1 per shard
+  static constexpr uint32_t hdr_max = claim + 4 * kClaims;
+  static constexpr uint32_t hdr_cnt = hdr_max + 4 * TACO_MAX_SHARDS;
+  static constexpr uint32_t end = hdr_cnt + 4 * TACO_MAX_SHARDS;
   static constexpr uint32_t bytes = end + 1024;                     // + alignment slack
 };
 
@@ -337,15 +352,18 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
   volatile int* tile_ring = reinterpret_cast<volatile int*>(sbase + S::tile_ring);
   volatile int* tile_of = reinterpret_cast<volatile int*>(sbase + S::tile_of);
   volatile int* claim = reinterpret_cast<volatile int*>(sbase + S::claim);
+  unsigned int* const hdr_max = reinterpret_cast<unsigned int*>(sbase + S::hdr_max);
+  unsigned int* const hdr_cnt = reinterpret_cast<unsigned int*>(sbase + S::hdr_cnt);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int shard = blockIdx.y;
+  const int P = gridDim.y;
   const int64_t nblocks = a.nblocks;
   const int64_t ntiles = (nblocks + kRows - 1) / kRows;
   const int64_t G = gridDim.x;
   // round-robin tiles per CTA: 3/4 of the even share, rounded up (a CTA with
-  // one tile starts it without waiting for a claim)
+  // one tile starts it without waiting for a claim); n_static * G <= ntiles
   const int n_static = static_cast<int>((3 * (ntiles / G) + 3) / 4);
 
   // ---- set-up: barriers, H_64, tensor memory ----
@@ -367,6 +385,7 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
     *abort_flag = 0u;
     fence_mbar_init();
   }
+  if (threadIdx.x < 2 * TACO_MAX_SHARDS) hdr_max[threadIdx.x] = 0u;   // hdr_cnt follows hdr_max
   // H_64 (entries (-1)^popcount(r & k)) as B: 64 rows of 128 bytes, K-major,
   // 16-byte pieces swizzled by (row & 7).
   for (int p = threadIdx.x; p < 64 * 8; p += kThreads) {
@@ -389,22 +408,27 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
   const uint32_t tmem = lds_u32(base + S::tmem_slot);
 
   grid_launch_dependents();
+  if (warp == 0 && lane == 0) {
+    prefetch_map(&map_x);
+    // the tiles of the first ring of stages into L2 while the preceding grid
+    // finishes (no data reaches this CTA before the wait below)
+    const int npf = min(n_static, (kStages + NC - 1) / NC);
+    for (int k = 0; k < npf; ++k)
+      for (int c = 0; c < NC; ++c)
+        tma_prefetch_3d(&map_x, c * 64, static_cast<int>((blockIdx.x + k * G) * kRows), shard);
+  }
   grid_dependency_wait();   // no global access before the preceding grid is done
-
-  float part_smax = 0.0f;
-  uint32_t part_cnt = 0;
 
   if (warp == 0) {
     // ---------------------------------------------------- TMA producer ----
     if (lane == 0) {
-      prefetch_map(&map_x);
       const uint64_t policy = l2_evict_first_policy();
       uint32_t i = 0;
       bool ok = true;
       for (int k = 0; ok; ++k) {
-        int tile;
+        int tile;   // the tile item: shard << kItemShift | tile, or -1
         if (k < n_static) {
-          tile = static_cast<int>(blockIdx.x + static_cast<int64_t>(k) * G);
+          tile = (shard << kItemShift) | static_cast<int>(blockIdx.x + static_cast<int64_t>(k) * G);
         } else {
           const uint32_t j = static_cast<uint32_t>(k - n_static), c = j % kClaims;
           if (!wait_here(base + S::cfull + 8 * c, (j / kClaims) & 1u, abort_flag)) break;
@@ -422,7 +446,8 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
             mbar_arrive(base + S::full + 8 * s);   // the end: an arrival without a copy
           } else {
             mbar_arrive_expect_tx(base + S::full + 8 * s, kAtomBytes);
-            tma_load_3d(base + S::stages + s * kAtomBytes, &map_x, c * 64, tile * kRows, shard,
+            tma_load_3d(base + S::stages + s * kAtomBytes, &map_x, c * 64,
+                        (tile & ((1 << kItemShift) - 1)) * kRows, tile >> kItemShift,
                         base + S::full + 8 * s, policy);
           }
         }
@@ -488,14 +513,17 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
   } else if (warp == kSchedWarp) {
     // ---------------------------------------------------- tile scheduler ----
     if (lane == 0) {
-      unsigned int* next =
-          reinterpret_cast<unsigned int*>(a.workspace + shard * kWorkspaceShardStride) + 1;
-      const int64_t first = static_cast<int64_t>(n_static) * G;   // first tile of the pool
+      // one pool for the whole launch: shard 0's tile word; item j of the
+      // pool is tile first + j / P of shard j % P
+      unsigned int* next = reinterpret_cast<unsigned int*>(a.workspace) + 1;
+      const int64_t first = static_cast<int64_t>(n_static) * G;   // first tile of each shard's pool
+      const int64_t pool = (ntiles - first) * P;
       for (uint32_t j = 0;; ++j) {
         const uint32_t c = j % kClaims;
         if (!wait_here(base + S::cempty + 8 * c, ((j / kClaims) & 1u) ^ 1u, abort_flag)) break;
-        const int64_t t = first + atomicAdd(next, 1u);
-        const int tile = t < ntiles ? static_cast<int>(t) : -1;
+        const int64_t t = atomicAdd(next, 1u);
+        const int tile = t < pool ? (static_cast<int>(t % P) << kItemShift) | static_cast<int>(first + t / P)
+                                  : -1;
         claim[c] = tile;
         mbar_arrive(base + S::cfull + 8 * c);
         if (tile < 0) break;
@@ -510,8 +538,6 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
     const bool leader = (warp == 2 + 4 * g) && lane == 0;
     const uint32_t tacc = tmem + (static_cast<uint32_t>(quad * 32) << 16) + g * NB;
     const uint32_t staging = base + S::codes + g * NC * kCodeAtomBytes;
-    uint8_t* shard_base = a.bundle + static_cast<size_t>(shard) * a.shard_bytes;
-    float2* __restrict__ scales_out = reinterpret_cast<float2*>(shard_base + a.scales_off);
     if (leader) prefetch_map(&map_codes);
 
     for (int k = g;; k += NG) {
@@ -524,7 +550,8 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
       if (group_any(1 + g, !got || *abort_flag != 0u)) break;
       tc_fence_after();
 
-      const int64_t tile = tile_k;
+      const int ts = tile_k >> kItemShift;                     // the tile's shard
+      const int64_t tile = tile_k & ((1 << kItemShift) - 1);
       const int64_t b = tile * kRows + row;
       const bool valid = b < nblocks;
 
@@ -613,7 +640,7 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
       }
       if (exact && valid) {
         const float2 as = exact_block<NB, VARIANT, FMT>(
-            a.x + static_cast<int64_t>(shard) * a.shard_elems + b * NB, a.sqrt_nE, a.inv_sqrt_n,
+            a.x + static_cast<int64_t>(ts) * a.shard_elems + b * NB, a.sqrt_nE, a.inv_sqrt_n,
             a.s_static, staging, row);
         alpha = as.x;
         sc = as.y;
@@ -625,13 +652,20 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
 #pragma unroll
         for (int c = 0; c < NC; ++c)
           tma_store_3d(&map_codes, staging + c * kCodeAtomBytes, c * 64,
-                       static_cast<int>(tile * kRows), shard);
+                       static_cast<int>(tile * kRows), ts);
         bulk_commit();
       }
-      if (valid) {
-        scales_out[b] = make_float2(alpha, sc);
-        part_smax = fmaxf(part_smax, sc);
-        part_cnt += (sc > 1.0f) ? 1u : 0u;
+      if (valid)
+        reinterpret_cast<float2*>(a.bundle + static_cast<size_t>(ts) * a.shard_bytes + a.scales_off)[b] =
+            make_float2(alpha, sc);
+      // the warp's share of its shard's header: the largest s (bits of a
+      // positive float order like its value; fmaxf drops NaN) and the count
+      // of s > 1
+      const uint32_t wmax = __reduce_max_sync(kFullMask, valid ? __float_as_uint(fmaxf(sc, 0.0f)) : 0u);
+      const uint32_t wcnt = __popc(__ballot_sync(kFullMask, valid && sc > 1.0f));
+      if (lane == 0) {
+        atomicMax(hdr_max + ts, wmax);
+        atomicAdd(hdr_cnt + ts, wcnt);
       }
     }
   }
@@ -639,9 +673,15 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
   // ---- tear-down: the per-tensor header (its arrival count overlaps the
   // last stores), then free the tensor memory once every store has read
   // the staging buffer (the kernel's end makes the stored codes visible) ----
+  // every CTA arrives on every shard's header (a CTA may have compressed
+  // tiles of any shard), so a shard's header is written once all G * P CTAs
+  // have brought their share
   tc_fence_before();
-  finish_header<kThreads>(part_smax, part_cnt, a.workspace + shard * kWorkspaceShardStride,
-                          a.headers + shard, a.N, a.h, NB, VARIANT, a.target_energy, QMAX);
+  __syncthreads();
+  if (threadIdx.x < P)
+    arrive_header(__uint_as_float(hdr_max[threadIdx.x]), hdr_cnt[threadIdx.x], G * P,
+                  a.workspace + threadIdx.x * kWorkspaceShardStride, a.headers + threadIdx.x, a.N, a.h, NB,
+                  VARIANT, a.target_energy, QMAX);
   if (warp >= 2 && warp < kSchedWarp && (warp - 2) % 4 == 0 && lane == 0) bulk_wait_read<0>();
   __syncthreads();
   if (warp == 1) {

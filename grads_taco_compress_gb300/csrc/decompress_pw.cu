@@ -136,6 +136,19 @@ __global__ void __launch_bounds__(kDecompressThreads, 1) decompress_pw_kernel(De
   }
   __syncthreads();
   grid_launch_dependents();
+  if (warp == kPwCons && lane == 0) {
+    // the CTA's first tile of the first shards (the first ring of stages)
+    // into L2 while the preceding grid finishes (a prefetch returns no data,
+    // so it may come before the wait)
+    int64_t b0 = 0;
+    int vb = 0;
+    if (it.total > 0) it.get(0, b0, vb);
+    if (vb > 0)
+      for (int p = 0; p < P && p < kPwStages; ++p) {
+        bulk_prefetch_l2(shard_of[p] + b0 * NB, static_cast<uint32_t>(vb) * NB);
+        bulk_prefetch_l2(shard_of[p] + a.scales_off + b0 * 8, (static_cast<uint32_t>(vb) * 8 + 15) & ~15u);
+      }
+  }
   grid_dependency_wait();   // no global access before the preceding grid is done
 
   float part_smax = 0.0f;   // reduce-recompress header partials (lane j == 0)

@@ -118,6 +118,24 @@ decompress_reduce_kernel(DecompressArgs a) {
     __syncwarp();
   }
   grid_launch_dependents();
+  if (lane == 0) {
+    // the first stages this warp copies (its first tile, or the CTA's item
+    // with the warp's index, which the warps claim first; shards 0 .. D-1)
+    // into L2 while the preceding grid finishes: a prefetch returns no
+    // data, so it may come before the wait
+    int64_t pb0 = -1;
+    int pvb = 0;
+    if constexpr (CLAIM) {
+      if (!cw.item(warp, pb0, pvb)) pb0 = -1;
+    } else if (ntiles > 0) {
+      ww.tile(0, pb0, pvb);
+    }
+    if (pb0 >= 0 && pvb > 0)
+      for (int p = 0; p < P && p < D; ++p) {
+        bulk_prefetch_l2(shard_of[p] + pb0 * NB, static_cast<uint32_t>(pvb) * NB);
+        bulk_prefetch_l2(shard_of[p] + a.scales_off + pb0 * 8, (static_cast<uint32_t>(pvb) * 8 + 15) & ~15u);
+      }
+  }
   grid_dependency_wait();   // no global access before the preceding grid is done
 
   // Producer state, kept identical in every lane (lane 0 issues the copies):

@@ -213,6 +213,12 @@ __device__ __forceinline__ void tma_load_1d(uint32_t dst, const void* src, uint3
       " [%0], [%1], %2, [%3], %4;"
       :: "r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy) : "memory");
 }
+// 1-D bulk prefetch global -> L2: src 16-byte aligned, bytes a multiple of
+// 16. Like the tensor form it returns nothing to the thread, so it may run
+// before the preceding grid's writes are visible.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(src), "r"(bytes) : "memory");
+}
 // L2 policy for data read once: evict first.
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t p;
@@ -439,15 +445,47 @@ __device__ __forceinline__ float block_max(float v) {
   return v;
 }
 
-// Per-tensor header of one shard, written in the same launch. Every thread
-// brings its (max s, count of s > 1); the CTA reduces them and folds the
-// result into two running totals in the shard's workspace (an atomic max on
-// the float's bits, which order like the values because every s is positive
-// and fmaxf drops NaN, and an atomic add), then counts its arrival with one
-// acquire-release add. The CTA that arrives last takes both totals with one
-// 64-bit exchange that also zeroes them, writes the header and resets the
-// counter: two dependent round trips to L2 after the last CTA's work.
+// Per-tensor header of one shard, written in the same launch. A CTA folds
+// its (max s, count of s > 1) into two running totals in the shard's
+// workspace (an atomic max on the float's bits, which order like the values
+// because every s is positive and fmaxf drops NaN, and an atomic add), then
+// counts its arrival with one acquire-release add. The arrival that
+// completes the count takes both totals with one 64-bit exchange that also
+// zeroes them, writes the header and resets the counter: two dependent round
+// trips to L2 after the last CTA's work.
 // Workspace of a shard (16 bytes): [u32 arrivals | u32 tile claims | u32 max-s bits | u32 count].
+__device__ __forceinline__ void arrive_header(float m, uint32_t n, uint32_t arrivals, uint8_t* ws_shard,
+                                              taco_header* hd, int64_t N, int64_t h, int block,
+                                              int variant, float target_energy, float q_max) {
+  uint32_t* counter = reinterpret_cast<uint32_t*>(ws_shard);
+  uint32_t* totals = reinterpret_cast<uint32_t*>(ws_shard + 8);   // 8-byte aligned pair
+  if (m > 0.0f)
+    asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(totals), "r"(__float_as_uint(m)) : "memory");
+  if (n != 0u)
+    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(totals + 1), "r"(n) : "memory");
+  // the release publishes this CTA's two updates; in the last arrival the
+  // acquire orders the exchange below after every other CTA's updates
+  uint32_t arrived;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(arrived) : "l"(counter) : "memory");
+  if (arrived != arrivals - 1u) return;
+  unsigned long long t;
+  asm volatile("atom.exch.relaxed.gpu.global.b64 %0, [%1], 0;" : "=l"(t) : "l"(totals) : "memory");
+  hd->N = N;
+  hd->h = h;
+  hd->block = block;
+  hd->variant = variant;
+  hd->target_energy = target_energy;
+  hd->q_max = q_max;
+  hd->s_max = __uint_as_float(static_cast<uint32_t>(t));
+  hd->n_clamped = static_cast<uint32_t>(t >> 32);
+  // with the exchange, leaves the workspace zero-filled for the next call
+  // (the arrival counter and the word after it, the tile-claim counter of
+  // the tensor-core compress, whose claims all came before the arrivals)
+  *reinterpret_cast<unsigned long long*>(ws_shard) = 0ull;
+}
+
+// One shard per CTA row (gridDim.x CTAs each): every thread brings its
+// (max s, count of s > 1), the CTA reduces them and arrives once.
 template <int THREADS>
 __device__ void finish_header(float part_smax, uint32_t part_cnt, uint8_t* ws_shard,
                               taco_header* hd, int64_t N, int64_t h, int block, int variant,
@@ -474,29 +512,7 @@ __device__ void finish_header(float part_smax, uint32_t part_cnt, uint8_t* ws_sh
     m = fmaxf(m, sh_max[w]);
     n += sh_cnt[w];
   }
-  uint32_t* counter = reinterpret_cast<uint32_t*>(ws_shard);
-  uint32_t* totals = reinterpret_cast<uint32_t*>(ws_shard + 8);   // 8-byte aligned pair
-  asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(totals), "r"(__float_as_uint(m)) : "memory");
-  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(totals + 1), "r"(n) : "memory");
-  // the release publishes this CTA's two updates; in the last CTA the
-  // acquire orders the exchange below after every other CTA's updates
-  uint32_t arrived;
-  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(arrived) : "l"(counter) : "memory");
-  if (arrived != gridDim.x - 1) return;
-  unsigned long long t;
-  asm volatile("atom.exch.relaxed.gpu.global.b64 %0, [%1], 0;" : "=l"(t) : "l"(totals) : "memory");
-  hd->N = N;
-  hd->h = h;
-  hd->block = block;
-  hd->variant = variant;
-  hd->target_energy = target_energy;
-  hd->q_max = q_max;
-  hd->s_max = __uint_as_float(static_cast<uint32_t>(t));
-  hd->n_clamped = static_cast<uint32_t>(t >> 32);
-  // with the exchange, leaves the workspace zero-filled for the next call
-  // (the arrival counter and the word after it, the tile counter of the
-  // tensor-core compress, whose claims all came before the arrivals)
-  *reinterpret_cast<unsigned long long*>(ws_shard) = 0ull;
+  arrive_header(m, n, gridDim.x, ws_shard, hd, N, h, block, variant, target_energy, q_max);
 }
 
 template <bool CLAMP>

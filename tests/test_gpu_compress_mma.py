@@ -194,6 +194,41 @@ def test_header_totals_over_the_full_grid(entry):
         assert hdr[p]["n_clamped"] == np.count_nonzero(s[p] > 1.0)
 
 
+@pytest.mark.parametrize("variant", [tb.VARIANT_DUAL, tb.VARIANT_ABSMAX])
+def test_headers_per_shard_under_the_shared_tile_pool(variant, oracle_rows):
+    """Eight shards, about a quarter of whose tiles go to one pool that every
+    CTA claims from, shards interleaved, so a CTA compresses tiles of other
+    shards than its own. Every header must still reduce its own shard's s
+    only: each shard has its own seeded data (so its own largest s and its
+    own count of s > 1; E* = 30000 clamps about one block in eight under
+    DUAL), and the headers are compared with the oracle's s of that shard.
+    A tile folded into another shard's totals moves a count or a maximum."""
+    P, N, h, n, E = 8, 2048, 1600, 64, 30000.0
+    x = W.make_shards(W.WORKLOADS["gpt2-1.5b-act"], N=N, P=P)
+    ws = tb.new_workspace(P)
+    bundle, headers = MMA(dev_bf16(x), n, E, variant, workspace=ws)
+    codes, alpha, s = tb.shard_views(bundle, P, N, h, n)
+    torch.cuda.synchronize()
+    assert int(ws.count_nonzero()) == 0
+    codes, alpha, s = codes.cpu().numpy(), alpha.cpu().numpy(), s.cpu().numpy()
+    hdr = tb.parse_headers(headers)
+    oc, oa, os_ = oracle_rows.compress(x, n, E, variant)
+    maxima = set()
+    for p in range(P):
+        parity.compare_codes(codes[p], oc[p], f"codes[{p}]")
+        parity.compare_scales(alpha[p], oa[p], f"alpha[{p}]")
+        parity.compare_scales(s[p], os_[p], f"s[{p}]")
+        assert hdr[p]["s_max"] == s[p].max()
+        assert abs(hdr[p]["s_max"] - os_[p].max()) <= 1e-6 * os_[p].max()
+        assert hdr[p]["n_clamped"] == np.count_nonzero(s[p] > 1.0)
+        near_one = np.count_nonzero(np.abs(os_[p].astype(np.float64) - 1.0) < 1e-6)
+        assert abs(int(hdr[p]["n_clamped"]) - np.count_nonzero(os_[p] > 1.0)) <= near_one
+        maxima.add(float(hdr[p]["s_max"]))
+    assert len(maxima) == P                  # the shards' headers differ
+    if variant == tb.VARIANT_DUAL:
+        assert min(int(hdr[p]["n_clamped"]) for p in range(P)) > 100
+
+
 FULL = ["tiny-512x1024", "gpt2-1.5b-act", "gpt3-6.7b-act", "gpt3-6.7b-grad", "qwen-7b-long"]
 
 
