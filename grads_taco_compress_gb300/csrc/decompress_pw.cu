@@ -48,6 +48,9 @@ struct PwShape {
   static constexpr int kStages = 4;                          // stages in the ring
   static constexpr uint32_t stage = kPwCodes + TB * 8;       // codes + (alpha, s) pairs
   static constexpr uint32_t out = kTileElems * 2;            // per consumer warp: a bf16 warp tile
+  // (reduce-recompress: the warp tile's codes, then its (alpha, s) pairs)
+  static_assert(NB * BPT + 8 * BPT <= out, "codes and pairs of a warp tile fit the output buffer");
+  static_assert((NB * BPT) % 16 == 0, "pairs staging 16-byte aligned");
   static constexpr uint32_t bars = kStages * stage + kPwCons * out;
   static constexpr uint32_t smem = bars + 2 * 8 * kStages + 16;
   static_assert(stage % 16 == 0 && out % 16 == 0, "TMA destinations 16-byte aligned");
@@ -286,9 +289,14 @@ __global__ void __launch_bounds__(kDecompressThreads, 1) decompress_pw_kernel(De
           store_codes<FMT, LPB, true, VARIANT == 2>(z, g2, s1, s2, out0 + sub * NB, j, cx);
         else
           store_codes<FMT, LPB, false, VARIANT == 2>(z, g2, s1, s2, out0 + sub * NB, j, cx);
+        // the (alpha, s) pairs are staged after the codes and stored by the
+        // copy engine too: no plain global stores stay in flight, so the
+        // release that publishes the header share waits for none
         uint8_t* const rc_shard = a.rc_shard + blockIdx.y * a.rc_stride;
+        float2* const pairs_out = reinterpret_cast<float2*>(rc_shard + a.scales_off) + wb0;
+        const uint32_t pstage = out0 + NB * BPT;
+        if (j == 0) sts64(pstage + 8 * sub, make_uint2(__float_as_uint(alpha), __float_as_uint(sc)));
         if (sub < wvb && j == 0) {
-          reinterpret_cast<float2*>(rc_shard + a.scales_off)[wb0 + sub] = make_float2(alpha, sc);
           part_smax = fmaxf(part_smax, sc);
           part_cnt += (sc > 1.0f) ? 1u : 0u;
         }
@@ -296,8 +304,12 @@ __global__ void __launch_bounds__(kDecompressThreads, 1) decompress_pw_kernel(De
         __syncwarp();
         if (lane == 0) {
           tma_store_1d(rc_shard + wb0 * NB, out0, static_cast<uint32_t>(wvb) * NB);
+          // whole 16-byte pairs of blocks (wb0 is even); an odd last block
+          // goes out from its lane
+          if (wvb >= 2) tma_store_1d(pairs_out, pstage, static_cast<uint32_t>(wvb & ~1) * 8);
           bulk_commit();
         }
+        if ((wvb & 1) && sub == wvb - 1 && j == 0) pairs_out[sub] = make_float2(alpha, sc);
         if (a.out == nullptr) continue;
       }
 
