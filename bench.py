@@ -89,6 +89,8 @@ KERNEL_SOURCES = {
     "compress_fwht": "compress.cu",          # CUDA-core FWHT alternative
     "decompress_reduce": "decompress_reduce.cu",
     "reduce_recompress": "decompress_reduce.cu",
+    "reduce_recompress_pw": "decompress_pw.cu",   # n = 64: the producer-warp kernel
+    "decompress_reduce_pw": "decompress_pw.cu",
 }
 COMMON_SOURCES = ("taco_device.cuh", "taco_launch.h", "taco_abi.cu")
 
