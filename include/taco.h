@@ -98,8 +98,9 @@ size_t taco_shard_scales_offset(int64_t N, int64_t h, int block);
 
 /* Bytes of device workspace that compress needs for P shards (16 per
  * shard). The workspace holds, per shard, an arrival counter and the running
- * maximum and count used to write the per-tensor header in the same launch,
- * and the counter from which the tensor-core compress hands out tiles. It must be zero-filled before
+ * maximum and count used to write the per-tensor header in the same launch;
+ * the first shard's slot also holds the counter from which the tensor-core
+ * compress hands out tiles of every shard. It must be zero-filled before
  * its first use; each call leaves it zero-filled again. Calls that share a
  * workspace must not overlap on the GPU (use one workspace per stream). */
 size_t taco_workspace_bytes(int P);
