@@ -506,10 +506,10 @@ def run_taco(args, w) -> None:
     fwht_bundles = [torch.empty((P, sb), dtype=torch.uint8, device=dev) for _ in range(R)]
 
     def compress_fwht(k):
-        st = lib.taco_compress_shards(xp[k], P, N, h, n, E, 0, fwht_bundles[k].data_ptr(), hp[k],
+        st = lib.taco_compress_shards_fwht(xp[k], P, N, h, n, E, 0, fwht_bundles[k].data_ptr(), hp[k],
                                       ws.data_ptr(), wsb, sptr)
         if st:
-            raise taco.TacoError(st, "taco_compress_shards")
+            raise taco.TacoError(st, "taco_compress_shards_fwht")
 
     for k in range(3):
         compress_fwht(k % R)
@@ -700,7 +700,7 @@ def run_taco(args, w) -> None:
                               "hbm_gbs": round(c_bytes / t_f / 1e9, 1),
                               "bf16_in_gbs": round(in_bytes / t_f / 1e9, 1),
                               "frac": round(c_bytes / t_f / 1e9 / hbm, 4),
-                              "impl": "CUDA-core FWHT (taco_compress_shards), not in the timed step"},
+                              "impl": "CUDA-core FWHT (taco_compress_shards_fwht), not in the timed step"},
             "compress_int8": {"us": round(t_ci * 1e6, 3), "alg_bytes": c_bytes,
                               "hbm_gbs": round(c_bytes / t_ci / 1e9, 1),
                               "frac": round(c_bytes / t_ci / 1e9 / hbm, 4),

@@ -9,7 +9,7 @@ AllGather would hand to the same calls.
 
   rank r:  X_r [M, h] = R row chunks of [M/R, h]
   1. compress      rank r compresses its R chunks         (taco_compress_shards_mma,
-                                                           or taco_compress_shards)
+                                                           or taco_compress_shards_fwht)
   2. ReduceScatter rank c receives chunk c of every rank  (pointers)
   3. reduce        rank c sums and recompresses them      (taco_reduce_recompress_ptrs)
   4. AllGather     every rank receives the R results      (pointers)
@@ -50,7 +50,7 @@ class EmulatedTwoShotAllReduce:
             self._expand = tb.taco_decompress_shards_int8_ptrs
             self._format = tb.FORMAT_INT8
         else:
-            self._compress = tb.taco_compress_shards_mma if compress == "mma" else tb.taco_compress_shards
+            self._compress = tb.taco_compress_shards_mma if compress == "mma" else tb.taco_compress_shards_fwht
             self._recompress = tb.taco_reduce_recompress_ptrs
             self._expand = tb.taco_decompress_shards_ptrs
             self._format = tb.FORMAT_E4M3

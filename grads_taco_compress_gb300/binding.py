@@ -38,7 +38,7 @@ assert HEADER_DTYPE.itemsize == HEADER_BYTES
 #: every symbol include/taco.h declares
 EXPORTED_SYMBOLS = (
     "taco_shard_bytes", "taco_shard_scales_offset",
-    "taco_workspace_bytes", "taco_compress", "taco_compress_shards",
+    "taco_workspace_bytes", "taco_compress", "taco_compress_shards", "taco_compress_shards_fwht",
     "taco_compress_shards_noalloc", "taco_compress_shards_mma",
     "taco_compress_shards_int8", "taco_decompress_reduce_int8",
     "taco_decompress_reduce_mma", "taco_decompress_reduce_mma_ptrs",
@@ -79,6 +79,7 @@ def _lib() -> ctypes.CDLL:
             "taco_workspace_bytes": (sz, [i32]),
             "taco_compress": (i32, [vp, i64, i64, i32, f32, i32, vp, vp, vp, sz, vp]),
             "taco_compress_shards": (i32, [vp, i32, i64, i64, i32, f32, i32, vp, vp, vp, sz, vp]),
+            "taco_compress_shards_fwht": (i32, [vp, i32, i64, i64, i32, f32, i32, vp, vp, vp, sz, vp]),
             "taco_compress_shards_noalloc": (i32, [vp, i32, i64, i64, i32, f32, i32, vp, vp, vp]),
             "taco_compress_shards_mma": (i32, [vp, i32, i64, i64, i32, f32, i32, vp, vp, vp, sz, vp]),
             "taco_compress_shards_int8": (i32, [vp, i32, i64, i64, i32, f32, i32, vp, vp, vp, sz, vp]),
@@ -191,11 +192,22 @@ def taco_compress_shards(x: torch.Tensor, block: int, target_energy: float = DEF
                          variant: int = VARIANT_DUAL, bundle: torch.Tensor | None = None,
                          headers: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
                          stream=None):
-    """Compress bf16 x [P, N, h] (cuda, contiguous) into a bundle of P shards.
+    """Compress bf16 x [P, N, h] (cuda, contiguous) into a bundle of P shards
+    (the tensor-core kernel; the CUDA-core FWHT beyond 2^31 - 256 blocks per
+    shard).
 
     Returns (bundle u8 [P, shard_bytes], headers u8 [P, 40]).
     """
     return _compress_shards("taco_compress_shards", x, block, target_energy, variant, bundle,
+                            headers, workspace, stream)
+
+
+def taco_compress_shards_fwht(x: torch.Tensor, block: int, target_energy: float = DEFAULT_TARGET_ENERGY,
+                              variant: int = VARIANT_DUAL, bundle: torch.Tensor | None = None,
+                              headers: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                              stream=None):
+    """taco_compress_shards with the whole rotation as a CUDA-core FWHT."""
+    return _compress_shards("taco_compress_shards_fwht", x, block, target_energy, variant, bundle,
                             headers, workspace, stream)
 
 

@@ -463,6 +463,23 @@ taco_status taco_compress_shards(const void* x_bf16, int P, int64_t N, int64_t h
                                  float target_energy, int variant, void* bundle_out,
                                  taco_header* headers_out, void* workspace,
                                  size_t workspace_bytes, void* stream) {
+  // the tensor-core kernel wherever its tensor copies can address the shard
+  // (faster on every measured shape), the CUDA-core FWHT beyond that
+  CompressArgs a{};
+  const taco_status st = compress_args(x_bf16, P, N, h, block, target_energy, variant, bundle_out,
+                                       headers_out, workspace, workspace_bytes, &a);
+  if (st != TACO_OK) return st;
+  if (a.nblocks > kMmaMaxBlocks)
+    return taco_compress_shards_fwht(x_bf16, P, N, h, block, target_energy, variant, bundle_out,
+                                     headers_out, workspace, workspace_bytes, stream);
+  return compress_mma_common(x_bf16, P, N, h, block, target_energy, variant, bundle_out,
+                             headers_out, workspace, workspace_bytes, stream, 0);
+}
+
+taco_status taco_compress_shards_fwht(const void* x_bf16, int P, int64_t N, int64_t h, int block,
+                                      float target_energy, int variant, void* bundle_out,
+                                      taco_header* headers_out, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
   CompressArgs a{};
   taco_status st = compress_args(x_bf16, P, N, h, block, target_energy, variant, bundle_out,
                                  headers_out, workspace, workspace_bytes, &a);

@@ -134,12 +134,30 @@ taco_status taco_compress(const void* x_bf16, int64_t N, int64_t h, int block,
  * The same for P tensors x [P, N, h] (contiguous) in one launch: shard p of
  * the bundle at `bundle_out` (P * taco_shard_bytes bytes) and header p of
  * `headers_out` [P]. 1 <= P <= TACO_MAX_SHARDS. These are the P chunks one
- * rank compresses before the ReduceScatter (TACO pt summary §2.B.3). */
+ * rank compresses before the ReduceScatter (TACO pt summary §2.B.3).
+ * taco_compress and taco_compress_shards run the tensor-core kernel of
+ * taco_compress_shards_mma (below) when a shard holds at most 2^31 - 256
+ * blocks, and the CUDA-core kernel of taco_compress_shards_fwht beyond that:
+ * the outputs meet the same parity bar either way. */
 taco_status taco_compress_shards(const void* x_bf16, int P, int64_t N, int64_t h,
                                  int block, float target_energy, int variant,
                                  void* bundle_out, taco_header* headers_out,
                                  void* workspace, size_t workspace_bytes,
                                  void* stream);
+
+/* ---- taco_compress_shards_fwht ---------------------------------------------
+ * taco_compress_shards with the whole rotation as a CUDA-core fast
+ * Walsh-Hadamard transform (log2 n butterfly levels in registers and warp
+ * shuffles; TACO pt summary §2.B.1 rotates each block by the orthonormal
+ * Hadamard matrix): same arguments, layout, headers, workspace and errors,
+ * no limit on blocks per shard beyond the shape checks. The energy is summed
+ * from x. A code can differ from the tensor-core kernel's by one E4M3 step
+ * where the fp32 rotated value differs in its last bits. */
+taco_status taco_compress_shards_fwht(const void* x_bf16, int P, int64_t N, int64_t h,
+                                      int block, float target_energy, int variant,
+                                      void* bundle_out, taco_header* headers_out,
+                                      void* workspace, size_t workspace_bytes,
+                                      void* stream);
 
 /* ---- taco_compress_shards_mma ----------------------------------------------
  * taco_compress_shards with the Hadamard rotation on the tensor cores
@@ -149,8 +167,8 @@ taco_status taco_compress_shards(const void* x_bf16, int P, int64_t N, int64_t h
  * [128 x 64] x [64 x 64] bf16 product accumulated in fp32, and the
  * log2(n/64) remaining butterfly levels run in registers. The block energy
  * is taken from the rotated block (sum t^2 = n sum x^2). The outputs meet the
- * same parity bar as taco_compress_shards; a code can differ from that
- * path's by one E4M3 step where the fp32 rotated value differs in its last
+ * same parity bar as taco_compress_shards_fwht; a code can differ from that
+ * kernel's by one E4M3 step where the fp32 rotated value differs in its last
  * bits. A block whose largest rotated magnitude lies outside [2^-40, 2^56]
  * takes a slower path: its energy is summed again from the rotated values
  * scaled by a power of two, or, for blocks of bf16 subnormals only and

@@ -64,8 +64,8 @@ def test_shard_layout(lib):
 
 
 def _compress(lib, x=A, P=1, N=4, h=256, block=128, E=4096.0, variant=0, bundle=A * 64,
-              headers=A * 128, ws=A * 256, wsb=WSB):
-    return lib.taco_compress_shards(x, P, N, h, block, E, variant, bundle, headers, ws, wsb, None)
+              headers=A * 128, ws=A * 256, wsb=WSB, entry="taco_compress_shards"):
+    return getattr(lib, entry)(x, P, N, h, block, E, variant, bundle, headers, ws, wsb, None)
 
 
 @no_gpu_only
@@ -82,9 +82,10 @@ def _compress(lib, x=A, P=1, N=4, h=256, block=128, E=4096.0, variant=0, bundle=
     (dict(ws=A * 256 + 8), ALIGN),
     (dict(x=A, bundle=A + 64), ARG),                  # input and output overlap
 ])
-def test_compress_rejects(lib, kwargs, status):
+@pytest.mark.parametrize("entry", ["taco_compress_shards", "taco_compress_shards_fwht"])
+def test_compress_rejects(lib, kwargs, status, entry):
     assert status not in (OK, CUDA)
-    assert _compress(lib, **kwargs) == status
+    assert _compress(lib, entry=entry, **kwargs) == status
 
 
 @no_gpu_only

@@ -177,7 +177,7 @@ def test_header_totals_over_the_full_grid(entry):
         headers = [o[1][None] for o in out]
         P = 1
     else:
-        fn = MMA if entry == "mma" else tb.taco_compress_shards
+        fn = MMA if entry == "mma" else tb.taco_compress_shards_fwht
         out = [fn(x, w.block, E, workspace=ws) for _ in range(2)]
         shards = [o[0] for o in out]
         headers = [o[1] for o in out]

@@ -193,7 +193,7 @@ def _compare_blocks(got_bits, want_bits, block, what, max_overflow_blocks=0, sam
 
 COMPRESS_ENTRIES = {
     "mma": (tb.taco_compress_shards_mma, O.FORMAT_E4M3),
-    "fwht": (tb.taco_compress_shards, O.FORMAT_E4M3),
+    "fwht": (tb.taco_compress_shards_fwht, O.FORMAT_E4M3),
     "int8": (tb.taco_compress_shards_int8, O.FORMAT_INT8),
 }
 

@@ -44,7 +44,7 @@ def bundle_from_arrays(codes, alpha, s, block) -> torch.Tensor:
 
 
 def gpu_compress(x_bits: np.ndarray, block: int, variant=tb.VARIANT_DUAL, target=E_STAR,
-                 entry=tb.taco_compress_shards):
+                 entry=tb.taco_compress_shards_fwht):
     """x_bits [P,N,h] -> (codes, alpha, s, headers) as numpy, via a compress entry."""
     P, N, h = x_bits.shape
     bundle, headers = entry(dev_bf16(x_bits), block, target, variant)
@@ -55,7 +55,7 @@ def gpu_compress(x_bits: np.ndarray, block: int, variant=tb.VARIANT_DUAL, target
 
 
 def check_compress_against_oracle(x_bits, block, variant=tb.VARIANT_DUAL, target=E_STAR,
-                                  entry=tb.taco_compress_shards):
+                                  entry=tb.taco_compress_shards_fwht):
     codes, alpha, s, hdr, _ = gpu_compress(x_bits, block, variant, target, entry)
     stats = []
     for p in range(x_bits.shape[0]):
@@ -132,7 +132,7 @@ def test_compress_variants_and_targets(block, variant):
 
 
 @pytest.mark.parametrize("block", [64, 128, 256])
-def test_compress_closed_form_blocks(block, entry=tb.taco_compress_shards):
+def test_compress_closed_form_blocks(block, entry=tb.taco_compress_shards_fwht):
     """Spike, constant and zero blocks: exact codes and exact round trip."""
     H = O.sylvester_hadamard(block)
     rows = []
@@ -178,18 +178,23 @@ def same_outputs(b1, h1, b2, h2, P, N, h, block):
     return same and torch.equal(h1, h2)
 
 
-def test_compress_deterministic_and_workspace_reset():
+BOTH = [tb.taco_compress_shards, tb.taco_compress_shards_fwht]   # tensor-core kernel, CUDA-core FWHT
+
+
+@pytest.mark.parametrize("entry", BOTH)
+def test_compress_deterministic_and_workspace_reset(entry):
     w = W.WORKLOADS["gpt3-6.7b-act"]
     x = dev_bf16(W.make_shards(w, N=300, P=2))
     ws = tb.new_workspace(2)
-    b1, h1 = tb.taco_compress_shards(x, w.block, workspace=ws)
-    b2, h2 = tb.taco_compress_shards(x, w.block, workspace=ws)
+    b1, h1 = entry(x, w.block, workspace=ws)
+    b2, h2 = entry(x, w.block, workspace=ws)
     torch.cuda.synchronize()
     assert same_outputs(b1, h1, b2, h2, 2, 300, w.h, w.block)
     assert int(ws.count_nonzero()) == 0      # counters and running totals
 
 
-def test_compress_does_not_write_outside_its_buffers():
+@pytest.mark.parametrize("entry", BOTH)
+def test_compress_does_not_write_outside_its_buffers(entry):
     w = W.WORKLOADS["gpt3-6.7b-grad"]
     N = 33
     x = dev_bf16(W.make_shards(w, N=N, P=2))
@@ -199,15 +204,16 @@ def test_compress_does_not_write_outside_its_buffers():
     bundle = big[guard: guard + 2 * sb].view(2, sb)
     hbig = torch.full((2 * 40 + 2 * 64,), 0xA5, dtype=torch.uint8, device="cuda")
     headers = hbig[64: 64 + 80].view(2, 40)
-    tb.taco_compress_shards(x, w.block, bundle=bundle, headers=headers)
+    entry(x, w.block, bundle=bundle, headers=headers)
     torch.cuda.synchronize()
     assert bool((big[:guard] == 0xA5).all()) and bool((big[-guard:] == 0xA5).all())
     assert bool((hbig[:64] == 0xA5).all()) and bool((hbig[-64:] == 0xA5).all())
 
 
-def test_compress_empty_tensor():
+@pytest.mark.parametrize("entry", BOTH)
+def test_compress_empty_tensor(entry):
     x = torch.empty((2, 0, 256), dtype=torch.bfloat16, device="cuda")
-    bundle, headers = tb.taco_compress_shards(x, 128)
+    bundle, headers = entry(x, 128)
     hdr = tb.parse_headers(headers)
     assert list(hdr["s_max"]) == [0.0, 0.0] and list(hdr["n_clamped"]) == [0, 0]
     assert list(hdr["N"]) == [0, 0]
