@@ -33,6 +33,8 @@
 //              rotation, computes alpha, s and the codes, writes the codes
 //              into a 64-byte-swizzled staging buffer that one thread stores
 //              with 3-D TMA tensor stores, and stores its (alpha, s) pair;
+//              each warp then folds its rows' largest s and count of s > 1
+//              into the CTA's totals for the tile's shard (shared memory);
 //   warp 10    tile scheduler (below).
 // Tile schedule: the CTAs of shard y (gridDim.x of them, blockIdx.y == y)
 // take 3/4 of the per-CTA share of that shard's tiles round-robin (tile
