@@ -46,6 +46,19 @@ def _decompress_rows(job):
     return hi - lo
 
 
+def _recompress_rows(job):
+    from oracle import taco_oracle as O
+    c_spec, a_spec, s_spec, rc_spec, ra_spec, rs_spec, lo, hi, block, target, variant, fmt = job
+    handles = [_attach(sp) for sp in (c_spec, a_spec, s_spec, rc_spec, ra_spec, rs_spec)]
+    (_, codes), (_, alpha), (_, s), (_, rc), (_, ra), (_, rs) = handles
+    c, a, sc, _ = O.reduce_recompress(np.ascontiguousarray(codes[:, lo:hi]), np.ascontiguousarray(alpha[:, lo:hi]),
+                                      np.ascontiguousarray(s[:, lo:hi]), block, target, variant, fmt)
+    rc[lo:hi], ra[lo:hi], rs[lo:hi] = c, a, sc
+    for shm, _ in handles:
+        shm.close()
+    return hi - lo
+
+
 class _Shared:
     """Numpy arrays in shared memory, released together."""
 
@@ -69,7 +82,7 @@ class _Shared:
 
 
 class OracleRows:
-    """oracle.compress / oracle.decompress_reduce over all rows, split across workers."""
+    """oracle.compress / decompress_reduce / reduce_recompress over all rows, split across workers."""
 
     def __init__(self, workers: int | None = None):
         self.workers = max(1, workers or os.cpu_count() or 1)
@@ -119,6 +132,25 @@ class OracleRows:
             jobs = [(cs, as_, ss, os_, lo, hi, block, fmt) for lo, hi in self._ranges(N)]
             assert sum(self.pool.map(_decompress_rows, jobs, chunksize=1)) == N
             return out.copy()
+        finally:
+            sh.close()
+
+    def reduce_recompress(self, codes, alpha, s, block, target, variant=0, fmt=0):
+        """Oracle reduce-recompress of P shards -> (codes u8 [N,h], alpha f32 [N,K], s f32 [N,K])."""
+        P, N, h = codes.shape
+        K = h // block
+        sh = _Shared()
+        try:
+            _, cs = sh.new((P, N, h), np.uint8, codes)
+            _, as_ = sh.new((P, N, K), np.float32, alpha)
+            _, ss = sh.new((P, N, K), np.float32, s)
+            rc, rcs = sh.new((N, h), np.uint8)
+            ra, ras = sh.new((N, K), np.float32)
+            rs, rss = sh.new((N, K), np.float32)
+            jobs = [(cs, as_, ss, rcs, ras, rss, lo, hi, block, float(target), variant, fmt)
+                    for lo, hi in self._ranges(N)]
+            assert sum(self.pool.map(_recompress_rows, jobs, chunksize=1)) == N
+            return rc.copy(), ra.copy(), rs.copy()
         finally:
             sh.close()
 

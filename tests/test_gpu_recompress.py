@@ -99,18 +99,21 @@ def test_recompress_ptrs_equals_bundle():
     assert np.array_equal(a2[0].cpu().numpy(), ra) and np.array_equal(s2[0].cpu().numpy(), rs)
 
 
-@pytest.mark.parametrize("name", ["gpt2-1.5b-act", "gpt3-6.7b-act", "qwen-7b-long"])
-def test_recompress_full_size_sampled(name):
+@pytest.mark.parametrize("name", ["tiny-512x1024", "gpt2-1.5b-act", "gpt3-6.7b-act", "gpt3-6.7b-grad",
+                                  "qwen-7b-long"])
+def test_recompress_full_size_every_element(name, oracle_rows):
+    """Every code, alpha and s of the full-size reduce-recompress of a
+    generated bundle against the oracle (run unchanged over row ranges in
+    worker processes), and the header against the GPU's own s."""
     w = W.WORKLOADS[name]
     codes, alpha, s = W.make_random_bundle(w.N, w.h, w.block, w.P, seed=6)
     rc, ra, rs, hdr, _, _ = gpu_recompress(codes, alpha, s, w.block)
-    rows = np.array(sorted(set([0, 1, w.N // 2, w.N - 1]) |
-                           set(np.random.default_rng(3).choice(w.N, 24, replace=False).tolist())))
-    oc, oa, os_, _ = O.reduce_recompress(codes[:, rows], alpha[:, rows], s[:, rows], w.block, E_STAR)
-    parity.compare_codes(rc[rows], oc, f"{name} recompressed codes")
-    parity.compare_scales(ra[rows], oa, f"{name} alpha")
-    parity.compare_scales(rs[rows], os_, f"{name} s")
+    oc, oa, os_ = oracle_rows.reduce_recompress(codes, alpha, s, w.block, E_STAR)
+    stats = parity.compare_codes(rc, oc, f"{name} recompressed codes")
+    parity.compare_scales(ra, oa, f"{name} alpha")
+    parity.compare_scales(rs, os_, f"{name} s")
     assert hdr["s_max"] == rs.max() and hdr["n_clamped"] == np.count_nonzero(rs > 1.0)
+    print(f"\nPARITY {name} reduce-recompress: {stats}")
 
 
 @pytest.mark.parametrize("Y,P,block,fmt", [(4, 4, 64, tb.FORMAT_E4M3), (2, 8, 128, tb.FORMAT_E4M3),
