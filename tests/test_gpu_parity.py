@@ -1,8 +1,9 @@
 """CUDA path against the CPU oracle, through the C ABI (libtaco).
 
 Small cases run the oracle on every element; full-size cases run the exact
-launches the benchmark times and check sampled rows one by one against the
-oracle, plus properties that hold at any size.
+launches the benchmark times and check every element against the oracle
+(run unchanged over row ranges in worker processes), plus properties that
+hold at any size.
 """
 
 from __future__ import annotations
