@@ -31,6 +31,33 @@ def _bits(v: np.ndarray) -> np.ndarray:
     return W.f32_to_bf16_bits(np.clip(v, -3.3e38, 3.3e38).astype(np.float32))
 
 
+def _extreme_cases(rng, block: int, aligned: bool = False):
+    """(name, values) of the extreme blocks, drawn from `rng`."""
+    cases = []
+    for m in MAGNITUDES:
+        if aligned and m > 1e38:
+            continue
+        cases.append((f"normal x {m:g}", rng.standard_normal(block) * m))
+        # magnitudes in [m, 2m) (values above 3.3e38 clipped): a block of
+        # one magnitude with random signs would rotate onto exact E4M3
+        # midpoints, where a difference of one fp32 ulp decides the tie
+        cases.append((f"[1,2) x {m:g}", m * (1.0 + rng.random(block)) * np.sign(rng.standard_normal(block))))
+    spike = np.zeros(block)
+    spike[3] = 2.0 ** -133                                          # the smallest bf16
+    cases.append(("spike 2^-133", spike))
+    spike = np.zeros(block)
+    spike[block - 1] = -(2.0 ** -126)
+    cases.append(("spike -2^-126", spike))
+    mixed = rng.laplace(0.0, 0.02, size=block)
+    mixed[7] = 1.0e38 if aligned else 3.0e38                        # one huge element
+    cases.append(("laplace + one huge element", mixed))
+    sub = rng.standard_normal(block) * 1e-30
+    sub[::2] = rng.standard_normal(block // 2) * 1e-39              # subnormals beside 1e-30
+    cases.append(("1e-30 with subnormals", sub))
+    cases.append(("zero", np.zeros(block)))
+    return cases
+
+
 def extreme_tensor(block: int, P: int = 2, N: int = 20, K: int = 4, seed: int = 0, labels: bool = False,
                    aligned: bool = False):
     """bf16 bits [P, N, K * block]: ordinary blocks with extreme ones among them
@@ -45,28 +72,7 @@ def extreme_tensor(block: int, P: int = 2, N: int = 20, K: int = 4, seed: int = 
     names = np.full((P, N, K), "ordinary", dtype=object)
     for p in range(P):
         rows = [r for r in range(N) if r % P == (0 if aligned else p)]
-        cases = []
-        for m in MAGNITUDES:
-            if aligned and m > 1e38:
-                continue
-            cases.append((f"normal x {m:g}", rng.standard_normal(block) * m))
-            # magnitudes in [m, 2m) (values above 3.3e38 clipped): a block of
-            # one magnitude with random signs would rotate onto exact E4M3
-            # midpoints, where a difference of one fp32 ulp decides the tie
-            cases.append((f"[1,2) x {m:g}", m * (1.0 + rng.random(block)) * np.sign(rng.standard_normal(block))))
-        spike = np.zeros(block)
-        spike[3] = 2.0 ** -133                                          # the smallest bf16
-        cases.append(("spike 2^-133", spike))
-        spike = np.zeros(block)
-        spike[block - 1] = -(2.0 ** -126)
-        cases.append(("spike -2^-126", spike))
-        mixed = rng.laplace(0.0, 0.02, size=block)
-        mixed[7] = 1.0e38 if aligned else 3.0e38                        # one huge element
-        cases.append(("laplace + one huge element", mixed))
-        sub = rng.standard_normal(block) * 1e-30
-        sub[::2] = rng.standard_normal(block // 2) * 1e-39              # subnormals beside 1e-30
-        cases.append(("1e-30 with subnormals", sub))
-        cases.append(("zero", np.zeros(block)))
+        cases = _extreme_cases(rng, block, aligned)
         for i, (name, c) in enumerate(cases):
             r, k = rows[i % len(rows)], (i // len(rows)) % K
             v[p, r, k] = c
@@ -223,6 +229,38 @@ def test_compress_extreme_blocks(block, variant, entry):
         got = out.view(torch.int16).cpu().numpy().view(np.uint16)
         _compare_blocks(got, ref, block, f"{entry} n={block} v={variant} tensor-core decompress-reduce",
                         2 * P, same)
+
+
+@pytest.mark.parametrize("block", [64, 256])
+@pytest.mark.parametrize("entry", ["mma", "int8"])
+def test_compress_extreme_blocks_in_the_shared_tile_pool(block, entry):
+    """Four shards of [2048, 16 n], large enough that about a quarter of each
+    shard's tiles go to the pool that every CTA of the tensor-core compress
+    claims from, so a CTA compresses tiles of other shards than its own.
+    Every 128-block tile holds one extreme block (the cases above in turn),
+    so blocks that take the rescale and exact paths (the latter re-reads the
+    block from its own shard's x) sit in pool tiles too. Codes, alpha and s
+    against the oracle as for the small tensors."""
+    fn, fmt = COMPRESS_ENTRIES[entry]
+    P, N, K = 4, 2048, 16
+    rng = np.random.default_rng(77 + block)
+    v = rng.laplace(0.0, 0.02, size=(P, N * K, block))
+    names = np.full((P, N * K), "ordinary", dtype=object)
+    cases = _extreme_cases(rng, block)
+    for p in range(P):
+        for t in range(N * K // 128):
+            name, c = cases[(t + p) % len(cases)]
+            b = t * 128 + int(rng.integers(0, 128))
+            v[p, b] = c
+            names[p, b] = name
+    x = _bits(v.reshape(P, N, K * block))
+    h = K * block
+    xd = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).cuda()
+    bundle, _ = fn(xd, block, E_STAR, tb.VARIANT_DUAL)
+    codes, alpha, s = (t.cpu().numpy() for t in tb.shard_views(bundle, P, N, h, block))
+    want, ratio = _oracle(x, block, tb.VARIANT_DUAL, fmt, with_ratio=True)
+    _compare_compress((codes, alpha, s), want, fmt, f"{entry} n={block} pooled", ratio,
+                      names.reshape(P, N, K), block)
 
 
 @pytest.mark.parametrize("target", [E_STAR, 1e-30, 2.0 ** 100])
