@@ -96,7 +96,7 @@ struct Smem {
   static constexpr uint32_t codes = hmat + kHBytes;                 // [group][chunk] atoms
   static constexpr uint32_t bars = codes + NG * NC * kCodeAtomBytes;
   // barriers: full[kStages], empty[kStages], tfull[NG], tempty[NG], info[NG],
-  // cfull[kClaims], cempty[kClaims], mma_done
+  // cfull[kClaims], cempty[kClaims], mma_done, hdr_ready
   static constexpr uint32_t full = bars;
   static constexpr uint32_t empty = full + 8 * kStages;
   static constexpr uint32_t tfull = empty + 8 * kStages;
@@ -105,13 +105,15 @@ struct Smem {
   static constexpr uint32_t cfull = info + 8 * NG;
   static constexpr uint32_t cempty = cfull + 8 * kClaims;
   static constexpr uint32_t mma_done = cempty + 8 * kClaims;
-  static constexpr uint32_t tmem_slot = mma_done + 8;
+  static constexpr uint32_t hdr_ready = mma_done + 8;              // every epilogue warp's share is in
+  static constexpr uint32_t tmem_slot = hdr_ready + 8;
   static constexpr uint32_t abort_flag = tmem_slot + 4;
   static constexpr uint32_t tile_ring = abort_flag + 4;   // int[kRing]: tile of the CTA's tile k
   static constexpr uint32_t tile_of = tile_ring + 4 * kRing;      // int[NG]: tile of accumulator g
   static constexpr uint32_t claim = tile_of + 4 * NG;             // int[kClaims]: claimed tiles
+  static constexpr uint32_t n_tiles = claim + 4 * kClaims;         // int: the CTA's tiles, -1 until known
   // u32[TACO_MAX_SHARDS] each: the CTA's largest s bits and count of s > 1 per shard
-  static constexpr uint32_t hdr_max = claim + 4 * kClaims;
+  static constexpr uint32_t hdr_max = n_tiles + 4;
   static constexpr uint32_t hdr_cnt = hdr_max + 4 * TACO_MAX_SHARDS;
   static constexpr uint32_t end = hdr_cnt + 4 * TACO_MAX_SHARDS;
   static constexpr uint32_t bytes = end + 1024;                     // + alignment slack
@@ -354,6 +356,7 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
   volatile int* tile_ring = reinterpret_cast<volatile int*>(sbase + S::tile_ring);
   volatile int* tile_of = reinterpret_cast<volatile int*>(sbase + S::tile_of);
   volatile int* claim = reinterpret_cast<volatile int*>(sbase + S::claim);
+  volatile int* n_tiles = reinterpret_cast<volatile int*>(sbase + S::n_tiles);
   unsigned int* const hdr_max = reinterpret_cast<unsigned int*>(sbase + S::hdr_max);
   unsigned int* const hdr_cnt = reinterpret_cast<unsigned int*>(sbase + S::hdr_cnt);
 
@@ -384,6 +387,8 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
       mbar_init(base + S::cempty + 8 * c, 1);
     }
     mbar_init(base + S::mma_done, 1);
+    mbar_init(base + S::hdr_ready, 4 * NG);   // one arrival per epilogue warp
+    *n_tiles = -1;
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -436,6 +441,7 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
           if (!wait_here(base + S::cfull + 8 * c, (j / kClaims) & 1u, abort_flag)) break;
           tile = claim[c];
           mbar_arrive(base + S::cempty + 8 * c);
+          if (tile < 0) *n_tiles = k;   // the CTA's tile count, for the epilogue's last tiles
         }
         tile_ring[k % kRing] = tile;   // published by the arrival on the first atom's barrier
         for (int c = 0; c < (tile < 0 ? 1 : NC); ++c, ++i) {
@@ -532,6 +538,18 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
       }
     }
     __syncwarp();
+    // The per-tensor headers, while the epilogue finishes its last codes:
+    // once every epilogue warp has folded in its last tile (hdr_ready), lane
+    // p brings the CTA's share of shard p and counts the CTA's arrival
+    // (every CTA arrives on every shard, since a CTA may have compressed
+    // tiles of any shard; the last of the G * P arrivals writes the header).
+    // After a wait that gave up the arrivals still happen, so that the
+    // workspace is reset.
+    wait_here(base + S::hdr_ready, 0, abort_flag);
+    if (lane < P)
+      arrive_header(__uint_as_float(hdr_max[lane]), hdr_cnt[lane], G * P,
+                    a.workspace + lane * kWorkspaceShardStride, a.headers + lane, a.N, a.h, NB, VARIANT,
+                    a.target_energy, QMAX);
   } else {
     // -------------------------------------------------------- epilogue ----
     const int g = (warp - 2) >> 2;               // group: accumulator and tiles k % NG == g
@@ -541,6 +559,18 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
     const uint32_t tacc = tmem + (static_cast<uint32_t>(quad * 32) << 16) + g * NB;
     const uint32_t staging = base + S::codes + g * NC * kCodeAtomBytes;
     if (leader) prefetch_map(&map_codes);
+    // the warp's share of its tile's shard header: the largest s (bits of a
+    // positive float order like its value; fmaxf drops NaN) and the count
+    // of s > 1, into the CTA's per-shard totals
+    auto fold_header = [&](int ts, bool valid, float sc) {
+      const uint32_t wmax = __reduce_max_sync(kFullMask, valid ? __float_as_uint(fmaxf(sc, 0.0f)) : 0u);
+      const uint32_t wcnt = __popc(__ballot_sync(kFullMask, valid && sc > 1.0f));
+      if (lane == 0) {
+        atomicMax(hdr_max + ts, wmax);
+        atomicAdd(hdr_cnt + ts, wcnt);
+      }
+    };
+    bool shared_all = false;   // the warp has arrived on hdr_ready
 
     for (int k = g;; k += NG) {
       const uint32_t use = static_cast<uint32_t>(k / NG);
@@ -617,6 +647,17 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
       // rescaled block of tiny t: ABSMAX's 448 / max |t|, or a tiny E* in
       // STATIC) the warp takes its codes from 2^-k t with the factor times
       // 2^k instead, which stays finite; lanes with k = 0 are unchanged.
+      // On the group's last tile the warp's share goes out before the codes,
+      // so that the header arrivals overlap them, unless a row of the warp
+      // takes the exact path (its alpha and s come after the codes).
+      const int nt = __shfl_sync(kFullMask, *n_tiles, 0);
+      bool folded = false;
+      if (!shared_all && nt >= 0 && k + NG >= nt && !__any_sync(kFullMask, exact && valid)) {
+        fold_header(ts, valid, sc);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(base + S::hdr_ready);
+        folded = shared_all = true;
+      }
       const float gplain = __fdividef(cscale, sc);
       const bool scaled = __any_sync(kFullMask, rescale && !(gplain <= 0x1.fffffep127f));
       const float gsc = scaled ? __fdividef(ldexpf(cscale, kr), sc) : gplain;
@@ -660,30 +701,18 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
       if (valid)
         reinterpret_cast<float2*>(a.bundle + static_cast<size_t>(ts) * a.shard_bytes + a.scales_off)[b] =
             make_float2(alpha, sc);
-      // the warp's share of its shard's header: the largest s (bits of a
-      // positive float order like its value; fmaxf drops NaN) and the count
-      // of s > 1
-      const uint32_t wmax = __reduce_max_sync(kFullMask, valid ? __float_as_uint(fmaxf(sc, 0.0f)) : 0u);
-      const uint32_t wcnt = __popc(__ballot_sync(kFullMask, valid && sc > 1.0f));
-      if (lane == 0) {
-        atomicMax(hdr_max + ts, wmax);
-        atomicAdd(hdr_cnt + ts, wcnt);
-      }
+      if (!folded) fold_header(ts, valid, sc);
+    }
+    // a warp whose last tile did not go out early (or that had none) arrives here
+    if (!shared_all) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(base + S::hdr_ready);
     }
   }
 
-  // ---- tear-down: the per-tensor header (its arrival count overlaps the
-  // last stores), then free the tensor memory once every store has read
-  // the staging buffer (the kernel's end makes the stored codes visible) ----
-  // every CTA arrives on every shard's header (a CTA may have compressed
-  // tiles of any shard), so a shard's header is written once all G * P CTAs
-  // have brought their share
+  // ---- tear-down: free the tensor memory once every store has read the
+  // staging buffer (the kernel's end makes the stored codes visible) ----
   tc_fence_before();
-  __syncthreads();
-  if (threadIdx.x < P)
-    arrive_header(__uint_as_float(hdr_max[threadIdx.x]), hdr_cnt[threadIdx.x], G * P,
-                  a.workspace + threadIdx.x * kWorkspaceShardStride, a.headers + threadIdx.x, a.N, a.h, NB,
-                  VARIANT, a.target_energy, QMAX);
   if (warp >= 2 && warp < kSchedWarp && (warp - 2) % 4 == 0 && lane == 0) bulk_wait_read<0>();
   __syncthreads();
   if (warp == 1) {
