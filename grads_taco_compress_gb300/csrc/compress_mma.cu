@@ -73,6 +73,45 @@ namespace {
 
 __device__ unsigned int g_compress_mma_fault;
 
+// The per-tensor header of this kernel. Workspace of a shard (16 bytes,
+// zero between calls):
+//   [u64: arrivals << 48 | count of s > 1][u32 running max-s bits][u32 tile claims]
+// A CTA's largest s is folded into the running maximum (an atomic max on
+// the float's bits, which order like the values because every s is positive
+// and fmaxf drops NaN), and a release fence follows it. The count of s > 1
+// rides on the CTA's arrival: one 64-bit add that counts the CTA and adds
+// the count, so the count needs no ordering of its own, and the fence before
+// it makes that add a release for the maximum; the add is an acquire. The
+// arrival that completes the count takes the maximum with one exchange that
+// zeroes it, writes the header and resets the counter and the tile word.
+constexpr int kArrivalShift = 48;   // arrivals above, the count of s > 1 below
+
+__device__ __forceinline__ void fold_max(float m, uint8_t* ws_shard) {
+  if (m > 0.0f)
+    asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(ws_shard + 8), "r"(__float_as_uint(m))
+                 : "memory");
+}
+__device__ __forceinline__ void release_fence() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+// after a release fence of this thread that follows every fold of the CTA
+__device__ __forceinline__ void arrive(uint32_t n, uint32_t arrivals, uint8_t* ws_shard, taco_header* hd,
+                                       int64_t N, int64_t h, int block, int variant, float target_energy,
+                                       float q_max) {
+  unsigned long long old;
+  asm volatile("atom.add.acquire.gpu.global.u64 %0, [%1], %2;"
+               : "=l"(old)
+               : "l"(ws_shard), "l"((1ull << kArrivalShift) + n)
+               : "memory");
+  if ((old >> kArrivalShift) != arrivals - 1u) return;
+  uint32_t m;
+  asm volatile("atom.exch.relaxed.gpu.global.b32 %0, [%1], 0;" : "=r"(m) : "l"(ws_shard + 8) : "memory");
+  write_header(hd, N, h, block, variant, target_energy, q_max, __uint_as_float(m),
+               static_cast<uint32_t>((old & ((1ull << kArrivalShift) - 1)) + n));
+  // leaves the workspace zero-filled for the next call: the counter and the
+  // tile word (every claim of the launch came before the arrivals)
+  *reinterpret_cast<volatile unsigned long long*>(ws_shard) = 0ull;
+  *reinterpret_cast<volatile uint32_t*>(ws_shard + 12) = 0u;
+}
+
 constexpr int kRows = 128;                    // blocks per tile (the MMA's M)
 constexpr int kRing = 8;                      // tile indices in flight, producer -> MMA lane
 constexpr int kClaims = 2;                    // claimed tiles in flight, scheduler -> producer
@@ -523,7 +562,7 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
     if (lane == 0) {
       // one pool for the whole launch: shard 0's tile word; item j of the
       // pool is tile first + j / P of shard j % P
-      unsigned int* next = reinterpret_cast<unsigned int*>(a.workspace) + 1;
+      unsigned int* next = reinterpret_cast<unsigned int*>(a.workspace) + 3;
       const int64_t first = static_cast<int64_t>(n_static) * G;   // first tile of each shard's pool
       const int64_t pool = (ntiles - first) * P;
       for (uint32_t j = 0;; ++j) {
@@ -538,18 +577,32 @@ compress_mma_kernel(const __grid_constant__ CUtensorMap map_x,
       }
     }
     __syncwarp();
-    // The per-tensor headers, while the epilogue finishes its last codes:
-    // once every epilogue warp has folded in its last tile (hdr_ready), lane
-    // p brings the CTA's share of shard p and counts the CTA's arrival
-    // (every CTA arrives on every shard, since a CTA may have compressed
-    // tiles of any shard; the last of the G * P arrivals writes the header).
-    // After a wait that gave up the arrivals still happen, so that the
-    // workspace is reset.
+    // The per-tensor headers; lane p handles shard p. Every CTA arrives on
+    // every shard (a CTA may have compressed tiles of any shard), and the
+    // last of the G * P arrivals writes the header. With the pool dry, the
+    // largest s the CTA has seen so far goes into the shard's running
+    // maximum and a release fence follows, while the last tiles are still on
+    // their way. Once every epilogue warp has folded in its last tile
+    // (hdr_ready), the arrival carries the count of s > 1; a second fold and
+    // fence come before it only if the CTA's largest s grew meanwhile. After
+    // a wait that gave up the arrivals still happen, so that the workspace
+    // is reset.
+    uint8_t* const ws_p = a.workspace + lane * kWorkspaceShardStride;
+    float m_early = 0.0f;
+    if (lane < P) {
+      m_early = __uint_as_float(reinterpret_cast<volatile unsigned int*>(hdr_max)[lane]);
+      fold_max(m_early, ws_p);
+      release_fence();
+    }
     wait_here(base + S::hdr_ready, 0, abort_flag);
-    if (lane < P)
-      arrive_header(__uint_as_float(hdr_max[lane]), hdr_cnt[lane], G * P,
-                    a.workspace + lane * kWorkspaceShardStride, a.headers + lane, a.N, a.h, NB, VARIANT,
-                    a.target_energy, QMAX);
+    if (lane < P) {
+      const float m = __uint_as_float(hdr_max[lane]);
+      if (m > m_early) {
+        fold_max(m, ws_p);
+        release_fence();
+      }
+      arrive(hdr_cnt[lane], G * P, ws_p, a.headers + lane, a.N, a.h, NB, VARIANT, a.target_energy, QMAX);
+    }
   } else {
     // -------------------------------------------------------- epilogue ----
     const int g = (warp - 2) >> 2;               // group: accumulator and tiles k % NG == g

@@ -453,7 +453,21 @@ __device__ __forceinline__ float block_max(float v) {
 // completes the count takes both totals with one 64-bit exchange that also
 // zeroes them, writes the header and resets the counter: two dependent round
 // trips to L2 after the last CTA's work.
-// Workspace of a shard (16 bytes): [u32 arrivals | u32 tile claims | u32 max-s bits | u32 count].
+// Workspace of a shard (16 bytes, zero between calls):
+//   [u32 arrivals | u32 tile claims | u32 max-s bits | u32 count]
+// (the tensor-core compress lays its own out differently: compress_mma.cu).
+__device__ __forceinline__ void write_header(taco_header* hd, int64_t N, int64_t h, int block, int variant,
+                                             float target_energy, float q_max, float s_max,
+                                             uint32_t n_clamped) {
+  hd->N = N;
+  hd->h = h;
+  hd->block = block;
+  hd->variant = variant;
+  hd->target_energy = target_energy;
+  hd->q_max = q_max;
+  hd->s_max = s_max;
+  hd->n_clamped = n_clamped;
+}
 __device__ __forceinline__ void arrive_header(float m, uint32_t n, uint32_t arrivals, uint8_t* ws_shard,
                                               taco_header* hd, int64_t N, int64_t h, int block,
                                               int variant, float target_energy, float q_max) {
@@ -470,17 +484,9 @@ __device__ __forceinline__ void arrive_header(float m, uint32_t n, uint32_t arri
   if (arrived != arrivals - 1u) return;
   unsigned long long t;
   asm volatile("atom.exch.relaxed.gpu.global.b64 %0, [%1], 0;" : "=l"(t) : "l"(totals) : "memory");
-  hd->N = N;
-  hd->h = h;
-  hd->block = block;
-  hd->variant = variant;
-  hd->target_energy = target_energy;
-  hd->q_max = q_max;
-  hd->s_max = __uint_as_float(static_cast<uint32_t>(t));
-  hd->n_clamped = static_cast<uint32_t>(t >> 32);
+  write_header(hd, N, h, block, variant, target_energy, q_max, __uint_as_float(static_cast<uint32_t>(t)),
+               static_cast<uint32_t>(t >> 32));
   // with the exchange, leaves the workspace zero-filled for the next call
-  // (the arrival counter and the word after it, the tile-claim counter of
-  // the tensor-core compress, whose claims all came before the arrivals)
   *reinterpret_cast<unsigned long long*>(ws_shard) = 0ull;
 }
 

@@ -34,8 +34,9 @@ constexpr int64_t kMmaMaxBlocks = (int64_t{1} << 31) - 256;
 
 // Largest grid row (CTAs per shard) of any launch.
 constexpr int kMaxCtasPerShard = 2048;
-// Workspace of one shard: arrival counter, tile-claim counter (tensor-core
-// compress), running max-s bits and running count (16 bytes).
+// Workspace of one shard: 16 bytes, zero between calls. Each kernel lays out
+// its header counters there (taco_device.cuh, compress_mma.cu); the first
+// shard's slot also holds the tensor-core compress's launch-wide tile pool.
 constexpr size_t kWorkspaceShardStride = 16;
 
 struct CompressArgs {
