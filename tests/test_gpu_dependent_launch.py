@@ -71,3 +71,35 @@ def test_inputs_written_by_the_previous_kernel(block, oracle_rows):
         parity.compare_codes(rcodes[0], qc, f"round {i} recompressed codes")
         parity.compare_scales(ralpha[0], qa, f"round {i} recompressed alpha")
         parity.compare_scales(rs[0], qs, f"round {i} recompressed s")
+
+
+def test_concurrent_compress_calls_on_two_streams(oracle_rows):
+    """Two compress calls of different tensors on two streams, each with its
+    own workspace, queued so that they overlap on the GPU several times over:
+    the tile pool's counter and the header totals live in each call's own
+    workspace, so every output must match the oracle of its own input."""
+    P, N, h, block = 4, 1024, 2048, 128
+    rng = np.random.default_rng(31)
+    xs = [W.f32_to_bf16_bits(rng.laplace(0, 0.03 * (i + 1), size=(P, N, h)).astype(np.float32)) for i in range(2)]
+    xd = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).cuda() for x in xs]
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    wss = [tb.new_workspace(P) for _ in range(2)]
+    bundles = [torch.empty((P, tb.shard_bytes(N, h, block)), dtype=torch.uint8, device="cuda") for _ in range(2)]
+    headers = [torch.empty((P, tb.HEADER_BYTES), dtype=torch.uint8, device="cuda") for _ in range(2)]
+    torch.cuda.synchronize()
+    for _ in range(5):
+        for i in range(2):
+            with torch.cuda.stream(streams[i]):
+                tb.taco_compress_shards(xd[i], block, bundle=bundles[i], headers=headers[i], workspace=wss[i],
+                                        stream=streams[i])
+    torch.cuda.synchronize()
+    for i in range(2):
+        assert int(wss[i].count_nonzero()) == 0
+        codes, alpha, s = (t.cpu().numpy() for t in tb.shard_views(bundles[i], P, N, h, block))
+        oc, oa, os_ = oracle_rows.compress(xs[i], block, E_STAR)
+        hdr = tb.parse_headers(headers[i])
+        for p in range(P):
+            parity.compare_codes(codes[p], oc[p], f"call {i} codes[{p}]")
+            parity.compare_scales(alpha[p], oa[p], f"call {i} alpha[{p}]")
+            parity.compare_scales(s[p], os_[p], f"call {i} s[{p}]")
+            assert hdr[p]["s_max"] == s[p].max() and hdr[p]["n_clamped"] == np.count_nonzero(s[p] > 1.0)
