@@ -120,7 +120,7 @@ size_t taco_workspace_bytes(int P);
  *                  API; this argument is this library's addition to the plain
  *                  compress(x, block, E*) signature, because the per-tensor
  *                  header is written in the same launch (the CTA that
- *                  finishes last reads counters that every CTA updates) and
+ *                  arrives last reads counters that every CTA updates) and
  *                  the library itself never allocates.
  * Every finite bf16 input is accepted, subnormals and values near the bf16
  * maximum included; no finite input gives a NaN code.
