@@ -419,15 +419,18 @@ const void* decompress_kernel_ptr(int block, int fmt, bool claim) {
 }
 
 namespace {
-template <int NB, int FMT>
+template <int NB, int FMT, bool CLAIM>
 void (*recompress_fn_fmt(int variant))(DecompressArgs) {
-  return variant == 0   ? decompress_reduce_kernel<NB, 1, 0, FMT>
-         : variant == 1 ? decompress_reduce_kernel<NB, 1, 1, FMT>
-                        : decompress_reduce_kernel<NB, 1, 2, FMT>;
+  return variant == 0   ? decompress_reduce_kernel<NB, 1, 0, FMT, CLAIM>
+         : variant == 1 ? decompress_reduce_kernel<NB, 1, 1, FMT, CLAIM>
+                        : decompress_reduce_kernel<NB, 1, 2, FMT, CLAIM>;
 }
+// claim: the warps of a CTA claim its tiles in order (E4M3 codes only)
 template <int NB>
-void (*recompress_fn(int variant, int fmt))(DecompressArgs) {
-  return fmt == 0 ? recompress_fn_fmt<NB, 0>(variant) : recompress_fn_fmt<NB, 1>(variant);
+void (*recompress_fn(int variant, int fmt, bool claim = false))(DecompressArgs) {
+  return fmt != 0 ? recompress_fn_fmt<NB, 1, false>(variant)
+         : claim  ? recompress_fn_fmt<NB, 0, true>(variant)
+                  : recompress_fn_fmt<NB, 0, false>(variant);
 }
 template <int NB>
 void (*gather_fn(int fmt))(DecompressArgs) {
@@ -435,11 +438,11 @@ void (*gather_fn(int fmt))(DecompressArgs) {
 }
 }  // namespace
 
-const void* recompress_kernel_ptr(int block, int variant, int fmt) {
+const void* recompress_kernel_ptr(int block, int variant, int fmt, bool claim) {
   switch (block) {
-    case 64: return reinterpret_cast<const void*>(recompress_fn<64>(variant, fmt));
-    case 128: return reinterpret_cast<const void*>(recompress_fn<128>(variant, fmt));
-    default: return reinterpret_cast<const void*>(recompress_fn<256>(variant, fmt));
+    case 64: return reinterpret_cast<const void*>(recompress_fn<64>(variant, fmt, claim));
+    case 128: return reinterpret_cast<const void*>(recompress_fn<128>(variant, fmt, claim));
+    default: return reinterpret_cast<const void*>(recompress_fn<256>(variant, fmt, claim));
   }
 }
 
@@ -506,9 +509,16 @@ cudaError_t launch_reduce_recompress(const DecompressArgs& a, int block, int var
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  void (*kern)(DecompressArgs) = block == 64    ? recompress_fn<64>(variant, fmt)
-                                 : block == 128 ? recompress_fn<128>(variant, fmt)
-                                                : recompress_fn<256>(variant, fmt);
+  // With E4M3 codes and at least kClaimRounds full grid-stride rounds per
+  // warp, the warps claim their CTA's tiles in order, as the
+  // decompress-reduce does: measured gpt3-6.7b-act 53.0 -> 52.2 us,
+  // gpt3-6.7b-grad 52.2 -> 51.9, qwen-7b-long 87.9 -> 86.6.
+  const int64_t bpt = 32 / (block / 64);
+  const int64_t rounds = a.nblocks / (static_cast<int64_t>(grid) * (kDecompressThreads / 32) * bpt);
+  const bool claim = fmt == 0 && rounds >= kClaimRounds;
+  void (*kern)(DecompressArgs) = block == 64    ? recompress_fn<64>(variant, fmt, claim)
+                                 : block == 128 ? recompress_fn<128>(variant, fmt, claim)
+                                                : recompress_fn<256>(variant, fmt, claim);
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
   return e != cudaSuccess ? e : cudaGetLastError();
 }

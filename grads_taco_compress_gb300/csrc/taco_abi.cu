@@ -136,6 +136,10 @@ cudaError_t device_info(const DeviceInfo** out) {
           if (err == cudaSuccess)
             err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ_recompress[b][v][f], k,
                                                                 kDecompressThreads, dsmem);
+          // the claimed-tile form of the same launch (E4M3 codes)
+          if (err == cudaSuccess && f == 0)
+            err = cudaFuncSetAttribute(recompress_kernel_ptr(blocks[b], v, f, true),
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, dsmem);
         }
       }
     }

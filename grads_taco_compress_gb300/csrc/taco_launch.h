@@ -127,7 +127,8 @@ inline bool decompress_uses_pw(int mode, int block, int fmt) {
 constexpr int64_t kPwMinBlocksPerCta = 64;
 cudaError_t launch_decompress(const DecompressArgs& a, int block, int fmt, int grid,
                               cudaStream_t stream);
-const void* recompress_kernel_ptr(int block, int variant, int fmt);
+// claim: the form whose warps claim their CTA's tiles in order (E4M3 codes)
+const void* recompress_kernel_ptr(int block, int variant, int fmt, bool claim = false);
 const void* gather_kernel_ptr(int block, int fmt);
 cudaError_t launch_decompress_shards(const DecompressArgs& a, int block, int fmt, int grid, int P,
                                      cudaStream_t stream);
