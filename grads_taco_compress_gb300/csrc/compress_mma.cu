@@ -35,7 +35,8 @@
 //              with 3-D TMA tensor stores, and stores its (alpha, s) pair;
 //              each warp then folds its rows' largest s and count of s > 1
 //              into the CTA's totals for the tile's shard (shared memory);
-//   warp 10    tile scheduler (below).
+//   warp 10    tile scheduler (below); once the pool is dry it also makes the
+//              CTA's per-tensor header arrivals, overlapping the last tiles.
 // Tile schedule: the CTAs of shard y (gridDim.x of them, blockIdx.y == y)
 // take 3/4 of the per-CTA share of that shard's tiles round-robin (tile
 // blockIdx.x + k * gridDim.x), then every CTA claims the rest of all shards'
